@@ -1,0 +1,137 @@
+"""Paged KV cache model: reshape-and-cache writes, block copies, gather.
+
+The pages give only logical shapes for one layer's cache
+("KV Cache优化实战" §1.2: [layers, kv_heads, seq, head_dim];
+"企业官网建设流程全解析" §1.3: [batch, seq, kv_heads, head_dim]).  Paging
+("KV Cache 与 vLLM" (zwxr.cn) §3.1-§3.2) only changes where each token's
+K/V lives: token ``n`` of a sequence sits at slot ``table[n // 16] * 16 +
+n % 16``.  Reading adopted for the physical pool of one layer:
+``[num_blocks, num_kv_heads, block_size, head_dim]``.
+
+Storage types:
+
+* ``f16`` / ``bf16``: the value is stored as is (the inputs are already in
+  that type, so the write is an exact copy);
+* ``fp8_e4m3``: per (token, KV head) -- the finer granularity the pages
+  recommend over one scale per tensor ("KV Cache优化实战" §3.2, §7.3) --
+  ``amax = max |x|`` over head_dim, ``s = amax / 448`` (``1`` when
+  ``amax == 0``), code = E4M3(x / s).  ``s`` and ``x / s`` are IEEE fp32
+  round-to-nearest divisions (reading: the pages give no formula; this is
+  the plain absmax one, fixed so that codes compare bit for bit).  The
+  dequantised value is ``decode(code) * s`` in fp64.
+
+Slots never written hold NaN in this model (fp32 storage) or a NaN code
+(FP8), so that a gather that strays onto one shows up at once.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import fp8
+
+DTYPES = ("f16", "bf16", "fp8_e4m3")
+
+
+def quantize_rows(x: np.ndarray):
+    """Per-row FP8 quantisation of float32 rows ``[..., head_dim]``.
+
+    Returns (codes uint8 [..., head_dim], scale float32 [...]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1)
+    scale = np.where(amax == 0, np.float32(1.0),
+                     amax.astype(np.float32) / np.float32(fp8.MAX_FINITE)).astype(np.float32)
+    y = (x / scale[..., None]).astype(np.float32)
+    return fp8.encode(y), scale
+
+
+class PagedCacheModel:
+    """One layer's K and V pools."""
+
+    def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int,
+                 dtype: str, block_size: int = 16):
+        if dtype not in DTYPES:
+            raise ValueError(f"unknown cache dtype {dtype}")
+        self.num_blocks, self.num_kv_heads, self.head_dim = num_blocks, num_kv_heads, head_dim
+        self.block_size, self.dtype = block_size, dtype
+        shape = (num_blocks, num_kv_heads, block_size, head_dim)
+        if dtype == "fp8_e4m3":
+            self.k = np.full(shape, 0x7F, dtype=np.uint8)
+            self.v = np.full(shape, 0x7F, dtype=np.uint8)
+            self.k_scale = np.full(shape[:3], np.nan, dtype=np.float32)
+            self.v_scale = np.full(shape[:3], np.nan, dtype=np.float32)
+        else:
+            self.k = np.full(shape, np.nan, dtype=np.float32)
+            self.v = np.full(shape, np.nan, dtype=np.float32)
+            self.k_scale = self.v_scale = None
+        # which slots have been written (parity compares filled slots only)
+        self.filled = np.zeros((num_blocks, block_size), dtype=bool)
+
+    def write(self, slot_mapping, k: np.ndarray, v: np.ndarray) -> None:
+        """Reshape-and-cache: token t's K/V ``[num_kv_heads, head_dim]`` to slot_mapping[t].
+
+        A slot of -1 skips the token.
+        """
+        bs = self.block_size
+        for t, slot in enumerate(slot_mapping):
+            slot = int(slot)
+            if slot < 0:
+                continue
+            blk, off = divmod(slot, bs)
+            if blk >= self.num_blocks:
+                raise IndexError(f"slot {slot} outside the pool")
+            if self.dtype == "fp8_e4m3":
+                kc, ks = quantize_rows(k[t])
+                vc, vs = quantize_rows(v[t])
+                self.k[blk, :, off, :] = kc
+                self.v[blk, :, off, :] = vc
+                self.k_scale[blk, :, off] = ks
+                self.v_scale[blk, :, off] = vs
+            else:
+                self.k[blk, :, off, :] = k[t]
+                self.v[blk, :, off, :] = v[t]
+            self.filled[blk, off] = True
+
+    def copy_block(self, src: int, dst: int) -> None:
+        """Copy all slots of a physical block (K, V and scales) for copy-on-write."""
+        self.k[dst] = self.k[src]
+        self.v[dst] = self.v[src]
+        if self.k_scale is not None:
+            self.k_scale[dst] = self.k_scale[src]
+            self.v_scale[dst] = self.v_scale[src]
+        self.filled[dst] = self.filled[src]
+
+    def _dequant(self, codes_or_vals, scales):
+        if self.dtype == "fp8_e4m3":
+            return fp8.decode(codes_or_vals) * scales.astype(np.float64)[..., None]
+        return codes_or_vals.astype(np.float64)
+
+    def gather(self, table, length: int):
+        """Contiguous fp64 K, V ``[length, num_kv_heads, head_dim]`` of one sequence.
+
+        Logical token n lives in physical block table[n // bs] at offset n % bs.
+        """
+        bs = self.block_size
+        pos = np.arange(length)
+        blocks = np.asarray(table, dtype=np.int64)[pos // bs]
+        offs = pos % bs
+        k = self.k[blocks, :, offs, :]          # [L, Hkv, D]
+        v = self.v[blocks, :, offs, :]
+        if self.dtype == "fp8_e4m3":
+            ks = self.k_scale[blocks, :, offs]
+            vs = self.v_scale[blocks, :, offs]
+            return self._dequant(k, ks), self._dequant(v, vs)
+        return k.astype(np.float64), v.astype(np.float64)
+
+
+def dequantize_rows(x: np.ndarray, dtype: str):
+    """fp64 values a cache of ``dtype`` holds for float32 input rows ``[..., head_dim]``.
+
+    The contiguous counterpart of write + gather: what token rows read back
+    as, without the paging.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    if dtype == "fp8_e4m3":
+        codes, s = quantize_rows(x)
+        return fp8.decode(codes) * s.astype(np.float64)[..., None]
+    return x.astype(np.float64)
