@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark: paged decode attention on one GB300 (per GPU; weak scaling under torchrun).
+
+One step = the whole decode hot path for one batch: host block manager
+(append slots + block tables), one metadata upload, copy-on-write block
+copies (when a shared block is appended to), append (reshape-and-cache)
+and attention (partial + log-sum-exp reduce kernels) for every layer.
+Inputs (new K/V rows and queries for every step) are resident in HBM before
+the timed region; between timed steps a 256 MiB buffer is written so the KV
+cache is read from HBM, not L2, and only the steps themselves are timed
+(CUDA events on the launching stream).
+
+Prints one JSON line.  ``--impl reference`` times the CPU fp64 oracle on the
+same workload instead (bounded samples per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_163_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "decode attn KV-read GB/s (% of GB300 HBM peak); seq-tokens/s per layer"
+WORKLOADS = {"tiny": 1, "llama3-8b": 2, "mha7b-40layer": 3, "prefix-share": 4, "long-fp8": 5}
+DEFAULT_WORKLOAD = "llama3-8b"
+SCRUB_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic per decode call (dram__bytes_read.sum + dram__bytes_write.sum, one
+# ncu capture), keyed by workload and by the hash of the decode kernel source it
+# was taken on; reported only while the source is unchanged.
+NCU_TRAFFIC = {}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_163_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Workload accounting
+# ---------------------------------------------------------------------------
+def step_accounting(w: wl.Workload, step: int):
+    """Algorithmic bytes of one attention call and the step's KV bytes / tokens."""
+    lens = w.context_lens + step
+    tokens = int(lens.sum())
+    kv = w.kv_bytes(step)                                      # K + V (+ scales) of all sequences
+    q_bytes = w.num_seqs * w.num_q_heads * w.head_dim * 2
+    table_bytes = int(sum(-(-int(L) // 16) for L in lens)) * 4
+    lens_bytes = w.num_seqs * 4
+    out_bytes = q_bytes
+    return {"tokens": tokens, "kv_bytes": kv,
+            "algo_bytes": kv + q_bytes + table_bytes + lens_bytes + out_bytes,
+            "roofline_bytes": kv + q_bytes + table_bytes + lens_bytes}
+
+
+def workload_config(w: wl.Workload, name: str, extra=None):
+    cfg = {"workload": name, "description": w.description, "num_seqs": w.num_seqs,
+           "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+           "layers": w.num_layers, "q_dtype": w.q_dtype, "cache_dtype": w.cache_dtype, "block_size": 16,
+           "context_tokens": int(w.context_lens.sum()), "max_context_len": w.max_context_len,
+           "seed": w.seed, "l2": "flushed: 256 MiB write between timed steps"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.count(",") >= 9]
+        os.unlink(self.file.name)
+        import datetime as dt
+        samples = []
+        for r in rows:
+            try:
+                ts = dt.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            samples.append((ts, [x.strip() for x in r[1:]]))
+        inside = [s for ts, s in samples if self.t0 is not None and self.t0 - 0.06 <= ts <= self.t1 + 0.06]
+        window = "timed"
+        if not inside:
+            inside = [s for _, s in samples]
+            window = "whole run (timed region shorter than the sampling interval)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in inside for n, v in zip(names, s[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max((float(s[3]) for s in inside if s[3].replace(".", "").isdigit()), default=None)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import torch
+    from paged_kv_cache_163_gb300 import capi, play
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    capi.load()
+    wid = WORKLOADS[args.workload]
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
+    total_steps = args.warmup + args.steps + e2e_steps
+    w = wl.make(wid, extra_steps=max(total_steps, CPU_MAX_STEPS) + 1)
+    cache = play.new_cache(w, device=dev)
+    play.prefill(w, cache, device=dev)
+    torch.cuda.synchronize()
+    assert cache.check() == 0
+
+    # every step's inputs resident in HBM before timing
+    ins = [play.step_inputs(w, s, device=dev) for s in range(args.warmup + args.steps)]
+    out = torch.empty_like(ins[0][2])
+    scrub = torch.empty(SCRUB_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for s in range(args.warmup):
+        k, v, q = ins[s]
+        scrub.fill_(s & 0xFF)
+        cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out)
+    torch.cuda.synchronize()
+    assert cache.check() == 0
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = capi.pkv_launch_count()
+    clocks.mark("t0")
+    for i in range(args.steps):
+        k, v, q = ins[args.warmup + i]
+        scrub.fill_((i + 7) & 0xFF)
+        ev[i][0].record(stream)
+        cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out, marks=marks[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    if world > 1:
+        torch.distributed.barrier()
+    launches = capi.pkv_launch_count() - launches0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_ms = [a.elapsed_time(b) for a, b in marks]
+    assert cache.check() == 0
+
+    steps_acc = [step_accounting(w, args.warmup + i) for i in range(args.steps)]
+    kv_total = sum(a["kv_bytes"] for a in steps_acc) * w.num_layers
+    tok_total = sum(a["tokens"] for a in steps_acc)
+    t_total = sum(step_ms) / 1e3
+    t_attn = sum(attn_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([t_total, t_attn], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_total, t_attn = t.tolist()
+
+    # end to end: inputs from pinned host memory, result read back, every step
+    e2e = None
+    if e2e_steps:
+        e2e = run_e2e(w, cache, e2e_steps, args.warmup + args.steps, dev, scrub)
+
+    peak, peak_kind = measured_peak()
+    per_launch_bytes = statistics.mean(a["roofline_bytes"] for a in steps_acc)
+    per_launch_s = t_attn / (args.steps * w.num_layers)
+    achieved = per_launch_bytes / per_launch_s / 1e9
+    traffic = NCU_TRAFFIC.get((args.workload, kernel_hash()))
+    value = world * kv_total / t_total / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_total * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.cache_dtype if w.cache_dtype != "fp8_e4m3" else "fp8_e4m3 (bf16 q, fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1); no dataset or weights)",
+        "config": workload_config(w, args.workload, {"parallelism": f"replicas x{world} (sequences sharded)"}),
+        "hbm_frac_step": round(value / world / peak, 4),
+        "seq_tokens_per_s_per_layer": round(world * tok_total / (t_total / w.num_layers), 1),
+        "attn_only": {"kv_read_gbs": round(kv_total / t_attn / 1e9, 2),
+                      "ms_per_step": round(t_attn * 1e3 / args.steps, 4)},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel + paged_reduce_kernel (one decode call)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": f"{peak_kind} copy GB/s",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": int(per_launch_bytes),
+                     "launch_us": round(per_launch_s * 1e6, 3)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    cache.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def run_e2e(w, cache, steps, first_step, dev, scrub):
+    """Same metric through the public API with host buffers: H2D inputs and D2H output every step."""
+    import torch
+    from paged_kv_cache_163_gb300 import play
+    hosts = []
+    for s in range(first_step, first_step + steps):
+        k = torch.from_numpy(w.step_rows(0, s)).to(play.torch_dtype(w.q_dtype)).pin_memory()
+        v = torch.from_numpy(w.step_rows(1, s)).to(play.torch_dtype(w.q_dtype)).pin_memory()
+        q = torch.from_numpy(np.stack([w.q_rows(layer, s) for layer in range(w.num_layers)])) \
+            .to(play.torch_dtype(w.q_dtype)).pin_memory()
+        hosts.append((k, v, q))
+    kd = torch.empty(hosts[0][0].shape, dtype=hosts[0][0].dtype, device=dev)
+    vd = torch.empty_like(kd)
+    qd = torch.empty(hosts[0][2].shape, dtype=hosts[0][2].dtype, device=dev)
+    out = torch.empty_like(qd)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    meta_bytes = 0
+    for i, (k, v, q) in enumerate(hosts):
+        scrub.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        kd.copy_(k, non_blocking=True)
+        vd.copy_(v, non_blocking=True)
+        qd.copy_(q, non_blocking=True)
+        cache.step(w.seq_ids, kd, vd, qd, scale=w.scale, out=out)
+        out_h.copy_(out, non_blocking=True)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert cache.check() == 0
+    t = sum(a.elapsed_time(b) for a, b in ev) / 1e3
+    kv = sum(step_accounting(w, first_step + i)["kv_bytes"] for i in range(steps)) * w.num_layers
+    lens = w.context_lens + first_step
+    max_blocks = int(max(-(-int(L) // 16) for L in lens))
+    meta_bytes = 4 * (w.num_seqs + w.num_seqs * max_blocks + w.num_seqs)
+    h2d = sum(x.numel() * x.element_size() for x in hosts[0]) + meta_bytes
+    return {"value": round(kv / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()), "steps": steps,
+            "ms_per_step": round(t * 1e3 / steps, 4)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm
+# ---------------------------------------------------------------------------
+CPU_MAX_STEPS = 400
+
+
+def oracle_sample_state(w: wl.Workload, seqs, max_steps=CPU_MAX_STEPS):
+    """Oracle allocator + paged cache pre-filled for the sampled sequences (setup, untimed)."""
+    from oracle.model import PagedKVOracle
+    need = sum(-(-int(w.context_lens[s] + max_steps + 1) // 16) for s in seqs) + 8
+    o = PagedKVOracle(1, need, w.num_kv_heads, w.head_dim, w.cache_dtype)
+    for s in seqs:
+        o.create(s)
+        L = int(w.context_lens[s]) - 1
+        if L > 0:
+            o.append([s] * L, [w.kv_rows(0, s, 0, L)], [w.kv_rows(1, s, 0, L)])
+    return o
+
+
+def oracle_steps(w, o, seqs, step0, budget_s, max_steps=None):
+    """Timed oracle decode steps (append + attention) over the sampled sequences."""
+    t_total, n, kv, toks = 0.0, 0, 0, 0
+    step = step0
+    while (t_total < budget_s and (max_steps is None or n < max_steps)) or n == 0:
+        k = np.stack([w.kv_rows(0, s, int(w.context_lens[s]) - 1 + step, int(w.context_lens[s]) + step)[0]
+                      for s in seqs])
+        v = np.stack([w.kv_rows(1, s, int(w.context_lens[s]) - 1 + step, int(w.context_lens[s]) + step)[0]
+                      for s in seqs])
+        q = w.q_rows(0, step)[list(seqs)]
+        t0 = time.perf_counter()
+        o.append(list(seqs), [k], [v])
+        o.decode(list(seqs), q, w.scale)
+        t_total += time.perf_counter() - t0
+        lens = [int(w.context_lens[s]) + step for s in seqs]
+        per_tok = w.num_kv_heads * (w.head_dim + 4 if w.cache_dtype == "fp8_e4m3" else 2 * w.head_dim)
+        kv += 2 * sum(lens) * per_tok
+        toks += sum(lens)
+        n += 1
+        step += 1
+    return t_total, n, kv, toks
+
+
+def sample_seqs(w, budget_tokens):
+    order = np.argsort(w.context_lens)[::-1]
+    seqs, tot = [], 0
+    for s in order[len(order) // 2:].tolist() + order[:len(order) // 2].tolist():
+        if tot > 0 and tot + w.context_lens[s] > budget_tokens:
+            continue
+        seqs.append(int(s))
+        tot += int(w.context_lens[s])
+        if tot >= budget_tokens:
+            break
+    return sorted(seqs)
+
+
+def cpu_baseline(w, budget_s):
+    seqs = sample_seqs(w, 6000 if w.cache_dtype != "fp8_e4m3" else 20000)
+    o = oracle_sample_state(w, seqs)
+    t, n, kv, toks = oracle_steps(w, o, seqs, 0, budget_s, max_steps=CPU_MAX_STEPS)
+    return {"value": round(kv / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seq_tokens_per_s_per_layer": round(toks / t, 1),
+            "sample": f"{n} oracle decode steps (append + fp64 attention, layer 0) over sequences {seqs} "
+                      f"of {len(w.context_lens)} ({toks // max(n, 1)} context tokens per step), "
+                      f"{t:.1f} s on 1 host core (BLAS threads = 1)"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    wid = WORKLOADS[args.workload]
+    w = wl.make(wid, extra_steps=max(args.warmup + args.steps + 1, CPU_MAX_STEPS + 1))
+    seqs = sample_seqs(w, 3000 if w.cache_dtype != "fp8_e4m3" else 17000)
+    o = oracle_sample_state(w, seqs, max_steps=args.warmup + args.steps + 1)
+    oracle_steps(w, o, seqs, 0, 0.0, max_steps=args.warmup)
+    t, n, kv, toks = oracle_steps(w, o, seqs, args.warmup, float("inf"), max_steps=args.steps)
+    value = kv / t / 1e9
+    peak, peak_kind = measured_peak()
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3 / n, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded N(0,1); no dataset or weights)",
+        "config": workload_config(w, args.workload, {"parallelism": "single host process"}),
+        "seq_tokens_per_s_per_layer": round(toks / t, 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: oracle append + fp64 attention over sequences {seqs} "
+                                   f"of {len(w.context_lens)}, layer 0"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local)
+    if res is not None and rank == 0:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

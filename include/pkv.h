@@ -1,0 +1,221 @@
+/*
+ * pkv.h -- C ABI of the GB300 paged KV cache decode library (libpkv.so).
+ *
+ * The calls follow the pages' statement of the problem ("KV Cache 与 vLLM"
+ * (zwxr.cn) §3.1-§3.4; "KV Cache优化实战" §4.2): the KV cache is cut into
+ * fixed physical blocks of 16 tokens, taken on demand; each sequence keeps a
+ * block table (logical block -> physical block); sequences with a common
+ * prefix share physical blocks and copy a shared block on write; a finished
+ * sequence's blocks are freed at once; every decode step appends the new
+ * token's K/V and the new query attends over the sequence's cache through
+ * its table.  Running out of blocks must not crash a request
+ * ("企业官网建设流程全解析" §6.4): the allocator fails the whole request with
+ * PKV_ERR_NO_BLOCKS and changes nothing.
+ *
+ * Conventions shared by every call:
+ *  - Every call returns a pkv_status.  Host calls validate their arguments and
+ *    leave all state unchanged on error.  pkv_last_error() gives a one-line
+ *    reason for the calling thread's last failure.
+ *  - Device calls take device pointers owned by the caller (the library never
+ *    allocates device memory), enqueue kernels on `stream` and do not
+ *    synchronise.  Launch errors are returned at once; errors that depend on
+ *    device data (a slot or block id outside the pool, a context length
+ *    beyond the table) are OR-ed into the caller's device word `d_error`
+ *    (int32, may be NULL) as PKV_DEVERR_* bits and read back with
+ *    pkv_read_device_error().  A kernel that finds such an error skips the
+ *    offending access; it never traps.
+ *  - Device arrays are dense and row-major in the shapes stated, and every
+ *    device pointer must be 16-byte aligned.
+ *  - Cache layout, per layer: k_cache, v_cache [num_blocks][num_kv_heads][16][head_dim];
+ *    FP8 scales k_scale, v_scale float32 [num_blocks][num_kv_heads][16].
+ *    Token n of a sequence lives at slot table[n / 16] * 16 + n % 16.
+ *  - Several layers are several calls with per-layer cache pointers.
+ *  - Not thread-safe per block manager handle.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID = -1,      /* bad argument, unknown sequence or block, misaligned pointer */
+  PKV_ERR_NO_BLOCKS = -2,    /* the free list cannot cover the request; nothing changed */
+  PKV_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
+  PKV_ERR_UNSUPPORTED = -4,  /* head_dim / group size / dtype combination not built */
+  PKV_ERR_DEVICE_CHECK = -5, /* pkv_read_device_error found a PKV_DEVERR_* bit set */
+  PKV_ERR_WORKSPACE = -6     /* workspace smaller than paged_attention_workspace_bytes */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2, PKV_F32 = 3 } pkv_dtype;
+
+/* Bits a kernel ORs into *d_error. */
+#define PKV_DEVERR_BAD_SLOT 1        /* append: slot >= num_blocks * 16 */
+#define PKV_DEVERR_BAD_BLOCK 2       /* copy / decode: block id outside [0, num_blocks) */
+#define PKV_DEVERR_BAD_CONTEXT_LEN 4 /* decode: context_len < 0 or > max_blocks_per_seq * 16 */
+#define PKV_DEVERR_WAIT_TIMEOUT 8    /* decode: a staging wait ran out its iteration limit */
+
+#define PKV_BLOCK_SIZE 16
+#define PKV_MAX_SEQS_PER_CALL 1024   /* paged_attention_decode batch limit */
+
+/* ------------------------------------------------------------------------ */
+/* Host block manager (pages: "KV Cache 与 vLLM" §3.1-§3.4).                  */
+/*                                                                          */
+/* Free list: FIFO, initialised to alloc_order (NULL = 0..num_blocks-1); a  */
+/* block is taken from the head and returned to the tail.  A block is       */
+/* shared while its reference count exceeds 1.                              */
+/* ------------------------------------------------------------------------ */
+typedef struct pkv_bm pkv_bm;
+
+/* num_blocks > 0; block_size must be 16; alloc_order (may be NULL) is a
+ * permutation of 0..num_blocks-1 copied by the call.  *out owns host memory
+ * released by pkv_bm_destroy. */
+pkv_status pkv_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *alloc_order,
+                         pkv_bm **out);
+void pkv_bm_destroy(pkv_bm *bm);
+
+/* Take one block from the free list (its count becomes 1). */
+pkv_status kv_block_alloc(pkv_bm *bm, int32_t *block_id);
+/* Drop one reference; at 0 the block joins the tail of the free list. */
+pkv_status kv_block_free(pkv_bm *bm, int32_t block_id);
+
+/* New empty sequence; seq_id must not exist. */
+pkv_status pkv_seq_create(pkv_bm *bm, int64_t seq_id);
+/* child gets a copy of parent's table and length; every block gains one
+ * reference (prefix sharing, "KV Cache 与 vLLM" §3.3). */
+pkv_status pkv_seq_fork(pkv_bm *bm, int64_t parent, int64_t child);
+/* Drop the sequence's references in logical order (freed blocks join the
+ * free list in that order) and forget the sequence. */
+pkv_status pkv_seq_free(pkv_bm *bm, int64_t seq_id);
+
+/* Append one token to each seq_ids[i], in order (a sequence may repeat).
+ * For a sequence of length n: if n % 16 == 0 a block is taken from the free
+ * list and added to its table; else if its last block is shared, a new block
+ * is taken, the pair (old -> new) is recorded in cow_src/cow_dst and the old
+ * block loses one reference (copy-on-write; the last holder writes in place).
+ * slot_mapping[i] = table[n / 16] * 16 + n % 16, then n becomes n + 1.
+ * Arrays: seq_ids[n], slot_mapping[n], cow_src[n], cow_dst[n] (host memory);
+ * *num_cow receives the number of pairs.  All-or-nothing: returns
+ * PKV_ERR_NO_BLOCKS, with nothing changed, when the free list cannot cover
+ * every block the batch needs. The caller must copy each pair (old -> new)
+ * with paged_kv_copy_blocks before writing the new tokens. */
+pkv_status pkv_seq_append_slots(pkv_bm *bm, const int64_t *seq_ids, int32_t n,
+                                int32_t *slot_mapping, int32_t *cow_src, int32_t *cow_dst,
+                                int32_t *num_cow);
+
+/* Export block tables: tables[i][j] = physical block of logical block j of
+ * seq_ids[i], -1 past the end (host int32 [n][max_blocks]); context_lens[i]
+ * = its token count (host int32 [n]).  PKV_ERR_INVALID if a table is longer
+ * than max_blocks. */
+pkv_status pkv_build_block_tables(const pkv_bm *bm, const int64_t *seq_ids, int32_t n,
+                                  int32_t max_blocks, int32_t *tables, int32_t *context_lens);
+
+int32_t pkv_bm_num_free(const pkv_bm *bm);
+int32_t pkv_bm_num_blocks(const pkv_bm *bm);
+/* The free list in FIFO order: writes min(cap, free) ids to out, *n = free. */
+pkv_status pkv_bm_free_list(const pkv_bm *bm, int32_t *out, int32_t cap, int32_t *n);
+pkv_status pkv_bm_refcount(const pkv_bm *bm, int32_t block_id, int32_t *count);
+pkv_status pkv_seq_len(const pkv_bm *bm, int64_t seq_id, int32_t *len);
+
+/* ------------------------------------------------------------------------ */
+/* Sizing ("KV Cache优化实战" §2.1: bytes = 2 x layers x kv_heads x head_dim */
+/* x tokens x bytes per element).  FP8 adds one fp32 scale per (token, KV   */
+/* head) for K and for V.  Returns -1 on a bad argument.                     */
+/* ------------------------------------------------------------------------ */
+int64_t pkv_kv_bytes(int32_t layers, int32_t kv_heads, int32_t head_dim, int64_t tokens,
+                     pkv_dtype cache_dtype);
+/* Whole blocks a byte budget buys for all layers' K, V (and scales). */
+int64_t pkv_pool_blocks(int64_t budget_bytes, int32_t layers, int32_t kv_heads, int32_t head_dim,
+                        pkv_dtype cache_dtype);
+
+/* ------------------------------------------------------------------------ */
+/* Device calls                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Copy-on-write block copy ("KV Cache 与 vLLM" §3.3): for each pair i, copy
+ * all 16 slots of physical block src[i] to dst[i] in k_cache and v_cache
+ * (and k_scale / v_scale when cache_dtype is FP8; NULL otherwise).
+ * src, dst: device int32 [num_pairs]; ids outside [0, num_blocks) set
+ * PKV_DEVERR_BAD_BLOCK and that pair is skipped. */
+pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                                const int32_t *src, const int32_t *dst, int32_t num_pairs,
+                                int32_t num_kv_heads, int32_t head_dim, pkv_dtype cache_dtype,
+                                int32_t num_blocks, int32_t *d_error, pkv_stream_t stream);
+
+/* Reshape-and-cache ("KV Cache 与 vLLM" §1.3 append; "企业官网建设流程全解析"
+ * §3.2): token t's rows k[t], v[t] ([num_kv_heads][head_dim], in_dtype
+ * F16 or BF16) are written to slot slot_mapping[t] (device int32
+ * [num_tokens]; -1 skips the token; >= num_blocks * 16 sets
+ * PKV_DEVERR_BAD_SLOT and skips it).
+ * 16-bit caches: cache_dtype must equal in_dtype; the copy is exact.
+ * FP8 E4M3 cache ("KV Cache优化实战" §3.2-§3.3, per-token per-head scale):
+ * per (token, KV head) amax = max |x| over head_dim, scale = amax / 448 in
+ * IEEE fp32 (1 when amax == 0), code = E4M3(x / scale) with an IEEE fp32
+ * division, round to nearest even, saturating to +-448; scale goes to
+ * k_scale / v_scale at the same slot. */
+pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int32_t num_tokens,
+                           int32_t num_kv_heads, int32_t head_dim, const int32_t *slot_mapping,
+                           void *k_cache, void *v_cache, pkv_dtype cache_dtype, float *k_scale,
+                           float *v_scale, int32_t num_blocks, int32_t *d_error,
+                           pkv_stream_t stream);
+
+/* Device workspace (bytes) paged_attention_decode needs for these shapes on
+ * the current device (split-KV partials).  Depends on the device's SM count. */
+pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           pkv_dtype q_dtype, pkv_dtype cache_dtype,
+                                           size_t *bytes);
+
+/* PagedAttention decode ("企业官网建设流程全解析" §1.2: softmax(q K^T * scale)
+ * V; "KV Cache 与 vLLM" §3.2: through the block table, reading only the
+ * sequence's blocks).  For sequence b and query head h, with G =
+ * num_q_heads / num_kv_heads and KV head h / G:
+ *   out[b][h] = sum_j softmax_j(scale * <q[b][h], K_j>) V_j
+ * over tokens j < context_lens[b] (the token appended this step included).
+ * q: [num_seqs][num_q_heads][head_dim] in q_dtype (F16 / BF16); out: same
+ * shape in out_dtype, either F32 (the fp32 accumulator result) or q_dtype
+ * (that result rounded once to nearest even).  Caches F16 or BF16 (q_dtype must match) or
+ * FP8_E4M3 (dequantised in the kernel with k_scale / v_scale).
+ * block_tables: device int32 [num_seqs][max_blocks_per_seq]; context_lens:
+ * device int32 [num_seqs]; max_context_len bounds every context_len.
+ * A context_len of 0 gives a zero output.  Work is split across the GPU
+ * in equal shares of (sequence, KV head, 16-token block) tiles; shares that
+ * cover part of a sequence leave fp32 partials in `workspace` (at least
+ * paged_attention_workspace_bytes) merged by a log-sum-exp reduce kernel.
+ * Supported: head_dim 64 or 128; G in {1, 2, 4, 8}; num_seqs <=
+ * PKV_MAX_SEQS_PER_CALL. */
+pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                  const void *k_cache,
+                                  const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
+                                  const float *v_scale, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                  int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                                  float scale, void *workspace, size_t workspace_bytes,
+                                  int32_t *d_error, pkv_stream_t stream);
+
+/* Synchronise `stream`, copy *d_error to *h_error and, if clear != 0, zero
+ * it.  Returns PKV_ERR_DEVICE_CHECK when any bit was set. */
+pkv_status pkv_read_device_error(int32_t *d_error, int32_t *h_error, int32_t clear,
+                                 pkv_stream_t stream);
+
+/* Number of kernel launches the calling thread has made through this
+ * library (for launch accounting). */
+int64_t pkv_launch_count(void);
+
+const char *pkv_status_string(pkv_status status);
+/* One-line reason for the calling thread's last failing call ("" if none). */
+const char *pkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

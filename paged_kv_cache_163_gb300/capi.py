@@ -1,0 +1,308 @@
+"""ctypes binding of libpkv.so: the C ABI's calls under the same names.
+
+Argument marshalling only: host arrays become pointers, torch tensors give
+their device pointers, shapes and dtypes are read off the tensors.  Every
+non-OK status raises ``PkvError`` (``NoBlocksError`` for PKV_ERR_NO_BLOCKS)
+with the library's one-line reason.  The library is loaded on first use; if
+it has not been built the first call raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32 = 0, 1, 2, 3
+DTYPE_NAMES = {"f16": PKV_F16, "bf16": PKV_BF16, "fp8_e4m3": PKV_FP8_E4M3, "f32": PKV_F32}
+BLOCK_SIZE = 16
+MAX_SEQS_PER_CALL = 1024
+DEVERR_BAD_SLOT, DEVERR_BAD_BLOCK, DEVERR_BAD_CONTEXT_LEN, DEVERR_WAIT_TIMEOUT = 1, 2, 4, 8
+
+STATUS = {0: "PKV_OK", -1: "PKV_ERR_INVALID", -2: "PKV_ERR_NO_BLOCKS", -3: "PKV_ERR_CUDA",
+          -4: "PKV_ERR_UNSUPPORTED", -5: "PKV_ERR_DEVICE_CHECK", -6: "PKV_ERR_WORKSPACE"}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str, reason: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {reason}")
+        self.status = status
+
+
+class NoBlocksError(PkvError):
+    pass
+
+
+_lib = None
+_i32p = C.POINTER(C.c_int32)
+_i64p = C.POINTER(C.c_int64)
+_vp = C.c_void_p
+
+# name: (restype, argtypes)
+_PROTOS = {
+    "pkv_bm_create": (C.c_int, [C.c_int32, C.c_int32, _i32p, C.POINTER(_vp)]),
+    "pkv_bm_destroy": (None, [_vp]),
+    "kv_block_alloc": (C.c_int, [_vp, _i32p]),
+    "kv_block_free": (C.c_int, [_vp, C.c_int32]),
+    "pkv_seq_create": (C.c_int, [_vp, C.c_int64]),
+    "pkv_seq_fork": (C.c_int, [_vp, C.c_int64, C.c_int64]),
+    "pkv_seq_free": (C.c_int, [_vp, C.c_int64]),
+    "pkv_seq_append_slots": (C.c_int, [_vp, _i64p, C.c_int32, _i32p, _i32p, _i32p, _i32p]),
+    "pkv_build_block_tables": (C.c_int, [_vp, _i64p, C.c_int32, C.c_int32, _i32p, _i32p]),
+    "pkv_bm_num_free": (C.c_int32, [_vp]),
+    "pkv_bm_num_blocks": (C.c_int32, [_vp]),
+    "pkv_bm_free_list": (C.c_int, [_vp, _i32p, C.c_int32, _i32p]),
+    "pkv_bm_refcount": (C.c_int, [_vp, C.c_int32, _i32p]),
+    "pkv_seq_len": (C.c_int, [_vp, C.c_int64, _i32p]),
+    "pkv_kv_bytes": (C.c_int64, [C.c_int32, C.c_int32, C.c_int32, C.c_int64, C.c_int]),
+    "pkv_pool_blocks": (C.c_int64, [C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int]),
+    "paged_kv_copy_blocks": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32,
+                                       C.c_int, C.c_int32, _vp, _vp]),
+    "paged_kv_append": (C.c_int, [_vp, _vp, C.c_int, C.c_int32, C.c_int32, C.c_int32, _vp, _vp, _vp,
+                                  C.c_int, _vp, _vp, C.c_int32, _vp, _vp]),
+    "paged_attention_workspace_bytes": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int,
+                                                  C.c_int, C.POINTER(C.c_size_t)]),
+    "paged_attention_decode": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, C.c_int, _vp, _vp, _vp, C.c_int32,
+                                         _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                         C.c_int32, C.c_float, _vp, C.c_size_t, _vp, _vp]),
+    "pkv_read_device_error": (C.c_int, [_vp, _i32p, C.c_int32, _vp]),
+    "pkv_launch_count": (C.c_int64, []),
+    "pkv_status_string": (C.c_char_p, [C.c_int]),
+    "pkv_last_error": (C.c_char_p, []),
+}
+
+
+def load(path: str = LIB_PATH):
+    """Load libpkv.so once; raises if it is missing (build it first)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m paged_kv_cache_163_gb300.build` (no fallback path exists)")
+        lib = C.CDLL(path)
+        for name, (res, args) in _PROTOS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def declared_symbols():
+    return list(_PROTOS)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        reason = load().pkv_last_error().decode(errors="replace")
+        cls = NoBlocksError if status == -2 else PkvError
+        raise cls(status, where, reason)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _i64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(C.POINTER(ctype))
+
+
+# ---- host block manager -------------------------------------------------------
+def pkv_bm_create(num_blocks: int, block_size: int = BLOCK_SIZE, alloc_order=None):
+    h = _vp()
+    order = None if alloc_order is None else _i32(alloc_order)
+    if order is not None and len(order) != num_blocks:
+        raise PkvError(-1, "pkv_bm_create", "alloc_order must have num_blocks entries")
+    _check(load().pkv_bm_create(num_blocks, block_size, None if order is None else _ptr(order, C.c_int32),
+                                C.byref(h)), "pkv_bm_create")
+    return h
+
+
+def pkv_bm_destroy(bm) -> None:
+    load().pkv_bm_destroy(bm)
+
+
+def kv_block_alloc(bm) -> int:
+    out = C.c_int32()
+    _check(load().kv_block_alloc(bm, C.byref(out)), "kv_block_alloc")
+    return out.value
+
+
+def kv_block_free(bm, block_id: int) -> None:
+    _check(load().kv_block_free(bm, block_id), "kv_block_free")
+
+
+def pkv_seq_create(bm, seq_id: int) -> None:
+    _check(load().pkv_seq_create(bm, seq_id), "pkv_seq_create")
+
+
+def pkv_seq_fork(bm, parent: int, child: int) -> None:
+    _check(load().pkv_seq_fork(bm, parent, child), "pkv_seq_fork")
+
+
+def pkv_seq_free(bm, seq_id: int) -> None:
+    _check(load().pkv_seq_free(bm, seq_id), "pkv_seq_free")
+
+
+def pkv_seq_append_slots(bm, seq_ids):
+    """Returns (slot_mapping int32[n], cow_src int32[k], cow_dst int32[k])."""
+    ids = _i64(seq_ids)
+    n = len(ids)
+    slots = np.empty(n, np.int32)
+    src = np.empty(max(n, 1), np.int32)
+    dst = np.empty(max(n, 1), np.int32)
+    ncow = C.c_int32()
+    _check(load().pkv_seq_append_slots(bm, _ptr(ids, C.c_int64), n, _ptr(slots, C.c_int32),
+                                       _ptr(src, C.c_int32), _ptr(dst, C.c_int32), C.byref(ncow)),
+           "pkv_seq_append_slots")
+    return slots, src[:ncow.value].copy(), dst[:ncow.value].copy()
+
+
+def pkv_build_block_tables(bm, seq_ids, max_blocks: int, tables=None, context_lens=None):
+    """Returns (tables int32[n, max_blocks] padded with -1, context_lens int32[n]).
+
+    ``tables`` / ``context_lens`` may be preallocated C-contiguous int32 arrays.
+    """
+    ids = _i64(seq_ids)
+    n = len(ids)
+    if tables is None:
+        tables = np.empty((n, max_blocks), np.int32)
+    if context_lens is None:
+        context_lens = np.empty(n, np.int32)
+    assert tables.dtype == np.int32 and tables.flags.c_contiguous and tables.size >= n * max_blocks
+    assert context_lens.dtype == np.int32 and context_lens.flags.c_contiguous and context_lens.size >= n
+    _check(load().pkv_build_block_tables(bm, _ptr(ids, C.c_int64), n, max_blocks, _ptr(tables, C.c_int32),
+                                         _ptr(context_lens, C.c_int32)), "pkv_build_block_tables")
+    return tables, context_lens
+
+
+def pkv_bm_num_free(bm) -> int:
+    return int(load().pkv_bm_num_free(bm))
+
+
+def pkv_bm_num_blocks(bm) -> int:
+    return int(load().pkv_bm_num_blocks(bm))
+
+
+def pkv_bm_free_list(bm) -> np.ndarray:
+    n = C.c_int32()
+    _check(load().pkv_bm_free_list(bm, None, 0, C.byref(n)), "pkv_bm_free_list")
+    out = np.empty(max(n.value, 1), np.int32)
+    _check(load().pkv_bm_free_list(bm, _ptr(out, C.c_int32), n.value, C.byref(n)), "pkv_bm_free_list")
+    return out[:n.value].copy()
+
+
+def pkv_bm_refcount(bm, block_id: int) -> int:
+    out = C.c_int32()
+    _check(load().pkv_bm_refcount(bm, block_id, C.byref(out)), "pkv_bm_refcount")
+    return out.value
+
+
+def pkv_seq_len(bm, seq_id: int) -> int:
+    out = C.c_int32()
+    _check(load().pkv_seq_len(bm, seq_id, C.byref(out)), "pkv_seq_len")
+    return out.value
+
+
+def pkv_kv_bytes(layers, kv_heads, head_dim, tokens, cache_dtype) -> int:
+    return int(load().pkv_kv_bytes(layers, kv_heads, head_dim, tokens, _dt(cache_dtype)))
+
+
+def pkv_pool_blocks(budget_bytes, layers, kv_heads, head_dim, cache_dtype) -> int:
+    return int(load().pkv_pool_blocks(budget_bytes, layers, kv_heads, head_dim, _dt(cache_dtype)))
+
+
+# ---- device calls --------------------------------------------------------------
+def _dt(x) -> int:
+    """pkv_dtype of a name ('bf16'), an int, or a torch dtype."""
+    if isinstance(x, int):
+        return x
+    if isinstance(x, str):
+        return DTYPE_NAMES[x]
+    import torch
+    m = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.uint8: PKV_FP8_E4M3, torch.float32: PKV_F32}
+    if hasattr(torch, "float8_e4m3fn"):
+        m[torch.float8_e4m3fn] = PKV_FP8_E4M3
+    return m[x]
+
+
+def _dp(t):
+    """Device pointer of a tensor (or None / an int address)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def paged_kv_copy_blocks(k_cache, v_cache, k_scale, v_scale, src, dst, num_pairs=None,
+                         d_error=None, stream=None) -> None:
+    nb, hkv, bs, d = k_cache.shape
+    n = src.numel() if num_pairs is None else num_pairs
+    _check(load().paged_kv_copy_blocks(_dp(k_cache), _dp(v_cache), _dp(k_scale), _dp(v_scale), _dp(src),
+                                       _dp(dst), n, hkv, d, _dt(k_cache.dtype), nb, _dp(d_error),
+                                       _stream(stream)), "paged_kv_copy_blocks")
+
+
+def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None,
+                    d_error=None, stream=None) -> None:
+    t, hkv, d = k.shape
+    nb = k_cache.shape[0]
+    _check(load().paged_kv_append(_dp(k), _dp(v), _dt(k.dtype), t, hkv, d, _dp(slot_mapping), _dp(k_cache),
+                                  _dp(v_cache), _dt(k_cache.dtype), _dp(k_scale), _dp(v_scale), nb,
+                                  _dp(d_error), _stream(stream)), "paged_kv_append")
+
+
+def paged_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, q_dtype,
+                                    cache_dtype) -> int:
+    out = C.c_size_t()
+    _check(load().paged_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, _dt(q_dtype),
+                                                  _dt(cache_dtype), C.byref(out)),
+           "paged_attention_workspace_bytes")
+    return out.value
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                           max_context_len, scale, workspace, d_error=None, stream=None,
+                           num_seqs=None) -> None:
+    b, hq, d = q.shape
+    if num_seqs is not None:
+        b = num_seqs
+    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    _check(load().paged_attention_decode(
+        _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_cache), _dp(v_cache), _dt(k_cache.dtype), _dp(k_scale),
+        _dp(v_scale), _dp(block_tables), block_tables.shape[-1], _dp(context_lens), int(max_context_len), b, hq,
+        hkv, d, nb, float(scale), _dp(workspace), workspace.numel() * workspace.element_size(),
+        _dp(d_error), _stream(stream)), "paged_attention_decode")
+
+
+def pkv_read_device_error(d_error, clear: bool = True, stream=None, raise_on_error: bool = False) -> int:
+    h = C.c_int32()
+    st = load().pkv_read_device_error(_dp(d_error), C.byref(h), 1 if clear else 0, _stream(stream))
+    if st != -5 or raise_on_error:
+        _check(st, "pkv_read_device_error")
+    return h.value
+
+
+def pkv_launch_count() -> int:
+    return int(load().pkv_launch_count())
+
+
+def pkv_status_string(status: int) -> str:
+    return load().pkv_status_string(status).decode()

@@ -1,0 +1,151 @@
+// Reshape-and-cache (append) and copy-on-write block copy kernels.
+//
+// Append ("KV Cache 与 vLLM" (zwxr.cn) §1.3, "企业官网建设流程全解析" §3.2):
+// every decode step writes the new token's K and V rows into the slot the
+// block manager gave it.  With an FP8 E4M3 cache ("KV Cache优化实战"
+// §3.2-§3.3) each (token, KV head) row is quantised with its own scale,
+// amax / 448, using IEEE fp32 divisions so the codes are reproducible.
+//
+// Copy ("KV Cache 与 vLLM" §3.3): a shared block that must change is
+// copied whole to a fresh block before the new token lands in it.
+#include "append.h"
+#include "common.cuh"
+
+namespace pkv {
+
+// One warp per (token, KV head, K-or-V) row.  Row = head_dim elements of
+// 16-bit input; lane i handles elements [i * D/32, (i + 1) * D/32).
+template <int D, int IDT, int CDT>
+__global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__ k,
+                                                     const uint8_t *__restrict__ v,
+                                                     const int32_t *__restrict__ slot_mapping,
+                                                     int32_t num_tokens, int32_t num_kv_heads,
+                                                     uint8_t *__restrict__ k_cache,
+                                                     uint8_t *__restrict__ v_cache,
+                                                     float *__restrict__ k_scale,
+                                                     float *__restrict__ v_scale,
+                                                     int32_t num_blocks, int32_t *err) {
+  constexpr int EPL = D / 32;  // elements per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads * 2;
+  if (gw >= rows) return;
+  const int kind = static_cast<int>(gw & 1);
+  const int64_t th = gw >> 1;  // token * num_kv_heads + head
+  const int64_t t = th / num_kv_heads;
+  const int h = static_cast<int>(th - t * num_kv_heads);
+  const int32_t slot = slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= static_cast<int64_t>(num_blocks) * kBS) {
+    if (lane == 0) report(err, PKV_DEVERR_BAD_SLOT);
+    return;
+  }
+  const int64_t blk = slot / kBS;
+  const int off = slot % kBS;
+  const int64_t row = (blk * num_kv_heads + h) * kBS + off;  // index of the cache row
+  const uint8_t *src = (kind ? v : k) + th * D * 2 + lane * EPL * 2;
+
+  if constexpr (CDT != PKV_FP8_E4M3) {
+    uint8_t *dst = (kind ? v_cache : k_cache) + row * D * 2 + lane * EPL * 2;
+    if constexpr (EPL * 2 == 8) {
+      *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(src);
+    } else {
+      *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(src);
+    }
+  } else {
+    float x[EPL];
+    unpack_row<IDT, EPL * 2>(src, x);
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2) {
+      float2 y = make_float2(__fdiv_rn(x[e], s), __fdiv_rn(x[e + 1], s));
+      uint32_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);  // y.x -> low byte
+      packed |= c2 << (8 * e);
+    }
+    uint8_t *dst = (kind ? v_cache : k_cache) + row * D + lane * EPL;
+    if constexpr (EPL == 4) {
+      *reinterpret_cast<uint32_t *>(dst) = packed;
+    } else {
+      *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
+    }
+    if (lane == 0) (kind ? v_scale : k_scale)[row] = s;
+  }
+}
+
+// One CTA per (pair, K-or-V): copies a whole physical block (all heads, all
+// 16 slots) and, for FP8, its scales.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t *k_cache, uint8_t *v_cache,
+                                                          float *k_scale, float *v_scale,
+                                                          const int32_t *__restrict__ src,
+                                                          const int32_t *__restrict__ dst,
+                                                          int64_t block_bytes, int32_t scale_elems,
+                                                          int32_t num_blocks, int32_t *err) {
+  const int pair = blockIdx.x;
+  const int kind = blockIdx.y;
+  const int32_t s = src[pair];
+  const int32_t d = dst[pair];
+  if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+    if (threadIdx.x == 0 && kind == 0) report(err, PKV_DEVERR_BAD_BLOCK);
+    return;
+  }
+  uint8_t *base = kind ? v_cache : k_cache;
+  const uint4 *sp = reinterpret_cast<const uint4 *>(base + s * block_bytes);
+  uint4 *dp = reinterpret_cast<uint4 *>(base + d * block_bytes);
+  const int64_t n16 = block_bytes / 16;
+  for (int64_t i = threadIdx.x; i < n16; i += blockDim.x) dp[i] = sp[i];
+  float *sc = kind ? v_scale : k_scale;
+  if (sc) {
+    for (int i = threadIdx.x; i < scale_elems; i += blockDim.x)
+      sc[static_cast<int64_t>(d) * scale_elems + i] = sc[static_cast<int64_t>(s) * scale_elems + i];
+  }
+}
+
+template <int D, int IDT, int CDT>
+static cudaError_t launch_append(const AppendArgs &a) {
+  const int64_t rows = static_cast<int64_t>(a.num_tokens) * a.num_kv_heads * 2;
+  const int64_t threads = rows * 32;
+  const int64_t blocks = (threads + 255) / 256;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  append_kernel<D, IDT, CDT><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
+      static_cast<const uint8_t *>(a.k), static_cast<const uint8_t *>(a.v), a.slot_mapping,
+      a.num_tokens, a.num_kv_heads, static_cast<uint8_t *>(a.k_cache),
+      static_cast<uint8_t *>(a.v_cache), a.k_scale, a.v_scale, a.num_blocks, a.d_error);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t dispatch_append_d(const AppendArgs &a) {
+  if (a.cache_dtype == PKV_FP8_E4M3) {
+    return a.in_dtype == PKV_BF16 ? launch_append<D, PKV_BF16, PKV_FP8_E4M3>(a)
+                                  : launch_append<D, PKV_F16, PKV_FP8_E4M3>(a);
+  }
+  return a.cache_dtype == PKV_BF16 ? launch_append<D, PKV_BF16, PKV_BF16>(a)
+                                   : launch_append<D, PKV_F16, PKV_F16>(a);
+}
+
+cudaError_t run_append(const AppendArgs &a) {
+  if (a.num_tokens == 0) return cudaSuccess;
+  return a.head_dim == 128 ? dispatch_append_d<128>(a) : dispatch_append_d<64>(a);
+}
+
+cudaError_t run_copy_blocks(const CopyArgs &a) {
+  if (a.num_pairs == 0) return cudaSuccess;
+  const int esz = a.cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
+  const int64_t block_bytes = static_cast<int64_t>(a.num_kv_heads) * kBS * a.head_dim * esz;
+  const int32_t scale_elems = a.num_kv_heads * kBS;
+  dim3 grid(a.num_pairs, 2);
+  copy_blocks_kernel<<<grid, 256, 0, a.stream>>>(
+      static_cast<uint8_t *>(a.k_cache), static_cast<uint8_t *>(a.v_cache),
+      a.cache_dtype == PKV_FP8_E4M3 ? a.k_scale : nullptr,
+      a.cache_dtype == PKV_FP8_E4M3 ? a.v_scale : nullptr, a.src, a.dst, block_bytes, scale_elems,
+      a.num_blocks, a.d_error);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

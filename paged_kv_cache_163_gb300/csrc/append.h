@@ -1,0 +1,37 @@
+// Launch interfaces of the append and block-copy kernels (validated arguments).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+struct AppendArgs {
+  const void *k, *v;
+  pkv_dtype in_dtype;
+  int32_t num_tokens, num_kv_heads, head_dim;
+  const int32_t *slot_mapping;
+  void *k_cache, *v_cache;
+  pkv_dtype cache_dtype;
+  float *k_scale, *v_scale;
+  int32_t num_blocks;
+  int32_t *d_error;
+  cudaStream_t stream;
+};
+
+struct CopyArgs {
+  void *k_cache, *v_cache;
+  float *k_scale, *v_scale;
+  const int32_t *src, *dst;
+  int32_t num_pairs, num_kv_heads, head_dim;
+  pkv_dtype cache_dtype;
+  int32_t num_blocks;
+  int32_t *d_error;
+  cudaStream_t stream;
+};
+
+cudaError_t run_append(const AppendArgs &a);
+cudaError_t run_copy_blocks(const CopyArgs &a);
+
+}  // namespace pkv

@@ -1,0 +1,254 @@
+// Host block manager for the paged KV cache.
+//
+// "KV Cache 与 vLLM" (zwxr.cn) §3.1-§3.4 and "KV Cache优化实战" §4.2: fixed
+// 16-token physical blocks taken on demand, a per-sequence block table,
+// prefix blocks shared by reference count and copied on write, blocks of a
+// finished sequence returned at once.  The free list is a FIFO so the
+// block a request gets is a deterministic function of the call history.
+// Every mutating call validates first and changes nothing on error; an
+// append batch is all-or-nothing (out of blocks must not crash a request:
+// "企业官网建设流程全解析" §6.4).
+#include <deque>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "pkv.h"
+#include "status.h"
+
+struct pkv_bm {
+  struct Seq {
+    std::vector<int32_t> blocks;
+    int32_t len = 0;
+  };
+  int32_t num_blocks = 0;
+  int32_t block_size = PKV_BLOCK_SIZE;
+  std::deque<int32_t> free_list;
+  std::vector<int32_t> ref;
+  std::unordered_map<int64_t, Seq> seqs;
+
+  int32_t pop() {
+    int32_t b = free_list.front();
+    free_list.pop_front();
+    ref[b] = 1;
+    return b;
+  }
+  void drop(int32_t b) {
+    if (--ref[b] == 0) free_list.push_back(b);
+  }
+};
+
+using pkv::fail;
+
+extern "C" {
+
+pkv_status pkv_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *alloc_order,
+                         pkv_bm **out) {
+  if (!out) return fail(PKV_ERR_INVALID, "pkv_bm_create: out is NULL");
+  if (num_blocks <= 0) return fail(PKV_ERR_INVALID, "pkv_bm_create: num_blocks must be > 0");
+  if (block_size != PKV_BLOCK_SIZE)
+    return fail(PKV_ERR_UNSUPPORTED, "pkv_bm_create: block_size must be 16");
+  std::vector<char> seen(num_blocks, 0);
+  if (alloc_order) {
+    for (int32_t i = 0; i < num_blocks; ++i) {
+      int32_t b = alloc_order[i];
+      if (b < 0 || b >= num_blocks || seen[b])
+        return fail(PKV_ERR_INVALID, "pkv_bm_create: alloc_order is not a permutation");
+      seen[b] = 1;
+    }
+  }
+  pkv_bm *bm = new pkv_bm();
+  bm->num_blocks = num_blocks;
+  bm->block_size = block_size;
+  bm->ref.assign(num_blocks, 0);
+  for (int32_t i = 0; i < num_blocks; ++i) bm->free_list.push_back(alloc_order ? alloc_order[i] : i);
+  *out = bm;
+  return PKV_OK;
+}
+
+void pkv_bm_destroy(pkv_bm *bm) { delete bm; }
+
+pkv_status kv_block_alloc(pkv_bm *bm, int32_t *block_id) {
+  if (!bm || !block_id) return fail(PKV_ERR_INVALID, "kv_block_alloc: NULL argument");
+  if (bm->free_list.empty()) return fail(PKV_ERR_NO_BLOCKS, "kv_block_alloc: free list empty");
+  *block_id = bm->pop();
+  return PKV_OK;
+}
+
+pkv_status kv_block_free(pkv_bm *bm, int32_t block_id) {
+  if (!bm) return fail(PKV_ERR_INVALID, "kv_block_free: NULL handle");
+  if (block_id < 0 || block_id >= bm->num_blocks || bm->ref[block_id] <= 0)
+    return fail(PKV_ERR_INVALID, "kv_block_free: block is not held");
+  bm->drop(block_id);
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_create(pkv_bm *bm, int64_t seq_id) {
+  if (!bm) return fail(PKV_ERR_INVALID, "pkv_seq_create: NULL handle");
+  if (bm->seqs.count(seq_id)) return fail(PKV_ERR_INVALID, "pkv_seq_create: sequence exists");
+  bm->seqs.emplace(seq_id, pkv_bm::Seq());
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_fork(pkv_bm *bm, int64_t parent, int64_t child) {
+  if (!bm) return fail(PKV_ERR_INVALID, "pkv_seq_fork: NULL handle");
+  auto it = bm->seqs.find(parent);
+  if (it == bm->seqs.end()) return fail(PKV_ERR_INVALID, "pkv_seq_fork: unknown parent");
+  if (bm->seqs.count(child)) return fail(PKV_ERR_INVALID, "pkv_seq_fork: child exists");
+  pkv_bm::Seq s = it->second;
+  for (int32_t b : s.blocks) ++bm->ref[b];
+  bm->seqs.emplace(child, std::move(s));
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_free(pkv_bm *bm, int64_t seq_id) {
+  if (!bm) return fail(PKV_ERR_INVALID, "pkv_seq_free: NULL handle");
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return fail(PKV_ERR_INVALID, "pkv_seq_free: unknown sequence");
+  for (int32_t b : it->second.blocks) bm->drop(b);
+  bm->seqs.erase(it);
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_append_slots(pkv_bm *bm, const int64_t *seq_ids, int32_t n,
+                                int32_t *slot_mapping, int32_t *cow_src, int32_t *cow_dst,
+                                int32_t *num_cow) {
+  if (!bm || n < 0 || (n > 0 && (!seq_ids || !slot_mapping || !cow_src || !cow_dst)) || !num_cow)
+    return fail(PKV_ERR_INVALID, "pkv_seq_append_slots: bad argument");
+  const int32_t bs = bm->block_size;
+  // Dry run: count the blocks the batch takes, tracking lengths, which last
+  // blocks are already private to the appender, and reference drops.
+  struct Local {
+    int32_t len;
+    bool last_private;  // last block was taken in this batch (count 1, exclusive)
+  };
+  std::unordered_map<int64_t, Local> local;
+  std::unordered_map<int32_t, int32_t> ref_drop;
+  int64_t need = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seq_ids[i]);
+    if (it == bm->seqs.end()) return fail(PKV_ERR_INVALID, "pkv_seq_append_slots: unknown sequence");
+    auto ins = local.emplace(seq_ids[i], Local{it->second.len, false});
+    Local &l = ins.first->second;
+    if (l.len % bs == 0) {
+      ++need;
+      l.last_private = true;
+    } else if (!l.last_private) {
+      int32_t last = it->second.blocks.back();
+      if (bm->ref[last] - ref_drop[last] > 1) {
+        ++need;
+        ++ref_drop[last];
+      }
+      l.last_private = true;  // after a copy, or when this holder is the last one
+    }
+    if (l.len == INT32_MAX) return fail(PKV_ERR_INVALID, "pkv_seq_append_slots: length overflow");
+    ++l.len;
+  }
+  if (need > static_cast<int64_t>(bm->free_list.size()))
+    return fail(PKV_ERR_NO_BLOCKS, "pkv_seq_append_slots: free list cannot cover the batch");
+  // Apply.
+  int32_t ncow = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    pkv_bm::Seq &s = bm->seqs[seq_ids[i]];
+    int32_t pos = s.len;
+    if (pos % bs == 0) {
+      s.blocks.push_back(bm->pop());
+    } else {
+      int32_t last = s.blocks.back();
+      if (bm->ref[last] > 1) {
+        int32_t fresh = bm->pop();
+        --bm->ref[last];
+        s.blocks.back() = fresh;
+        cow_src[ncow] = last;
+        cow_dst[ncow] = fresh;
+        ++ncow;
+      }
+    }
+    slot_mapping[i] = s.blocks[pos / bs] * bs + pos % bs;
+    s.len = pos + 1;
+  }
+  *num_cow = ncow;
+  return PKV_OK;
+}
+
+pkv_status pkv_build_block_tables(const pkv_bm *bm, const int64_t *seq_ids, int32_t n,
+                                  int32_t max_blocks, int32_t *tables, int32_t *context_lens) {
+  if (!bm || n < 0 || max_blocks < 0 || (n > 0 && (!seq_ids || !context_lens)) ||
+      (n > 0 && max_blocks > 0 && !tables))
+    return fail(PKV_ERR_INVALID, "pkv_build_block_tables: bad argument");
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seq_ids[i]);
+    if (it == bm->seqs.end()) return fail(PKV_ERR_INVALID, "pkv_build_block_tables: unknown sequence");
+    if (static_cast<int64_t>(it->second.blocks.size()) > max_blocks)
+      return fail(PKV_ERR_INVALID, "pkv_build_block_tables: table longer than max_blocks");
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const pkv_bm::Seq &s = bm->seqs.at(seq_ids[i]);
+    int32_t *row = tables + static_cast<int64_t>(i) * max_blocks;
+    int32_t nb = static_cast<int32_t>(s.blocks.size());
+    for (int32_t j = 0; j < nb; ++j) row[j] = s.blocks[j];
+    for (int32_t j = nb; j < max_blocks; ++j) row[j] = -1;
+    context_lens[i] = s.len;
+  }
+  return PKV_OK;
+}
+
+int32_t pkv_bm_num_free(const pkv_bm *bm) {
+  return bm ? static_cast<int32_t>(bm->free_list.size()) : -1;
+}
+
+int32_t pkv_bm_num_blocks(const pkv_bm *bm) { return bm ? bm->num_blocks : -1; }
+
+pkv_status pkv_bm_free_list(const pkv_bm *bm, int32_t *out, int32_t cap, int32_t *n) {
+  if (!bm || !n || cap < 0 || (cap > 0 && !out))
+    return fail(PKV_ERR_INVALID, "pkv_bm_free_list: bad argument");
+  int32_t i = 0;
+  for (int32_t b : bm->free_list) {
+    if (i >= cap) break;
+    out[i++] = b;
+  }
+  *n = static_cast<int32_t>(bm->free_list.size());
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_refcount(const pkv_bm *bm, int32_t block_id, int32_t *count) {
+  if (!bm || !count || block_id < 0 || block_id >= bm->num_blocks)
+    return fail(PKV_ERR_INVALID, "pkv_bm_refcount: bad argument");
+  *count = bm->ref[block_id];
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_len(const pkv_bm *bm, int64_t seq_id, int32_t *len) {
+  if (!bm || !len) return fail(PKV_ERR_INVALID, "pkv_seq_len: bad argument");
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return fail(PKV_ERR_INVALID, "pkv_seq_len: unknown sequence");
+  *len = it->second.len;
+  return PKV_OK;
+}
+
+static int64_t elem_bytes_per_token_head(int32_t head_dim, pkv_dtype dt) {
+  switch (dt) {
+    case PKV_F16:
+    case PKV_BF16:
+      return 2 * static_cast<int64_t>(head_dim);
+    case PKV_FP8_E4M3:
+      return static_cast<int64_t>(head_dim) + 4;  // codes + one fp32 scale
+  }
+  return -1;
+}
+
+int64_t pkv_kv_bytes(int32_t layers, int32_t kv_heads, int32_t head_dim, int64_t tokens,
+                     pkv_dtype cache_dtype) {
+  int64_t per = elem_bytes_per_token_head(head_dim, cache_dtype);
+  if (layers < 0 || kv_heads < 0 || head_dim <= 0 || tokens < 0 || per < 0) return -1;
+  return 2 * static_cast<int64_t>(layers) * kv_heads * tokens * per;
+}
+
+int64_t pkv_pool_blocks(int64_t budget_bytes, int32_t layers, int32_t kv_heads, int32_t head_dim,
+                        pkv_dtype cache_dtype) {
+  int64_t per_block = pkv_kv_bytes(layers, kv_heads, head_dim, PKV_BLOCK_SIZE, cache_dtype);
+  if (budget_bytes < 0 || per_block <= 0) return -1;
+  return budget_bytes / per_block;
+}
+
+}  // extern "C"

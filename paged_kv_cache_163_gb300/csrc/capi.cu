@@ -1,0 +1,248 @@
+// C ABI of the device calls: argument validation, launch configuration,
+// workspace layout.  Kernels live in append.cu and decode_*.cu.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <string>
+
+#include "append.h"
+#include "decode.h"
+#include "pkv.h"
+#include "status.h"
+
+namespace pkv {
+namespace {
+
+thread_local int64_t t_launches = 0;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status cuda_fail(cudaError_t e, const char *where) {
+  std::string msg = std::string(where) + ": " + cudaGetErrorString(e);
+  return fail(PKV_ERR_CUDA, msg.c_str());
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+using DecodeFn = cudaError_t (*)(int, int, int, const DecodeParams *, int, int64_t *, int *);
+
+DecodeFn pick_decode(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
+  if (cache_dtype == PKV_F16 && q_dtype == PKV_F16) return decode_call_f16;
+  if (cache_dtype == PKV_BF16 && q_dtype == PKV_BF16) return decode_call_bf16;
+  if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_F16) return decode_call_fp8_f16;
+  if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_BF16) return decode_call_fp8_bf16;
+  return nullptr;
+}
+
+int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
+
+struct DecodeLayout {
+  int64_t cum_bytes, ml_bytes, o_bytes, total;
+  int max_ctas;
+};
+
+// Shapes and dtypes checked by the caller.  Fills the workspace layout and
+// the largest grid the instance runs with on this device.
+pkv_status decode_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, pkv_dtype q_dtype, pkv_dtype cache_dtype,
+                         DecodeLayout *lay) {
+  DecodeFn fn = pick_decode(q_dtype, cache_dtype);
+  if (!fn) return fail(PKV_ERR_UNSUPPORTED, "decode: unsupported q / cache dtype pair");
+  const int group = num_q_heads / num_kv_heads;
+  int ctas = 0;
+  cudaError_t e = fn(head_dim, group, kDecodePrepare, nullptr, 0, nullptr, &ctas);
+  if (e == cudaErrorNotSupported)
+    return fail(PKV_ERR_UNSUPPORTED, "decode: head_dim must be 64 or 128 and group 1, 2, 4 or 8");
+  if (e != cudaSuccess) return cuda_fail(e, "decode: kernel setup");
+  const int sms = sm_count();
+  if (sms <= 0) return fail(PKV_ERR_CUDA, "decode: cannot query the SM count");
+  lay->max_ctas = sms * ctas;
+  const int64_t slots = static_cast<int64_t>(lay->max_ctas) * kDecodeWarps +
+                        static_cast<int64_t>(num_seqs) * num_kv_heads;
+  lay->cum_bytes = round256((static_cast<int64_t>(num_seqs) + 1) * 4);
+  lay->ml_bytes = round256(slots * group * 2 * 4);
+  lay->o_bytes = round256(slots * group * head_dim * 4);
+  lay->total = lay->cum_bytes + lay->ml_bytes + lay->o_bytes;
+  return PKV_OK;
+}
+
+pkv_status check_heads(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (head_dim != 64 && head_dim != 128) return fail(PKV_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int64_t pkv_launch_count(void) { return t_launches; }
+
+pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                                const int32_t *src, const int32_t *dst, int32_t num_pairs,
+                                int32_t num_kv_heads, int32_t head_dim, pkv_dtype cache_dtype,
+                                int32_t num_blocks, int32_t *d_error, pkv_stream_t stream) {
+  if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0)
+    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: bad sizes");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "paged_kv_copy_blocks: head_dim must be 64 or 128");
+  if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3)
+    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: bad cache dtype");
+  if (num_pairs == 0) return PKV_OK;
+  if (num_pairs > 65535) return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: at most 65535 pairs per call");
+  if (!k_cache || !v_cache || !src || !dst || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: NULL or misaligned pointer");
+  if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale))
+    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: FP8 cache needs k_scale and v_scale");
+  CopyArgs a{k_cache, v_cache, k_scale, v_scale, src, dst, num_pairs, num_kv_heads,
+             head_dim, cache_dtype, num_blocks, d_error, reinterpret_cast<cudaStream_t>(stream)};
+  cudaError_t e = run_copy_blocks(a);
+  if (e != cudaSuccess) return cuda_fail(e, "paged_kv_copy_blocks");
+  ++t_launches;
+  return PKV_OK;
+}
+
+pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int32_t num_tokens,
+                           int32_t num_kv_heads, int32_t head_dim, const int32_t *slot_mapping,
+                           void *k_cache, void *v_cache, pkv_dtype cache_dtype, float *k_scale,
+                           float *v_scale, int32_t num_blocks, int32_t *d_error,
+                           pkv_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0)
+    return fail(PKV_ERR_INVALID, "paged_kv_append: bad sizes");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "paged_kv_append: head_dim must be 64 or 128");
+  if (in_dtype != PKV_F16 && in_dtype != PKV_BF16)
+    return fail(PKV_ERR_INVALID, "paged_kv_append: input rows must be F16 or BF16");
+  if (cache_dtype != PKV_FP8_E4M3 && cache_dtype != in_dtype)
+    return fail(PKV_ERR_UNSUPPORTED, "paged_kv_append: a 16-bit cache must match the input dtype");
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !aligned16(k) || !aligned16(v) ||
+      !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PKV_ERR_INVALID, "paged_kv_append: NULL or misaligned pointer");
+  if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale))
+    return fail(PKV_ERR_INVALID, "paged_kv_append: FP8 cache needs k_scale and v_scale");
+  AppendArgs a{k, v, in_dtype, num_tokens, num_kv_heads, head_dim, slot_mapping, k_cache, v_cache,
+               cache_dtype, k_scale, v_scale, num_blocks, d_error,
+               reinterpret_cast<cudaStream_t>(stream)};
+  cudaError_t e = run_append(a);
+  if (e != cudaSuccess) return cuda_fail(e, "paged_kv_append");
+  ++t_launches;
+  return PKV_OK;
+}
+
+pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           pkv_dtype q_dtype, pkv_dtype cache_dtype,
+                                           size_t *bytes) {
+  if (!bytes || num_seqs < 0 || num_seqs > PKV_MAX_SEQS_PER_CALL)
+    return fail(PKV_ERR_INVALID, "paged_attention_workspace_bytes: bad argument");
+  pkv_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
+  if (s != PKV_OK) return s;
+  DecodeLayout lay;
+  s = decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, q_dtype, cache_dtype, &lay);
+  if (s != PKV_OK) return s;
+  *bytes = static_cast<size_t>(lay.total);
+  return PKV_OK;
+}
+
+pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                  const void *k_cache,
+                                  const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
+                                  const float *v_scale, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                  int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                                  float scale, void *workspace, size_t workspace_bytes,
+                                  int32_t *d_error, pkv_stream_t stream) {
+  if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS_PER_CALL)
+    return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: num_seqs must be in [0, 1024]");
+  pkv_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
+  if (s != PKV_OK) return s;
+  if (max_blocks_per_seq < 0 || max_context_len < 0 || num_blocks <= 0)
+    return fail(PKV_ERR_INVALID, "paged_attention_decode: bad sizes");
+  if (static_cast<int64_t>(num_seqs) * num_kv_heads > (1 << 24))
+    return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: too many (sequence, KV head) pairs");
+  if (out_dtype != PKV_F32 && out_dtype != q_dtype)
+    return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: out_dtype must be F32 or q_dtype");
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace ||
+      !aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(workspace))
+    return fail(PKV_ERR_INVALID, "paged_attention_decode: NULL or misaligned pointer");
+  if (cache_dtype == PKV_FP8_E4M3 &&
+      (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
+    return fail(PKV_ERR_INVALID, "paged_attention_decode: FP8 cache needs aligned k_scale and v_scale");
+  DecodeLayout lay;
+  s = decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, q_dtype, cache_dtype, &lay);
+  if (s != PKV_OK) return s;
+  if (workspace_bytes < static_cast<size_t>(lay.total))
+    return fail(PKV_ERR_WORKSPACE, "paged_attention_decode: workspace smaller than required");
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  DecodeParams p;
+  p.out = static_cast<uint8_t *>(out);
+  p.out_f32 = out_dtype == PKV_F32 ? 1 : 0;
+  p.q = static_cast<const uint8_t *>(q);
+  p.k_cache = static_cast<const uint8_t *>(k_cache);
+  p.v_cache = static_cast<const uint8_t *>(v_cache);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_context_len = max_context_len;
+  p.num_seqs = num_seqs;
+  p.num_kv_heads = num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.ws_cum = reinterpret_cast<int32_t *>(ws);
+  p.ws_ml = reinterpret_cast<float *>(ws + lay.cum_bytes);
+  p.ws_o = reinterpret_cast<float *>(ws + lay.cum_bytes + lay.ml_bytes);
+  p.d_error = d_error;
+  p.stream = reinterpret_cast<cudaStream_t>(stream);
+
+  // Grid: enough warps that each gets a few tiles of the largest possible
+  // share, capped at one wave of resident CTAs.
+  constexpr int64_t kMinTilesPerWarp = 4;
+  const int64_t max_tiles = static_cast<int64_t>(num_seqs) * num_kv_heads *
+                            ((static_cast<int64_t>(max_context_len) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE);
+  int64_t grid = (max_tiles + kDecodeWarps * kMinTilesPerWarp - 1) / (kDecodeWarps * kMinTilesPerWarp);
+  if (grid < 1) grid = 1;
+  if (grid > lay.max_ctas) grid = lay.max_ctas;
+
+  DecodeFn fn = pick_decode(q_dtype, cache_dtype);
+  cudaError_t e = fn(head_dim, num_q_heads / num_kv_heads, kDecodeLaunch, &p, static_cast<int>(grid),
+                     &t_launches, nullptr);
+  if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode");
+  return PKV_OK;
+}
+
+pkv_status pkv_read_device_error(int32_t *d_error, int32_t *h_error, int32_t clear,
+                                 pkv_stream_t stream) {
+  if (!d_error || !h_error) return fail(PKV_ERR_INVALID, "pkv_read_device_error: NULL pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h_error, d_error, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && clear) {
+    e = cudaMemsetAsync(d_error, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_read_device_error");
+  if (*h_error != 0) return fail(PKV_ERR_DEVICE_CHECK, "device-side check failed");
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,556 @@
+// PagedAttention decode: split-KV partial kernel and log-sum-exp reduce.
+//
+// What is computed ("企业官网建设流程全解析" (KV Cache 原理篇) §1.2, §3.2;
+// "KV Cache 与 vLLM" (zwxr.cn) §3.2): for sequence b and query head h
+// (KV head h / G), out = softmax(scale * q K^T) V over the sequence's
+// context_len cached tokens, reached through its block table.
+//
+// How (GB300 design, not from the pages):
+//  * The work is the list of tiles (sequence, KV head, logical block), each
+//    one contiguous [16][head_dim] chunk of K and of V in HBM.  The tiles are
+//    flattened (sequence-major, then KV head, then block) and every warp of a
+//    persistent grid takes an equal contiguous share, so ragged lengths load
+//    balance to one tile.  A share that covers a whole (sequence, KV head)
+//    writes the output; one that covers part of it writes an fp32 partial
+//    (o, m, l) and the reduce kernel merges partials by log-sum-exp
+//    (flash-decoding style split-KV).
+//  * Each warp streams its tiles through a private ring of shared-memory
+//    stages filled by bulk asynchronous copies (cp.async.bulk, mbarrier
+//    completion), so ~100 KB per SM is in flight with no CTA-wide sync.
+//  * The GQA group's G query heads stay in registers (fp32, pre-scaled by
+//    scale * log2 e).  Scores: lanes split head_dim, partial dot products are
+//    reduced across lanes with a transposing butterfly (G heads reduce in
+//    G-1+log2(lanes/G) shuffles), online softmax in base 2.
+//  * FP8 tiles are dequantised in registers: the per-token K scale multiplies
+//    the score and the per-token V scale folds into the probability.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+#include "decode.h"
+
+namespace pkv {
+
+constexpr int round_up_c(int x, int m) { return (x + m - 1) / m * m; }
+constexpr int clamp_c(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+template <int D, int G, int CDT, int QDT>
+struct DecodeCfg {
+  static constexpr int kWarps = 8;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kEsz = CDT == PKV_FP8_E4M3 ? 1 : 2;
+  static constexpr int kRow = D * kEsz;                     // bytes of one token's row
+  static constexpr int kTile = kBS * kRow;                  // one (block, head) tile of K or V
+  static constexpr int kLPT = (D == 128 && G == 8) ? 16 : 8;  // lanes per token in q.K
+  static constexpr int kTPP = 32 / kLPT;                    // tokens per pass
+  static constexpr int kPasses = kBS / kTPP;
+  static constexpr int kChunk = (kRow / kLPT) < 16 ? (kRow / kLPT) : 16;  // bytes per load
+  static constexpr int kNChunk = kRow / (kLPT * kChunk);    // loads per lane per token
+  static constexpr int kEPC = kChunk / kEsz;                // elements per load
+  static constexpr int kEPT = kEPC * kNChunk;               // q elements per lane
+  static constexpr int kDPL = D / 32;                       // output elements per lane
+  static constexpr int kScale = CDT == PKV_FP8_E4M3 ? kBS * 4 : 0;
+  static constexpr int kQ = G * D * 2;
+  static constexpr int kOffV = kTile;
+  static constexpr int kOffKS = 2 * kTile;
+  static constexpr int kOffVS = 2 * kTile + kScale;
+  static constexpr int kOffQ = 2 * kTile + 2 * kScale;
+  static constexpr int kStage = round_up_c(kOffQ + kQ, 128);
+  static constexpr int kStages = clamp_c(27900 / kStage, 2, 6);
+  static constexpr int kCumBytes = round_up_c((PKV_MAX_SEQS_PER_CALL + 1) * 4, 128);
+  static constexpr int kMiscBytes = 128;                    // scan scratch
+  static constexpr int kBarBytes = round_up_c(kWarps * kStages * 8, 128);
+  static constexpr int kDescBytes = kWarps * 64 * 8;        // two windows of 32 tile descriptors
+  static constexpr int kSmem = kCumBytes + kMiscBytes + kBarBytes + kDescBytes + kWarps * kStages * kStage;
+  static_assert(G <= kLPT, "group larger than lanes per token");
+  static_assert((kBS + 3) * G * 4 <= kTile, "probability buffer must fit in the K tile");
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kEPT * kLPT == D, "q.K lane split");
+};
+
+// Butterfly over the kLPT lanes of one token: v[G] partial dot products per
+// lane in, the full dot product of head (lane % LPT) / (LPT / G) out.
+template <int G, int LPT>
+__device__ __forceinline__ float reduce_heads(float (&v)[G], int lane) {
+  int n = G;
+#pragma unroll
+  for (int off = LPT / 2; off >= 1; off >>= 1) {
+    if (n > 1) {
+      const bool up = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < G / 2; ++i) {
+        if (i < n / 2) {
+          const float send = up ? v[i] : v[i + n / 2];
+          const float keep = up ? v[i + n / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(kFull, send, off);
+        }
+      }
+      n >>= 1;
+    } else {
+      v[0] += __shfl_xor_sync(kFull, v[0], off);
+    }
+  }
+  return v[0];
+}
+
+// Tile index t -> (sequence, KV head, block) using the exclusive prefix sum
+// cum[] of blocks per sequence (in shared memory).
+__device__ __forceinline__ int find_seq(const int32_t *cum, int num_seqs, int hkv, int64_t t) {
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(hkv) * cum[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Descriptor of one tile: x = physical block (-1 if invalid),
+// y = item << 7 | first << 6 | last << 5 | valid tokens.
+__device__ __forceinline__ int2 tile_desc(const DecodeParams &p, const int32_t *cum, int64_t t) {
+  const int b = find_seq(cum, p.num_seqs, p.num_kv_heads, t);
+  const int nb = cum[b + 1] - cum[b];
+  const int64_t r = t - static_cast<int64_t>(p.num_kv_heads) * cum[b];
+  const int kvh = static_cast<int>(r / nb);
+  const int lb = static_cast<int>(r - static_cast<int64_t>(kvh) * nb);
+  const int L = __ldg(p.context_lens + b);
+  const int ntok = min(kBS, L - lb * kBS);
+  int32_t blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + lb);
+  if (blk < 0 || blk >= p.num_blocks) {
+    report(p.d_error, PKV_DEVERR_BAD_BLOCK);
+    blk = -1;
+  }
+  const int item = b * p.num_kv_heads + kvh;
+  return make_int2(blk, (item << 7) | ((lb == 0) << 6) | ((lb == nb - 1) << 5) | ntok);
+}
+
+template <int D, int G, int CDT, int QDT>
+__global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
+    paged_decode_kernel(const DecodeParams p) {
+  using C = DecodeCfg<D, G, CDT, QDT>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  int32_t *cum = reinterpret_cast<int32_t *>(smem);
+  int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kCumBytes);
+  uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + C::kCumBytes + C::kMiscBytes);
+  int2 *desc_all = reinterpret_cast<int2 *>(smem + C::kCumBytes + C::kMiscBytes + C::kBarBytes);
+  uint8_t *stage_all = smem + C::kCumBytes + C::kMiscBytes + C::kBarBytes + C::kDescBytes;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---- prologue: blocks per sequence and their exclusive prefix sum -------
+  {
+    constexpr int PER = (PKV_MAX_SEQS_PER_CALL + C::kThreads - 1) / C::kThreads;
+    int nbk[PER];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int s = tid * PER + i;
+      int nb = 0;
+      if (s < p.num_seqs) {
+        const int L = p.context_lens[s];
+        if (L < 0 || L > p.max_context_len ||
+            static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBS) {
+          report(p.d_error, PKV_DEVERR_BAD_CONTEXT_LEN);
+        } else {
+          nb = (L + kBS - 1) / kBS;
+        }
+      }
+      nbk[i] = nb;
+      sum += nb;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) misc[warp] = incl;
+    if (lane < C::kStages) mbar_init(bars_all + warp * C::kStages + lane, 1);
+    __syncthreads();
+    if (warp == 0) {
+      int x = lane < C::kWarps ? misc[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += n;
+      }
+      if (lane < C::kWarps) misc[16 + lane] = x;  // inclusive warp totals
+    }
+    __syncthreads();
+    int run = incl - sum + (warp > 0 ? misc[16 + warp - 1] : 0);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int s = tid * PER + i;
+      if (s < p.num_seqs) cum[s] = run;
+      run += nbk[i];
+    }
+    if (tid == 0) cum[p.num_seqs] = misc[16 + C::kWarps - 1];
+    fence_barrier_init();
+    __syncthreads();
+    if (blockIdx.x == 0) {
+      for (int s = tid; s <= p.num_seqs; s += C::kThreads) p.ws_cum[s] = cum[s];
+    }
+  }
+
+  // ---- this warp's share of the tiles --------------------------------------
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * C::kWarps;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * C::kWarps + warp;
+  const int64_t total = static_cast<int64_t>(cum[p.num_seqs]) * p.num_kv_heads;
+  const int64_t t0 = gw * total / nwarps;
+  const int64_t t1 = (gw + 1) * total / nwarps;
+  const int count = static_cast<int>(t1 - t0);
+  if (count <= 0) return;
+
+  uint64_t *bars = bars_all + warp * C::kStages;
+  int2 *desc = desc_all + warp * 64;
+  uint8_t *stages = stage_all + warp * C::kStages * C::kStage;
+  const uint64_t pol = policy_evict_first();
+  const size_t head_tile = static_cast<size_t>(C::kTile);
+
+  auto fill_window = [&](int w) {  // descriptors of warp-local tiles [32 w, 32 w + 32)
+    const int64_t t = t0 + 32 * static_cast<int64_t>(w) + lane;
+    int2 d = make_int2(-1, 0);
+    if (t < t1) d = tile_desc(p, cum, t);
+    desc[(w & 1) * 32 + lane] = d;
+  };
+
+  auto issue = [&](int m) {  // lane 0 starts the copies of warp-local tile m
+    const int2 d = desc[((m >> 5) & 1) * 32 + (m & 31)];
+    if (lane == 0) {
+      const int st = m % C::kStages;
+      uint8_t *sb = stages + st * C::kStage;
+      const int item = d.y >> 7;
+      const bool need_q = (m == 0) || ((d.y >> 6) & 1);
+      const uint32_t bytes = (d.x >= 0 ? 2 * C::kTile + 2 * C::kScale : 0) + (need_q ? C::kQ : 0);
+      fence_proxy_async_smem();
+      if (bytes == 0) {
+        mbar_arrive(bars + st);
+      } else {
+        mbar_arrive_expect_tx(bars + st, bytes);
+        if (d.x >= 0) {
+          const int kvh = item % p.num_kv_heads;
+          const size_t tile = static_cast<size_t>(d.x) * p.num_kv_heads + kvh;
+          bulk_g2s(sb, p.k_cache + tile * head_tile, C::kTile, bars + st, pol);
+          bulk_g2s(sb + C::kOffV, p.v_cache + tile * head_tile, C::kTile, bars + st, pol);
+          if constexpr (C::kScale > 0) {
+            bulk_g2s(sb + C::kOffKS, p.k_scale + tile * kBS, C::kScale, bars + st, pol);
+            bulk_g2s(sb + C::kOffVS, p.v_scale + tile * kBS, C::kScale, bars + st, pol);
+          }
+        }
+        if (need_q) bulk_g2s(sb + C::kOffQ, p.q + static_cast<size_t>(item) * C::kQ, C::kQ, bars + st);
+      }
+    }
+  };
+
+  fill_window(0);
+  fill_window(1);
+  __syncwarp();
+#pragma unroll 1
+  for (int i = 0; i < C::kStages && i < count; ++i) issue(i);
+
+  const int jl = lane % C::kLPT;  // lane within its token group
+  const int tg = lane / C::kLPT;  // token group
+  const int hd = jl / (C::kLPT / G);                  // head this lane's score belongs to
+  const bool lead = (jl % (C::kLPT / G)) == 0;        // one writer per (token, head)
+
+  float qreg[G][C::kEPT];
+  float o[G][C::kDPL];
+  float m[G], l[G];
+  float m_mine = -INFINITY;
+  int cur_item = -1;
+  bool whole_start = false, saw_last = false;
+
+  auto flush = [&](int item, bool whole) {
+    if (whole) {
+      const size_t base = (static_cast<size_t>(item) * G) * D + lane * C::kDPL;  // element index
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float inv = l[g] > 0.f ? 1.f / l[g] : 0.f;
+        float r[C::kDPL];
+#pragma unroll
+        for (int e = 0; e < C::kDPL; ++e) r[e] = o[g][e] * inv;
+        if (p.out_f32) {
+          float *dst = reinterpret_cast<float *>(p.out) + base + g * D;
+          if constexpr (C::kDPL == 4) {
+            *reinterpret_cast<float4 *>(dst) = make_float4(r[0], r[1], r[2], r[3]);
+          } else {
+            *reinterpret_cast<float2 *>(dst) = make_float2(r[0], r[1]);
+          }
+        } else {
+          uint8_t *dst = p.out + (base + g * D) * 2;
+          if constexpr (C::kDPL == 4) {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(pack2<QDT>(r[0], r[1]), pack2<QDT>(r[2], r[3]));
+          } else {
+            *reinterpret_cast<uint32_t *>(dst) = pack2<QDT>(r[0], r[1]);
+          }
+        }
+      }
+    } else {
+      const int64_t slot = gw + item;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float *op = p.ws_o + (slot * G + g) * D + lane * C::kDPL;
+        if constexpr (C::kDPL == 4) {
+          *reinterpret_cast<float4 *>(op) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+        } else {
+          *reinterpret_cast<float2 *>(op) = make_float2(o[g][0], o[g][1]);
+        }
+        if (lane == 0) {
+          p.ws_ml[(slot * G + g) * 2] = m[g];
+          p.ws_ml[(slot * G + g) * 2 + 1] = l[g];
+        }
+      }
+    }
+  };
+
+#pragma unroll 1
+  for (int n = 0; n < count; ++n) {
+    if (n > 0 && (n & 31) == 0) {
+      __syncwarp();
+      fill_window((n >> 5) + 1);
+      __syncwarp();
+    }
+    const int2 d = desc[((n >> 5) & 1) * 32 + (n & 31)];
+    const int st = n % C::kStages;
+    uint8_t *sb = stages + st * C::kStage;
+    const bool ok = __all_sync(kFull, mbar_wait(bars + st, (n / C::kStages) & 1));
+    if (!ok) {
+      if (lane == 0) report(p.d_error, PKV_DEVERR_WAIT_TIMEOUT);
+      // let the copies this warp still has in flight land before leaving
+      for (int k = n + 1; k < count && k < n + C::kStages; ++k)
+        mbar_wait(bars + k % C::kStages, (k / C::kStages) & 1);
+      return;
+    }
+    const int item = d.y >> 7;
+    const int ntok = d.y & 31;
+    if (item != cur_item) {
+      if (cur_item >= 0) flush(cur_item, whole_start && saw_last);
+      cur_item = item;
+      whole_start = (d.y >> 6) & 1;
+      // this item's G query heads -> registers, pre-scaled by scale * log2(e)
+      const uint8_t *qs = sb + C::kOffQ;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+#pragma unroll
+        for (int c = 0; c < C::kNChunk; ++c) {
+          const int d0 = (jl + c * C::kLPT) * C::kEPC;
+#pragma unroll
+          for (int e = 0; e < C::kEPC; e += 2) {
+            const float2 f = unpack2<QDT>(*reinterpret_cast<const uint32_t *>(qs + (g * D + d0 + e) * 2));
+            qreg[g][c * C::kEPC + e] = f.x * p.scale_log2;
+            qreg[g][c * C::kEPC + e + 1] = f.y * p.scale_log2;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < C::kDPL; ++e) o[g][e] = 0.f;
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+      }
+      m_mine = -INFINITY;
+    }
+    saw_last = (d.y >> 5) & 1;
+
+    if (d.x >= 0) {
+      const uint8_t *ks = sb;
+      const uint8_t *vs = sb + C::kOffV;
+      // -- scores of this tile: s = (q . k) * scale * log2 e, base-2 domain --
+      float sc[C::kPasses];
+#pragma unroll
+      for (int ps = 0; ps < C::kPasses; ++ps) {
+        const int tok = ps * C::kTPP + tg;
+        float part[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) part[g] = 0.f;
+#pragma unroll
+        for (int c = 0; c < C::kNChunk; ++c) {
+          float x[C::kEPC];
+          unpack_row<CDT, C::kChunk>(ks + tok * C::kRow + (jl + c * C::kLPT) * C::kChunk, x);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < C::kEPC; ++e) part[g] = fmaf(qreg[g][c * C::kEPC + e], x[e], part[g]);
+        }
+        float r = reduce_heads<G, C::kLPT>(part, lane);
+        if constexpr (CDT == PKV_FP8_E4M3) r *= reinterpret_cast<const float *>(sb + C::kOffKS)[tok];
+        sc[ps] = tok < ntok ? r : -INFINITY;
+      }
+      // -- online softmax over this tile (per head) --
+      float mx = sc[0];
+#pragma unroll
+      for (int ps = 1; ps < C::kPasses; ++ps) mx = fmaxf(mx, sc[ps]);
+#pragma unroll
+      for (int off = C::kLPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+      const float m_new = fmaxf(m_mine, mx);
+      const float alpha = exp2f(m_mine - m_new);
+      float pr[C::kPasses];
+      float psum = 0.f;
+#pragma unroll
+      for (int ps = 0; ps < C::kPasses; ++ps) {
+        pr[ps] = exp2f(sc[ps] - m_new);
+        psum += pr[ps];
+      }
+#pragma unroll
+      for (int off = C::kLPT; off < 32; off <<= 1) psum += __shfl_xor_sync(kFull, psum, off);
+      m_mine = m_new;
+      __syncwarp();  // every lane is done with K: its space now holds probabilities
+      float *pbuf = reinterpret_cast<float *>(sb);  // [16][G] probabilities, then alpha, sum, max
+      if (lead) {
+#pragma unroll
+        for (int ps = 0; ps < C::kPasses; ++ps) {
+          const int tok = ps * C::kTPP + tg;
+          float pv = pr[ps];
+          if constexpr (CDT == PKV_FP8_E4M3) pv *= reinterpret_cast<const float *>(sb + C::kOffVS)[tok];
+          pbuf[tok * G + hd] = pv;
+        }
+        if (tg == 0) {
+          pbuf[kBS * G + hd] = alpha;
+          pbuf[(kBS + 1) * G + hd] = psum;
+          pbuf[(kBS + 2) * G + hd] = m_new;
+        }
+      }
+      __syncwarp();
+      // -- o = o * alpha + P V --
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float a = pbuf[kBS * G + g];
+        l[g] = l[g] * a + pbuf[(kBS + 1) * G + g];
+        m[g] = pbuf[(kBS + 2) * G + g];
+#pragma unroll
+        for (int e = 0; e < C::kDPL; ++e) o[g][e] *= a;
+      }
+#pragma unroll
+      for (int t = 0; t < kBS; ++t) {
+        if (t < ntok) {
+          float x[C::kDPL];
+          unpack_row<CDT, C::kDPL * C::kEsz>(vs + t * C::kRow + lane * C::kDPL * C::kEsz, x);
+          float pw[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) pw[g] = pbuf[t * G + g];
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < C::kDPL; ++e) o[g][e] = fmaf(pw[g], x[e], o[g][e]);
+        }
+      }
+    }
+    __syncwarp();  // the stage is free again
+    if (n + C::kStages < count) issue(n + C::kStages);
+  }
+  flush(cur_item, whole_start && saw_last);
+}
+
+// One CTA per (sequence, KV head): merge the partials of the warps that
+// shared it, out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+template <int D, int G, int QDT>
+__global__ void __launch_bounds__(128) paged_reduce_kernel(const DecodeParams p, int64_t nwarps) {
+  const int item = blockIdx.x;
+  const int b = item / p.num_kv_heads;
+  const int kvh = item - b * p.num_kv_heads;
+  const int32_t *cum = p.ws_cum;
+  const int nb = cum[b + 1] - cum[b];
+  const size_t obase = static_cast<size_t>(item) * G * D;  // element index of this item's output
+  if (nb == 0) {
+    for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) {
+      if (p.out_f32) reinterpret_cast<float2 *>(p.out)[obase / 2 + i] = make_float2(0.f, 0.f);
+      else reinterpret_cast<uint32_t *>(p.out)[obase / 2 + i] = 0u;
+    }
+    return;
+  }
+  const int64_t total = static_cast<int64_t>(cum[p.num_seqs]) * p.num_kv_heads;
+  const int64_t start = static_cast<int64_t>(p.num_kv_heads) * cum[b] + static_cast<int64_t>(kvh) * nb;
+  const int64_t last = start + nb - 1;
+  // warp owning tile t: the w with floor(w T / W) <= t < floor((w + 1) T / W)
+  const int64_t w_first = ((start + 1) * nwarps - 1) / total;
+  const int64_t w_last = ((last + 1) * nwarps - 1) / total;
+  if (w_first == w_last) return;  // written by the decode kernel
+  for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) {
+    const int g = (2 * i) / D;
+    const int dd = (2 * i) % D;
+    // warps whose share is empty (more warps than tiles) wrote no partial
+    auto empty = [&](int64_t w) { return (w * total / nwarps) == ((w + 1) * total / nwarps); };
+    float mmax = -INFINITY;
+    for (int64_t w = w_first; w <= w_last; ++w)
+      if (!empty(w)) mmax = fmaxf(mmax, p.ws_ml[((w + item) * G + g) * 2]);
+    float num0 = 0.f, num1 = 0.f, den = 0.f;
+    for (int64_t w = w_first; w <= w_last; ++w) {
+      if (empty(w)) continue;
+      const int64_t slot = w + item;
+      const float ms = p.ws_ml[(slot * G + g) * 2];
+      if (ms == -INFINITY) continue;
+      const float sc = exp2f(ms - mmax);
+      const float2 ov = *reinterpret_cast<const float2 *>(p.ws_o + (slot * G + g) * D + dd);
+      num0 = fmaf(sc, ov.x, num0);
+      num1 = fmaf(sc, ov.y, num1);
+      den = fmaf(sc, p.ws_ml[(slot * G + g) * 2 + 1], den);
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const float r0 = num0 * inv, r1 = num1 * inv;
+    if (p.out_f32) reinterpret_cast<float2 *>(p.out)[obase / 2 + i] = make_float2(r0, r1);
+    else reinterpret_cast<uint32_t *>(p.out)[obase / 2 + i] = pack2<QDT>(r0, r1);
+  }
+}
+
+template <int D, int G, int CDT, int QDT>
+struct DecodeInstance {
+  using C = DecodeCfg<D, G, CDT, QDT>;
+  static cudaError_t prepare(int *ctas_per_sm) {
+    static int cached = -1;
+    if (cached < 0) {
+      cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, G, CDT, QDT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+      if (e != cudaSuccess) return e;
+      int n = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<D, G, CDT, QDT>,
+                                                        C::kThreads, C::kSmem);
+      if (e != cudaSuccess) return e;
+      cached = n > 0 ? n : 1;
+    }
+    *ctas_per_sm = cached;
+    return cudaSuccess;
+  }
+  static cudaError_t launch(const DecodeParams &p, int grid, int64_t *launches) {
+    paged_decode_kernel<D, G, CDT, QDT><<<grid, C::kThreads, C::kSmem, p.stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    paged_reduce_kernel<D, G, QDT><<<p.num_seqs * p.num_kv_heads, 128, 0, p.stream>>>(
+        p, static_cast<int64_t>(grid) * C::kWarps);
+    *launches += 2;
+    return cudaGetLastError();
+  }
+};
+
+}  // namespace pkv
+
+namespace pkv {
+
+template <int D, int G, int CDT, int QDT>
+cudaError_t decode_op(int op, const DecodeParams *p, int grid, int64_t *launches, int *ctas) {
+  using I = DecodeInstance<D, G, CDT, QDT>;
+  if (op == kDecodePrepare) return I::prepare(ctas);
+  return I::launch(*p, grid, launches);
+}
+
+template <int CDT, int QDT>
+cudaError_t decode_family(int D, int G, int op, const DecodeParams *p, int grid, int64_t *launches,
+                          int *ctas) {
+  if (D == 128) {
+    switch (G) {
+      case 1: return decode_op<128, 1, CDT, QDT>(op, p, grid, launches, ctas);
+      case 2: return decode_op<128, 2, CDT, QDT>(op, p, grid, launches, ctas);
+      case 4: return decode_op<128, 4, CDT, QDT>(op, p, grid, launches, ctas);
+      case 8: return decode_op<128, 8, CDT, QDT>(op, p, grid, launches, ctas);
+    }
+  } else if (D == 64) {
+    switch (G) {
+      case 1: return decode_op<64, 1, CDT, QDT>(op, p, grid, launches, ctas);
+      case 2: return decode_op<64, 2, CDT, QDT>(op, p, grid, launches, ctas);
+      case 4: return decode_op<64, 4, CDT, QDT>(op, p, grid, launches, ctas);
+      case 8: return decode_op<64, 8, CDT, QDT>(op, p, grid, launches, ctas);
+    }
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace pkv

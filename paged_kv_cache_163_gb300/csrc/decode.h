@@ -1,0 +1,50 @@
+// Launch interface of the decode kernels (arguments already validated).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr int kDecodeWarps = 8;  // warps per CTA of the decode kernel
+
+struct DecodeParams {
+  uint8_t *out;
+  int32_t out_f32;   // 1: out is float32, 0: out has the query's 16-bit type
+  const uint8_t *q;
+  const uint8_t *k_cache;
+  const uint8_t *v_cache;
+  const float *k_scale;
+  const float *v_scale;
+  const int32_t *block_tables;
+  const int32_t *context_lens;
+  int32_t max_blocks_per_seq;
+  int32_t max_context_len;
+  int32_t num_seqs;
+  int32_t num_kv_heads;
+  int32_t num_blocks;
+  float scale_log2;  // scale * log2(e)
+  int32_t *ws_cum;   // [num_seqs + 1] exclusive prefix sum of blocks per sequence
+  float *ws_ml;      // [slots][G][2] partial (max, sum), base-2 domain
+  float *ws_o;       // [slots][G][head_dim] partial unnormalised outputs
+  int32_t *d_error;
+  cudaStream_t stream;
+};
+
+enum DecodeOp { kDecodePrepare = 0, kDecodeLaunch = 1 };
+
+// op == kDecodePrepare: *ctas_per_sm = resident CTAs per SM of the instance.
+// op == kDecodeLaunch: launch the partial kernel on `grid` CTAs, then the reduce.
+// Returns cudaErrorNotSupported when (head_dim, group) has no instance.
+cudaError_t decode_call_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                            int64_t *launches, int *ctas_per_sm);
+cudaError_t decode_call_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                             int64_t *launches, int *ctas_per_sm);
+cudaError_t decode_call_fp8_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                                int64_t *launches, int *ctas_per_sm);
+cudaError_t decode_call_fp8_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                                 int64_t *launches, int *ctas_per_sm);
+
+}  // namespace pkv

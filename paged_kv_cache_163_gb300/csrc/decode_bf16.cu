@@ -1,0 +1,11 @@
+// Decode kernel instances: cache BF16, query BF16.
+#include "decode.cuh"
+
+namespace pkv {
+
+cudaError_t decode_call_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                         int64_t *launches, int *ctas_per_sm) {
+  return decode_family<PKV_BF16, PKV_BF16>(head_dim, group, op, p, grid, launches, ctas_per_sm);
+}
+
+}  // namespace pkv

@@ -1,0 +1,11 @@
+// Decode kernel instances: cache F16, query F16.
+#include "decode.cuh"
+
+namespace pkv {
+
+cudaError_t decode_call_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                        int64_t *launches, int *ctas_per_sm) {
+  return decode_family<PKV_F16, PKV_F16>(head_dim, group, op, p, grid, launches, ctas_per_sm);
+}
+
+}  // namespace pkv

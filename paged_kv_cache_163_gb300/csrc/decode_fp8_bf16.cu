@@ -1,0 +1,11 @@
+// Decode kernel instances: cache FP8_E4M3, query BF16.
+#include "decode.cuh"
+
+namespace pkv {
+
+cudaError_t decode_call_fp8_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                             int64_t *launches, int *ctas_per_sm) {
+  return decode_family<PKV_FP8_E4M3, PKV_BF16>(head_dim, group, op, p, grid, launches, ctas_per_sm);
+}
+
+}  // namespace pkv

@@ -1,0 +1,232 @@
+"""A multi-layer paged KV cache on one GPU, driven through the C ABI.
+
+Orchestration only: the block manager, the cache writes, block copies and
+attention all run in libpkv.so; torch supplies device memory, pinned
+staging buffers and the stream.
+
+One decode step, as the pages describe it ("KV Cache 与 vLLM" (zwxr.cn)
+§3.1-§3.4): the block manager hands every sequence a slot for its new token
+(taking a block when the last one is full, copying a shared block on
+write); the block tables go to the device; per layer, shared blocks are
+copied, the new K/V rows are written, and the new queries attend over each
+sequence's cache through its table.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import capi
+
+_TORCH_DTYPES = None
+
+
+def torch_dtype(name: str):
+    global _TORCH_DTYPES
+    import torch
+    if _TORCH_DTYPES is None:
+        _TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}
+    return _TORCH_DTYPES[name]
+
+
+class _PinnedRing:
+    """Pinned int32 staging buffers reused round-robin, each guarded by an event."""
+
+    def __init__(self, slots: int = 4):
+        self.bufs = [None] * slots
+        self.events = [None] * slots
+        self.i = 0
+
+    def take(self, n: int):
+        import torch
+        k = self.i
+        self.i = (self.i + 1) % len(self.bufs)
+        if self.events[k] is not None:
+            self.events[k].synchronize()
+        if self.bufs[k] is None or self.bufs[k].numel() < n:
+            self.bufs[k] = torch.empty(max(n, 1024), dtype=torch.int32, pin_memory=True)
+        return k, self.bufs[k]
+
+    def done(self, k: int, stream):
+        import torch
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        self.events[k] = ev
+
+
+class PagedKVCache:
+    def __init__(self, *, num_layers: int, num_blocks: int, num_kv_heads: int, head_dim: int,
+                 cache_dtype: str, alloc_order=None, device="cuda", poison: bool = False):
+        import torch
+        self.num_layers, self.num_blocks = num_layers, num_blocks
+        self.num_kv_heads, self.head_dim, self.cache_dtype = num_kv_heads, head_dim, cache_dtype
+        self.device = torch.device(device)
+        self.bm = capi.pkv_bm_create(num_blocks, capi.BLOCK_SIZE, alloc_order)
+        shape = (num_layers, num_blocks, num_kv_heads, capi.BLOCK_SIZE, head_dim)
+        tdt = torch_dtype(cache_dtype)
+        self.k = torch.empty(shape, dtype=tdt, device=self.device)
+        self.v = torch.empty(shape, dtype=tdt, device=self.device)
+        if cache_dtype == "fp8_e4m3":
+            self.k_scale = torch.empty(shape[:4], dtype=torch.float32, device=self.device)
+            self.v_scale = torch.empty(shape[:4], dtype=torch.float32, device=self.device)
+        else:
+            self.k_scale = self.v_scale = None
+        if poison:  # unwritten slots read as NaN: a kernel that strays onto one shows it
+            for t in (self.k, self.v, self.k_scale, self.v_scale):
+                if t is not None:
+                    t.view(torch.uint8).fill_(0xFF)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._ring = _PinnedRing()
+        self._meta = torch.empty(1024, dtype=torch.int32, device=self.device)
+        self._ws = {}
+        self.cow_pairs = []          # every (src, dst) copy, in order
+
+    def close(self):
+        if self.bm is not None:
+            capi.pkv_bm_destroy(self.bm)
+            self.bm = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- sequences ---------------------------------------------------------------
+    def create(self, seq: int):
+        capi.pkv_seq_create(self.bm, seq)
+
+    def fork(self, parent: int, child: int):
+        capi.pkv_seq_fork(self.bm, parent, child)
+
+    def free(self, seq: int):
+        capi.pkv_seq_free(self.bm, seq)
+
+    def seq_len(self, seq: int) -> int:
+        return capi.pkv_seq_len(self.bm, seq)
+
+    # -- metadata upload ---------------------------------------------------------
+    def _upload(self, parts, stream):
+        """Copy int32 host arrays to the device in one transfer; returns device views."""
+        import torch
+        sizes = [int(np.asarray(p).size) for p in parts]
+        total = sum(sizes)
+        k, pin = self._ring.take(total)
+        host = pin.numpy()
+        off = 0
+        for p, n in zip(parts, sizes):
+            host[off:off + n] = np.asarray(p, dtype=np.int32).reshape(-1)
+            off += n
+        if self._meta.numel() < total:
+            self._meta = torch.empty(max(total, 2 * self._meta.numel()), dtype=torch.int32, device=self.device)
+        with torch.cuda.stream(stream):
+            self._meta[:total].copy_(pin[:total], non_blocking=True)
+        self._ring.done(k, stream)
+        views, off = [], 0
+        for n in sizes:
+            views.append(self._meta[off:off + n])
+            off += n
+        return views
+
+    def _stream(self, stream):
+        import torch
+        return torch.cuda.current_stream(self.device) if stream is None else stream
+
+    # -- append --------------------------------------------------------------------
+    def append(self, seq_ids, k_rows, v_rows, layers=None, stream=None):
+        """Append one token per entry of seq_ids.
+
+        k_rows / v_rows: device tensors [num_layers, n, Hkv, D] (or [n, Hkv, D]
+        applied to every layer) in f16 / bf16.  Returns (slots, cow_src, cow_dst).
+        """
+        stream = self._stream(stream)
+        slots, cs, cd = capi.pkv_seq_append_slots(self.bm, seq_ids)
+        d_slots, d_src, d_dst = self._upload([slots, cs, cd], stream)
+        self._apply_append(slots, cs, d_slots, d_src, d_dst, k_rows, v_rows, layers, stream)
+        self.cow_pairs.extend(zip(cs.tolist(), cd.tolist()))
+        return slots, cs, cd
+
+    def _apply_append(self, slots, cs, d_slots, d_src, d_dst, k_rows, v_rows, layers, stream):
+        layers = range(self.num_layers) if layers is None else layers
+        for li in layers:
+            ks = self.k_scale[li] if self.k_scale is not None else None
+            vs = self.v_scale[li] if self.v_scale is not None else None
+            if len(cs):
+                capi.paged_kv_copy_blocks(self.k[li], self.v[li], ks, vs, d_src, d_dst, len(cs),
+                                          d_error=self.err, stream=stream)
+            kr = k_rows[li] if k_rows.dim() == 4 else k_rows
+            vr = v_rows[li] if v_rows.dim() == 4 else v_rows
+            if len(slots):
+                capi.paged_kv_append(kr, vr, d_slots, self.k[li], self.v[li], ks, vs,
+                                     d_error=self.err, stream=stream)
+
+    # -- decode ------------------------------------------------------------------
+    def tables(self, seq_ids):
+        lens = [self.seq_len(s) for s in seq_ids]
+        max_blocks = max(1, max((-(-L // capi.BLOCK_SIZE) for L in lens), default=1))
+        tables, ctx = capi.pkv_build_block_tables(self.bm, seq_ids, max_blocks)
+        return tables, ctx
+
+    def workspace(self, num_seqs, num_q_heads, q_dtype):
+        import torch
+        key = (num_seqs, num_q_heads, q_dtype)
+        if key not in self._ws:
+            n = capi.paged_attention_workspace_bytes(num_seqs, num_q_heads, self.num_kv_heads, self.head_dim,
+                                                     q_dtype, self.cache_dtype)
+            self._ws[key] = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+        return self._ws[key]
+
+    def decode(self, seq_ids, q, scale=None, out=None, layers=None, stream=None):
+        """q: device [num_layers, B, Hq, D] (or [B, Hq, D] for layer 0); returns out like q."""
+        import torch
+        stream = self._stream(stream)
+        tables, ctx = self.tables(seq_ids)
+        d_tables, d_ctx = self._upload([tables, ctx], stream)
+        d_tables = d_tables.view(tables.shape)
+        return self._decode_layers(seq_ids, q, scale, out, layers, d_tables, d_ctx, int(ctx.max(initial=0)),
+                                   stream)
+
+    def _decode_layers(self, seq_ids, q, scale, out, layers, d_tables, d_ctx, max_len, stream, marks=None):
+        import torch
+        one = q.dim() == 3
+        if scale is None:
+            scale = float(np.float32(1.0) / np.sqrt(np.float32(self.head_dim)))
+        if out is None:
+            out = torch.empty_like(q)
+        b, hq = q.shape[-3], q.shape[-2]
+        ws = self.workspace(b, hq, {torch.float16: "f16", torch.bfloat16: "bf16"}[q.dtype])
+        layers = ([0] if one else range(self.num_layers)) if layers is None else layers
+        if marks is not None:          # events bracketing the attention launches only
+            marks[0].record(stream)
+        for li in layers:
+            ks = self.k_scale[li] if self.k_scale is not None else None
+            vs = self.v_scale[li] if self.v_scale is not None else None
+            capi.paged_attention_decode(out if one else out[li], q if one else q[li], self.k[li], self.v[li],
+                                        ks, vs, d_tables, d_ctx, max_len, scale, ws, d_error=self.err,
+                                        stream=stream)
+        if marks is not None:
+            marks[1].record(stream)
+        return out
+
+    def step(self, seq_ids, k_rows, v_rows, q, scale=None, out=None, stream=None, marks=None):
+        """One decode step for all layers: append then attend (one metadata transfer).
+
+        ``marks``: optional pair of CUDA events recorded around the attention launches.
+        """
+        stream = self._stream(stream)
+        slots, cs, cd = capi.pkv_seq_append_slots(self.bm, seq_ids)
+        tables, ctx = self.tables(seq_ids)
+        d_slots, d_src, d_dst, d_tables, d_ctx = self._upload([slots, cs, cd, tables, ctx], stream)
+        self._apply_append(slots, cs, d_slots, d_src, d_dst, k_rows, v_rows, None, stream)
+        self.cow_pairs.extend(zip(cs.tolist(), cd.tolist()))
+        return self._decode_layers(seq_ids, q, scale, out, None, d_tables.view(tables.shape), d_ctx,
+                                   int(ctx.max(initial=0)), stream, marks)
+
+    def check(self, stream=None) -> int:
+        """Synchronise and return (and clear) the device error bits."""
+        return capi.pkv_read_device_error(self.err, clear=True, stream=self._stream(stream))
+
+
+def blocks_for(length: int) -> int:
+    return int(math.ceil(length / capi.BLOCK_SIZE))

@@ -1,0 +1,172 @@
+"""GPU parity of reshape-and-cache (append) and copy-on-write block copies.
+
+Bit-exact against the oracle: 16-bit caches hold the input bits; the FP8
+cache holds the oracle's E4M3 codes and fp32 scales, including an
+exhaustive sweep over every E4M3 value and every midpoint between two
+neighbours (round-to-nearest-even ties), subnormals, +-0 and saturation.
+"""
+import numpy as np
+import pytest
+
+from oracle import fp8
+from oracle.cache import PagedCacheModel
+from paged_kv_cache_163_gb300 import workloads as wl
+
+from helpers import cache_bits, oracle_bits
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from paged_kv_cache_163_gb300 import capi as c
+    c.load()
+    return c
+
+
+def run_append(capi, rows_k, rows_v, slots, num_blocks, hkv, d, in_dtype, cache_dtype):
+    from paged_kv_cache_163_gb300.engine import torch_dtype
+    dev = torch.device("cuda")
+    kc = torch.empty((num_blocks, hkv, 16, d), dtype=torch_dtype(cache_dtype), device=dev)
+    vc = torch.empty_like(kc)
+    kc.view(torch.uint8).fill_(0xFF)
+    vc.view(torch.uint8).fill_(0xFF)
+    ks = vs = None
+    if cache_dtype == "fp8_e4m3":
+        ks = torch.full((num_blocks, hkv, 16), float("nan"), device=dev)
+        vs = torch.full_like(ks, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    k = torch.from_numpy(rows_k).to(dev).to(torch_dtype(in_dtype))
+    v = torch.from_numpy(rows_v).to(dev).to(torch_dtype(in_dtype))
+    s = torch.from_numpy(np.asarray(slots, dtype=np.int32)).to(dev)
+    capi.paged_kv_append(k, v, s, kc, vc, ks, vs, d_error=err)
+    flag = capi.pkv_read_device_error(err)
+    return kc, vc, ks, vs, flag
+
+
+def compare_with_oracle(kc, vc, ks, vs, model: PagedCacheModel, cache_dtype):
+    filled = model.filled            # [blocks, 16]
+    if cache_dtype == "fp8_e4m3":
+        for got, want in ((cache_bits(kc), model.k), (cache_bits(vc), model.v)):
+            g = got.transpose(0, 2, 1, 3)[filled]      # [n, hkv, d]
+            w = want.transpose(0, 2, 1, 3)[filled]
+            assert np.array_equal(g, w), f"{np.sum(g != w)} codes differ"
+        for got, want in ((ks, model.k_scale), (vs, model.v_scale)):
+            g = got.cpu().numpy().transpose(0, 2, 1)[filled]
+            w = want.transpose(0, 2, 1)[filled]
+            assert np.array_equal(g.view(np.uint32), w.view(np.uint32))
+    else:
+        for got, want in ((cache_bits(kc), model.k), (cache_bits(vc), model.v)):
+            g = got.transpose(0, 2, 1, 3)[filled]
+            w = oracle_bits(want.transpose(0, 2, 1, 3)[filled], cache_dtype)
+            assert np.array_equal(g, w)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("in_dtype,cache_dtype", [("f16", "f16"), ("bf16", "bf16"),
+                                                  ("bf16", "fp8_e4m3"), ("f16", "fp8_e4m3")])
+def test_append_random_rows_bit_exact(capi, d, in_dtype, cache_dtype):
+    rng = np.random.default_rng(d + len(cache_dtype))
+    nb, hkv, t = 37, 4, 300
+    x = rng.standard_normal((2, t, hkv, d)).astype(np.float32)
+    x *= rng.uniform(1e-3, 30, (2, t, hkv, 1)).astype(np.float32)
+    x[:, ::17] *= 20                      # outlier tokens
+    x[:, 5, 1] = 0.0                      # an all-zero row
+    x[:, 6, 2] = -0.0
+    x = wl.round_to(x, in_dtype)
+    slots = rng.permutation(nb * 16)[:t].astype(np.int32)
+    slots[::23] = -1                      # skipped tokens
+    kc, vc, ks, vs, flag = run_append(capi, x[0], x[1], slots, nb, hkv, d, in_dtype, cache_dtype)
+    assert flag == 0
+    model = PagedCacheModel(nb, hkv, d, cache_dtype)
+    model.write(slots, x[0], x[1])
+    compare_with_oracle(kc, vc, ks, vs, model, cache_dtype)
+    # slots never written keep their poison bytes
+    untouched = ~model.filled
+    raw = kc.view(torch.uint8).cpu().numpy().reshape(nb, hkv, 16, -1).transpose(0, 2, 1, 3)[untouched]
+    assert np.all(raw == 0xFF)
+
+
+@pytest.mark.parametrize("in_dtype", ["bf16", "f16"])
+def test_fp8_grid_and_midpoint_sweep(capi, in_dtype):
+    """Rows whose amax is 448 (scale exactly 1): every E4M3 value and every tie."""
+    grid = fp8.decode_table()[:0x7F]                      # 0 .. 448
+    mids = (grid[:-1] + grid[1:]) / 2
+    vals = np.concatenate([grid, mids, -grid, -mids, [2.0 ** -11, 3 * 2.0 ** -11, -0.0]])
+    vals = vals[np.abs(vals) <= 448]
+    if in_dtype == "f16":                                 # keep values f16 can hold exactly
+        vals = vals[(vals == 0) | (np.abs(vals) >= 2.0 ** -24)]
+    d = 128
+    per = d - 1
+    n = -(-len(vals) // per)
+    rows = np.zeros((n, per), dtype=np.float64)
+    rows.flat[:len(vals)] = vals
+    rows = np.concatenate([np.full((n, 1), 448.0), rows], axis=1).astype(np.float32)
+    assert np.array_equal(wl.round_to(rows, in_dtype), rows)
+    x = rows[:, None, :]                                  # [n, 1 head, d]
+    slots = np.arange(n, dtype=np.int32)
+    nb = -(-n // 16)
+    kc, vc, ks, vs, flag = run_append(capi, x, -x, slots, nb, 1, d, in_dtype, "fp8_e4m3")
+    assert flag == 0
+    model = PagedCacheModel(nb, 1, d, "fp8_e4m3")
+    model.write(slots, x, -x)
+    assert np.all(model.k_scale.reshape(-1)[:n] == 1.0)
+    compare_with_oracle(kc, vc, ks, vs, model, "fp8_e4m3")
+
+
+def test_fp8_scale_ties_and_tiny_rows(capi):
+    """Rows whose amax makes x / s land on ties and subnormals after a real division."""
+    rng = np.random.default_rng(5)
+    d, hkv, t = 128, 2, 512
+    amax = wl.round_to(rng.uniform(1e-6, 1e4, (t, hkv)).astype(np.float32), "bf16")
+    codes = rng.integers(0, 0x7F, (t, hkv, d))
+    base = fp8.decode_table()[codes] / 448.0              # grid points scaled by amax / 448
+    x = wl.round_to((base * amax[..., None]).astype(np.float32), "bf16")
+    x[..., 0] = amax
+    x[..., 1::2] *= -1
+    slots = rng.permutation(64 * 16)[:t].astype(np.int32)
+    kc, vc, ks, vs, flag = run_append(capi, x, x[::-1].copy(), slots, 64, hkv, d, "bf16", "fp8_e4m3")
+    assert flag == 0
+    model = PagedCacheModel(64, hkv, d, "fp8_e4m3")
+    model.write(slots, x, x[::-1].copy())
+    compare_with_oracle(kc, vc, ks, vs, model, "fp8_e4m3")
+
+
+def test_bad_slot_sets_flag_and_skips(capi):
+    x = np.ones((3, 2, 64), dtype=np.float32)
+    kc, vc, ks, vs, flag = run_append(capi, x, x, [0, 5 * 16, 17], 4, 2, 64, "bf16", "bf16")
+    assert flag & capi.DEVERR_BAD_SLOT
+    raw = cache_bits(kc)
+    assert np.all(raw[0, :, 0] == 0x3F80) and np.all(raw[1, :, 1] == 0x3F80)
+
+
+@pytest.mark.parametrize("cache_dtype,d", [("bf16", 128), ("f16", 64), ("fp8_e4m3", 128)])
+def test_copy_blocks(capi, cache_dtype, d):
+    from paged_kv_cache_163_gb300.engine import torch_dtype
+    dev = torch.device("cuda")
+    nb, hkv = 20, 8
+    g = torch.Generator(device="cpu").manual_seed(3)
+    kc = torch.randint(0, 255, (nb, hkv, 16, d * (1 if cache_dtype == "fp8_e4m3" else 2)), generator=g,
+                       dtype=torch.uint8).to(dev)
+    vc = torch.randint(0, 255, kc.shape, generator=g, dtype=torch.uint8).to(dev)
+    kc_t, vc_t = kc.view(torch_dtype(cache_dtype)), vc.view(torch_dtype(cache_dtype))
+    ks = vs = None
+    if cache_dtype == "fp8_e4m3":
+        ks = torch.rand((nb, hkv, 16), generator=g).to(dev)
+        vs = torch.rand((nb, hkv, 16), generator=g).to(dev)
+    before = [t.clone() if t is not None else None for t in (kc, vc, ks, vs)]
+    src = torch.tensor([3, 7, 11], dtype=torch.int32, device=dev)
+    dst = torch.tensor([15, 0, 19], dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    capi.paged_kv_copy_blocks(kc_t, vc_t, ks, vs, src, dst, d_error=err)
+    assert capi.pkv_read_device_error(err) == 0
+    for now, old in zip((kc, vc, ks, vs), before):
+        if now is None:
+            continue
+        exp = old.clone()
+        exp[dst.long()] = old[src.long()]
+        assert torch.equal(now, exp)
+    bad = torch.tensor([25], dtype=torch.int32, device=dev)
+    capi.paged_kv_copy_blocks(kc_t, vc_t, ks, vs, bad, src[:1], d_error=err)
+    assert capi.pkv_read_device_error(err) & capi.DEVERR_BAD_BLOCK

@@ -1,0 +1,221 @@
+"""GPU parity of paged decode attention against the fp64 oracle.
+
+Every workload runs through the C ABI exactly as the benchmark does (host
+block manager -> append -> decode).  Integer results (block tables, slot
+mappings, copy-on-write pairs, cache bytes) must be bit-exact; attention
+outputs must satisfy max |err| <= 1e-2 and relative L2 <= 2e-3.
+
+Small workloads compare every output and every cache byte; the full-size
+ones compare every output for the oracle-sized ones (workloads 2-4) and
+sampled sequences plus sampled cache blocks for the 16 x 16K-32K FP8 one.
+"""
+import numpy as np
+import pytest
+
+from oracle.allocator import AllocatorModel
+from oracle.cache import quantize_rows
+from paged_kv_cache_163_gb300 import workloads as wl
+
+from helpers import (assert_close, cache_bits, check_rounding, oracle_bits, oracle_play, oracle_seq_output,
+                     to_f64)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def play():
+    from paged_kv_cache_163_gb300 import capi, play as p
+    capi.load()
+    return p
+
+
+def check_tables(cache, o, seqs):
+    t, lens = cache.tables(seqs)
+    mt, ml = o.alloc.block_tables(seqs, t.shape[1])
+    assert t.tolist() == mt and lens.tolist() == ml
+
+
+def check_cache_bytes(cache, o, w, layer=0):
+    model = o.layers[0]
+    filled = model.filled
+    if w.cache_dtype == "fp8_e4m3":
+        for got, want in ((cache.k[layer], model.k), (cache.v[layer], model.v)):
+            g = cache_bits(got).transpose(0, 2, 1, 3)[filled]
+            assert np.array_equal(g, want.transpose(0, 2, 1, 3)[filled])
+        for got, want in ((cache.k_scale[layer], model.k_scale), (cache.v_scale[layer], model.v_scale)):
+            g = got.cpu().numpy().transpose(0, 2, 1)[filled]
+            assert np.array_equal(g, want.transpose(0, 2, 1)[filled])
+    else:
+        for got, want in ((cache.k[layer], model.k), (cache.v[layer], model.v)):
+            g = cache_bits(got).transpose(0, 2, 1, 3)[filled]
+            assert np.array_equal(g, oracle_bits(want.transpose(0, 2, 1, 3)[filled], w.cache_dtype))
+
+
+def full_oracle_check(play, w, layers=1):
+    cache, out = play.run(w, poison=True, out_dtype="f32")
+    assert cache.check() == 0
+    o = oracle_play(w, layers=1)
+    check_tables(cache, o, w.seq_ids)
+    assert cache.cow_pairs == o.cow_log
+    check_cache_bytes(cache, o, w)
+    res = []
+    for li in range(layers):
+        ref = o.decode(w.seq_ids, w.q_rows(li), w.scale)
+        res.append(assert_close(to_f64(out[li]), ref, f"{w.name} layer {li}"))
+    check_rounding(cache, w, out)
+    assert cache.check() == 0
+    cache.close()
+    return res
+
+
+def test_tiny_gqa_fp16(play):
+    full_oracle_check(play, wl.make(1))
+
+
+def test_llama3_8b_shape_bf16(play):
+    full_oracle_check(play, wl.make(2))
+
+
+def test_prefix_sharing_bf16(play):
+    w = wl.make(4)
+    full_oracle_check(play, w)
+
+
+def test_mha_40_layers_fp16(play):
+    w = wl.make(3)
+    cache, out = play.run(w, poison=False, out_dtype="f32")
+    assert cache.check() == 0
+    # tables: logical block j of sequence b is physical j * 8 + b
+    t, lens = cache.tables(w.seq_ids)
+    assert np.array_equal(t, np.arange(128)[None, :] * 8 + np.arange(8)[:, None])
+    assert np.all(lens == 2048)
+    # all 40 layers hold the same K/V rows; queries differ per layer
+    K = [wl.round_to(w.kv_rows(0, s, 0, 2048), "f16").astype(np.float64) for s in range(8)]
+    V = [wl.round_to(w.kv_rows(1, s, 0, 2048), "f16").astype(np.float64) for s in range(8)]
+    from oracle.attention import decode_attention
+    for li in range(0, 40, 3):
+        q = w.q_rows(li)
+        ref = np.stack([decode_attention(q[s], K[s], V[s], w.scale) for s in range(8)])
+        assert_close(to_f64(out[li]), ref, f"layer {li}")
+    # cache bytes of sampled layers equal the input rows
+    for li in (0, 39):
+        got = cache_bits(cache.k[li])[t[3]]                     # [128, 32, 16, 128] of sequence 3
+        want = oracle_bits(K[3].reshape(128, 16, 32, 128).transpose(0, 2, 1, 3), "f16")
+        assert np.array_equal(got, want)
+    check_rounding(cache, w, out, layers=[0, 17, 39])
+    cache.close()
+
+
+def test_long_context_fp8_sampled(play):
+    w = wl.make(5)
+    cache, out = play.run(w, poison=False, out_dtype="f32")
+    assert cache.check() == 0
+    # tables bit-exact against the oracle allocator
+    model = AllocatorModel(w.num_blocks, 16, w.alloc_order)
+    for op in w.prefill_ops() + [("append", w.seq_ids)]:
+        if op[0] == "create":
+            model.create(op[1])
+        else:
+            model.append_slots(op[1])
+    t, lens = cache.tables(w.seq_ids)
+    mt, ml = model.block_tables(w.seq_ids, t.shape[1])
+    assert t.tolist() == mt and lens.tolist() == ml
+    q = w.q_rows(0)
+    got = to_f64(out[0])
+    rng = np.random.default_rng(0)
+    for s in sorted(set([int(np.argmax(w.context_lens)), int(np.argmin(w.context_lens))]
+                        + rng.choice(w.num_seqs, 2, replace=False).tolist())):
+        ref = oracle_seq_output(w, s, q[s])
+        assert_close(got[s], ref, f"sequence {s}")
+        # sampled blocks: codes and scales equal the oracle's quantisation of the rows
+        for lb in (0, int(lens[s] - 1) // 16):
+            rows_k = w.kv_rows(0, s, lb * 16, min(lb * 16 + 16, int(lens[s])))
+            codes, scales = quantize_rows(rows_k)
+            n = len(rows_k)
+            gk = cache_bits(cache.k[0][int(t[s, lb])])[:, :n].transpose(1, 0, 2)
+            gs = cache.k_scale[0][int(t[s, lb])][:, :n].cpu().numpy().T
+            assert np.array_equal(gk, codes) and np.array_equal(gs, scales)
+    check_rounding(cache, w, out)
+    cache.close()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("q_dtype,cache_dtype", [("f16", "f16"), ("bf16", "bf16"),
+                                                 ("bf16", "fp8_e4m3"), ("f16", "fp8_e4m3")])
+def test_every_instance_ragged(play, d, group, q_dtype, cache_dtype):
+    hkv = 2
+    lens = [1, 15, 16, 17, 31, 33, 200, 777, 2]
+    w = wl.custom(f"inst-{d}-{group}-{cache_dtype}", lens=lens, num_q_heads=hkv * group, num_kv_heads=hkv,
+                  head_dim=d, q_dtype=q_dtype, cache_dtype=cache_dtype, outlier_p=0.002,
+                  seed=d * 10 + group)
+    full_oracle_check(play, w)
+
+
+def test_one_long_sequence_among_short(play):
+    # one sequence holds most tiles: its (sequence, head) pairs are split across many warps
+    lens = [40000, 3, 16, 1, 100]
+    w = wl.custom("split-heavy", lens=lens, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                  q_dtype="bf16", cache_dtype="bf16", seed=9)
+    cache, out = play.run(w, out_dtype="f32")
+    assert cache.check() == 0
+    q = w.q_rows(0)
+    got = to_f64(out[0])
+    for s in range(len(lens)):
+        assert_close(got[s], oracle_seq_output(w, s, q[s]), f"sequence {s}")
+    cache.close()
+
+
+def test_max_batch_short_contexts(play):
+    lens = (np.arange(1024) % 70) + 1
+    w = wl.custom("max-batch", lens=lens, num_q_heads=8, num_kv_heads=2, head_dim=64, q_dtype="f16",
+                  cache_dtype="f16", seed=12)
+    cache, out = play.run(w, out_dtype="f32")
+    assert cache.check() == 0
+    q = w.q_rows(0)
+    got = to_f64(out[0])
+    for s in range(0, 1024, 37):
+        assert_close(got[s], oracle_seq_output(w, s, q[s]), f"sequence {s}")
+    cache.close()
+
+
+def test_empty_context_and_empty_batch(play):
+    from paged_kv_cache_163_gb300 import capi
+    w = wl.custom("with-empty", lens=[5, 40], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                  q_dtype="bf16", cache_dtype="bf16", seed=4)
+    cache = play.new_cache(w, poison=True)
+    play.prefill(w, cache)
+    cache.create(99)                                  # a sequence with no tokens
+    q = play.to_device(np.stack([w.q_rows(0)[0], w.q_rows(0)[1], w.q_rows(0)[0]]), "bf16", "cuda")
+    out = cache.decode([0, 1, 99], q, scale=w.scale, out=torch.empty(q.shape, device="cuda"))
+    assert cache.check() == 0
+    got = to_f64(out)
+    assert np.all(got[2] == 0.0)
+    for i, s in enumerate([0, 1]):
+        L = w.context_lens[s] - 1                     # pre-fill only: no decode-step append here
+        from oracle.attention import decode_attention
+        from oracle.cache import dequantize_rows
+        K = dequantize_rows(w.kv_rows(0, s, 0, L), "bf16")
+        V = dequantize_rows(w.kv_rows(1, s, 0, L), "bf16")
+        assert_close(got[i], decode_attention(q[i].float().cpu().numpy(), K, V, w.scale))
+    # an empty batch is a no-op
+    capi.paged_attention_decode(out[:0], q[:0], cache.k[0], cache.v[0], None, None,
+                                torch.zeros((0, 1), dtype=torch.int32, device="cuda"),
+                                torch.zeros(0, dtype=torch.int32, device="cuda"), 0, w.scale,
+                                cache.workspace(3, 8, "bf16"), num_seqs=0)
+    cache.close()
+
+
+def test_multi_step_decode_matches_oracle(play):
+    w = wl.make(2, extra_steps=4, num_seqs=6)
+    cache, out = play.run(w)
+    for step in range(1, 4):
+        k, v, q = play.step_inputs(w, step)
+        out = cache.step(w.seq_ids, k, v, q, scale=w.scale, out=torch.empty(q.shape, device="cuda"))
+        qh = w.q_rows(0, step)
+        got = to_f64(out[0])
+        for s in range(w.num_seqs):
+            assert_close(got[s], oracle_seq_output(w, s, qh[s], step=step), f"step {step} seq {s}")
+    assert cache.check() == 0
+    cache.close()

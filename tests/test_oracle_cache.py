@@ -15,7 +15,7 @@ from oracle.model import PagedKVOracle
 from paged_kv_cache_163_gb300 import workloads as wl
 
 
-def play(w, alloc_order=None, layers=1):
+def play(w, alloc_order=None, layers=1):  # same as helpers.oracle_play
     o = PagedKVOracle(layers, w.num_blocks, w.num_kv_heads, w.head_dim, w.cache_dtype,
                       alloc_order=w.alloc_order if alloc_order is None else alloc_order)
     for op in w.prefill_ops():
