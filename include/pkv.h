@@ -202,6 +202,32 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
                                   float scale, void *workspace, size_t workspace_bytes,
                                   int32_t *d_error, pkv_stream_t stream);
 
+/* Decode without a workspace argument, for callers that cannot allocate
+ * device memory: a plugin whose host framework owns every device
+ * allocation, or a latency-critical loop where an allocation could
+ * synchronise the device.  The pages have no counterpart of this call; it
+ * is a packaging variant of paged_attention_decode with the same arguments
+ * (minus workspace / workspace_bytes) and the same results.
+ * Scratch: a PKV_STATIC_SCRATCH_BYTES (16 MiB) __device__ buffer inside the
+ * library; every GPU that loads the library holds one until the process
+ * exits.  Shapes whose paged_attention_workspace_bytes exceeds it return
+ * PKV_ERR_WORKSPACE with the size in pkv_last_error().  The call allocates
+ * nothing.  Its first call on a device looks up the buffer's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls on a device share the buffer and it
+ * keeps the last call's contents (nothing in it needs to start at zero);
+ * calls whose kernels overlap on the GPU race, so serialise them. */
+#define PKV_STATIC_SCRATCH_BYTES (16u << 20)
+pkv_status paged_attention_decode_static(void *out, pkv_dtype out_dtype, const void *q,
+                                         pkv_dtype q_dtype, const void *k_cache, const void *v_cache,
+                                         pkv_dtype cache_dtype, const float *k_scale,
+                                         const float *v_scale, const int32_t *block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                         int32_t max_context_len, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t num_blocks, float scale, int32_t *d_error,
+                                         pkv_stream_t stream);
+
 /* Synchronise `stream`, copy *d_error to *h_error and, if clear != 0, zero
  * it.  Returns PKV_ERR_DEVICE_CHECK when any bit was set. */
 pkv_status pkv_read_device_error(int32_t *d_error, int32_t *h_error, int32_t clear,

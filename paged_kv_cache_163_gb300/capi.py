@@ -68,6 +68,9 @@ _PROTOS = {
     "paged_attention_decode": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, C.c_int, _vp, _vp, _vp, C.c_int32,
                                          _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                          C.c_int32, C.c_float, _vp, C.c_size_t, _vp, _vp]),
+    "paged_attention_decode_static": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, C.c_int, _vp, _vp, _vp,
+                                                C.c_int32, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                                C.c_int32, C.c_int32, C.c_float, _vp, _vp]),
     "pkv_read_device_error": (C.c_int, [_vp, _i32p, C.c_int32, _vp]),
     "pkv_launch_count": (C.c_int64, []),
     "pkv_status_string": (C.c_char_p, [C.c_int]),
@@ -290,6 +293,20 @@ def paged_attention_decode(out, q, k_cache, v_cache, k_scale, v_scale, block_tab
         _dp(v_scale), _dp(block_tables), block_tables.shape[-1], _dp(context_lens), int(max_context_len), b, hq,
         hkv, d, nb, float(scale), _dp(workspace), workspace.numel() * workspace.element_size(),
         _dp(d_error), _stream(stream)), "paged_attention_decode")
+
+
+def paged_attention_decode_static(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                                  max_context_len, scale, d_error=None, stream=None, num_seqs=None) -> None:
+    """paged_attention_decode with the library's static scratch (no workspace, no allocation)."""
+    b, hq, d = q.shape
+    if num_seqs is not None:
+        b = num_seqs
+    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    _check(load().paged_attention_decode_static(
+        _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_cache), _dp(v_cache), _dt(k_cache.dtype),
+        _dp(k_scale), _dp(v_scale), _dp(block_tables), block_tables.shape[-1], _dp(context_lens),
+        int(max_context_len), b, hq, hkv, d, nb, float(scale), _dp(d_error), _stream(stream)),
+        "paged_attention_decode_static")
 
 
 def pkv_read_device_error(d_error, clear: bool = True, stream=None, raise_on_error: bool = False) -> int:
