@@ -228,6 +228,62 @@ pkv_status paged_attention_decode_static(void *out, pkv_dtype out_dtype, const v
                                          int32_t num_blocks, float scale, int32_t *d_error,
                                          pkv_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Decode step executor: one call runs a whole decode step of a batch        */
+/* ("KV Cache 与 vLLM" §3.1-§3.4, "企业官网建设流程全解析" §3.2): the block    */
+/* manager gives every sequence a slot (taking or copying blocks), the slot   */
+/* mapping, copy pairs, lengths and block tables go to the device in one      */
+/* transfer, and for every layer the shared blocks are copied, the new K/V    */
+/* rows are written and the new queries attend.  Host work is O(batch +       */
+/* table size); all device work is enqueued on `stream`.                      */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t num_layers, num_blocks, num_kv_heads, num_q_heads, head_dim;
+  pkv_dtype q_dtype, cache_dtype;
+  void *k_cache, *v_cache;          /* layer 0; layer l at + l * cache_layer_stride bytes */
+  int64_t cache_layer_stride;
+  float *k_scale, *v_scale;         /* FP8 only (else NULL); layer l at + l * scale_layer_stride bytes */
+  int64_t scale_layer_stride;
+} pkv_pool_desc;
+
+typedef struct pkv_stepper pkv_stepper;
+
+/* Bytes of pinned host staging and of device metadata a stepper needs for
+ * batches of up to max_seqs sequences of up to max_blocks_per_seq blocks. */
+size_t pkv_stepper_host_bytes(int32_t max_seqs, int32_t max_blocks_per_seq);
+size_t pkv_stepper_device_bytes(int32_t max_seqs, int32_t max_blocks_per_seq);
+
+/* All buffers are caller-owned and must outlive the stepper: host_staging
+ * pinned host memory of pkv_stepper_host_bytes (double-buffered, each half
+ * guarded by an event), dev_meta device memory of pkv_stepper_device_bytes,
+ * workspace of paged_attention_workspace_bytes(max_seqs, ...).  The pool
+ * descriptor is copied.  The stepper creates two CUDA events, nothing else. */
+pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32_t max_blocks_per_seq,
+                              int32_t *host_staging, size_t host_staging_bytes, int32_t *dev_meta,
+                              size_t dev_meta_bytes, void *workspace, size_t workspace_bytes,
+                              pkv_stepper **out);
+void pkv_stepper_destroy(pkv_stepper *st);
+
+/* One decode step for seq_ids[0..n) (distinct).  Per layer l (byte strides):
+ * k_new, v_new + l * kv_layer_stride: [n][num_kv_heads][head_dim] rows of
+ * the new token in q_dtype (stride 0 reuses one tensor for every layer);
+ * q + l * q_layer_stride: [n][num_q_heads][head_dim] in q_dtype;
+ * out + l * out_layer_stride: same shape in out_dtype (F32 or q_dtype).
+ * Validated before anything changes: n <= max_seqs, every table stays within
+ * max_blocks_per_seq.  PKV_ERR_NO_BLOCKS leaves the block manager as it was.
+ * The copy pairs of the step are written to cow_src / cow_dst (host, [n],
+ * may be NULL) and their number to *num_cow (may be NULL).  Every layer's
+ * copies and appends are enqueued before the first layer's attention; the
+ * optional CUDA events attn_begin / attn_end (cudaEvent_t, may be NULL) are
+ * recorded on `stream` just before the first and just after the last
+ * attention launch, so a caller can time the attention alone. */
+pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids, int32_t n,
+                            const void *k_new, const void *v_new, int64_t kv_layer_stride,
+                            const void *q, int64_t q_layer_stride, void *out, pkv_dtype out_dtype,
+                            int64_t out_layer_stride, float scale, int32_t *cow_src, int32_t *cow_dst,
+                            int32_t *num_cow, int32_t *d_error, void *attn_begin, void *attn_end,
+                            pkv_stream_t stream);
+
 /* Synchronise `stream`, copy *d_error to *h_error and, if clear != 0, zero
  * it.  Returns PKV_ERR_DEVICE_CHECK when any bit was set. */
 pkv_status pkv_read_device_error(int32_t *d_error, int32_t *h_error, int32_t clear,

@@ -37,6 +37,17 @@ class NoBlocksError(PkvError):
 
 
 _lib = None
+
+
+class PoolDesc(C.Structure):
+    """pkv_pool_desc: per-layer pools as base pointers plus byte strides."""
+    _fields_ = [("num_layers", C.c_int32), ("num_blocks", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("num_q_heads", C.c_int32), ("head_dim", C.c_int32), ("q_dtype", C.c_int),
+                ("cache_dtype", C.c_int), ("k_cache", C.c_void_p), ("v_cache", C.c_void_p),
+                ("cache_layer_stride", C.c_int64), ("k_scale", C.c_void_p), ("v_scale", C.c_void_p),
+                ("scale_layer_stride", C.c_int64)]
+
+
 _i32p = C.POINTER(C.c_int32)
 _i64p = C.POINTER(C.c_int64)
 _vp = C.c_void_p
@@ -71,6 +82,13 @@ _PROTOS = {
     "paged_attention_decode_static": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, C.c_int, _vp, _vp, _vp,
                                                 C.c_int32, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                                 C.c_int32, C.c_int32, C.c_float, _vp, _vp]),
+    "pkv_stepper_host_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
+    "pkv_stepper_device_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
+    "pkv_stepper_create": (C.c_int, [C.POINTER(PoolDesc), C.c_int32, C.c_int32, _vp, C.c_size_t, _vp, C.c_size_t,
+                                     _vp, C.c_size_t, C.POINTER(_vp)]),
+    "pkv_stepper_destroy": (None, [_vp]),
+    "pkv_stepper_step": (C.c_int, [_vp, _vp, _i64p, C.c_int32, _vp, _vp, C.c_int64, _vp, C.c_int64, _vp, C.c_int,
+                                   C.c_int64, C.c_float, _i32p, _i32p, _i32p, _vp, _vp, _vp, _vp]),
     "pkv_read_device_error": (C.c_int, [_vp, _i32p, C.c_int32, _vp]),
     "pkv_launch_count": (C.c_int64, []),
     "pkv_status_string": (C.c_char_p, [C.c_int]),
@@ -307,6 +325,52 @@ def paged_attention_decode_static(out, q, k_cache, v_cache, k_scale, v_scale, bl
         _dp(k_scale), _dp(v_scale), _dp(block_tables), block_tables.shape[-1], _dp(context_lens),
         int(max_context_len), b, hq, hkv, d, nb, float(scale), _dp(d_error), _stream(stream)),
         "paged_attention_decode_static")
+
+
+def pkv_stepper_host_bytes(max_seqs, max_blocks_per_seq) -> int:
+    return int(load().pkv_stepper_host_bytes(max_seqs, max_blocks_per_seq))
+
+
+def pkv_stepper_device_bytes(max_seqs, max_blocks_per_seq) -> int:
+    return int(load().pkv_stepper_device_bytes(max_seqs, max_blocks_per_seq))
+
+
+def pkv_stepper_create(pool: PoolDesc, max_seqs, max_blocks_per_seq, host_staging, dev_meta, workspace):
+    h = _vp()
+    _check(load().pkv_stepper_create(C.byref(pool), max_seqs, max_blocks_per_seq, host_staging.data_ptr(),
+                                     host_staging.numel() * host_staging.element_size(), _dp(dev_meta),
+                                     dev_meta.numel() * dev_meta.element_size(), _dp(workspace),
+                                     workspace.numel() * workspace.element_size(), C.byref(h)),
+           "pkv_stepper_create")
+    return h
+
+
+def pkv_stepper_destroy(st) -> None:
+    load().pkv_stepper_destroy(st)
+
+
+def _layer_stride(t, layers):
+    """Byte stride between layers of a per-layer tensor ([layers, ...] or one tensor for all: 0)."""
+    return t.stride(0) * t.element_size() if t.dim() == 4 and layers > 1 else 0
+
+
+def pkv_stepper_step(st, bm, seq_ids, k_new, v_new, q, out, scale, layers, d_error=None, events=None,
+                     stream=None):
+    """One decode step; returns (cow_src, cow_dst) of the step."""
+    ids = _i64(seq_ids)
+    n = len(ids)
+    src = np.empty(max(n, 1), np.int32)
+    dst = np.empty(max(n, 1), np.int32)
+    ncow = C.c_int32()
+    ev0 = ev1 = None
+    if events is not None:
+        ev0, ev1 = (e.cuda_event for e in events)
+    _check(load().pkv_stepper_step(
+        st, bm, _ptr(ids, C.c_int64), n, _dp(k_new), _dp(v_new), _layer_stride(k_new, layers), _dp(q),
+        _layer_stride(q, layers), _dp(out), _dt(out.dtype), _layer_stride(out, layers), float(scale),
+        _ptr(src, C.c_int32), _ptr(dst, C.c_int32), C.byref(ncow), _dp(d_error), ev0, ev1, _stream(stream)),
+        "pkv_stepper_step")
+    return src[:ncow.value].copy(), dst[:ncow.value].copy()
 
 
 def pkv_read_device_error(d_error, clear: bool = True, stream=None, raise_on_error: bool = False) -> int:

@@ -443,16 +443,23 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
 
 // One CTA per (sequence, KV head): merge the partials of the warps that
 // shared it, out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+// The partial maxima and sums are reduced across the CTA first; then each
+// thread accumulates its output elements over the partials with independent,
+// coalesced loads.
 template <int D, int G, int QDT>
 __global__ void __launch_bounds__(128) paged_reduce_kernel(const DecodeParams p, int64_t nwarps) {
+  __shared__ float s_red[4][G];
+  __shared__ float s_m[G];
+  __shared__ float s_inv[G];
   const int item = blockIdx.x;
   const int b = item / p.num_kv_heads;
   const int kvh = item - b * p.num_kv_heads;
   const int32_t *cum = p.ws_cum;
   const int nb = cum[b + 1] - cum[b];
   const size_t obase = static_cast<size_t>(item) * G * D;  // element index of this item's output
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   if (nb == 0) {
-    for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) {
+    for (int i = tid; i < G * D / 2; i += blockDim.x) {
       if (p.out_f32) reinterpret_cast<float2 *>(p.out)[obase / 2 + i] = make_float2(0.f, 0.f);
       else reinterpret_cast<uint32_t *>(p.out)[obase / 2 + i] = 0u;
     }
@@ -465,28 +472,65 @@ __global__ void __launch_bounds__(128) paged_reduce_kernel(const DecodeParams p,
   const int64_t w_first = ((start + 1) * nwarps - 1) / total;
   const int64_t w_last = ((last + 1) * nwarps - 1) / total;
   if (w_first == w_last) return;  // written by the decode kernel
-  for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) {
+  // With fewer tiles than warps some warps own nothing and wrote no partial.
+  const bool all_own = total >= nwarps;
+  auto owns = [&](int64_t w) { return all_own || (w * total / nwarps) != ((w + 1) * total / nwarps); };
+  const float *ml = p.ws_ml + (w_first + item) * G * 2;  // partial of warp w at ml[(w - w_first) * 2G]
+  const int np = static_cast<int>(w_last - w_first + 1);
+
+  float v[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) v[g] = -INFINITY;
+  for (int k = tid; k < np; k += blockDim.x)
+    if (owns(w_first + k))
+#pragma unroll
+      for (int g = 0; g < G; ++g) v[g] = fmaxf(v[g], ml[(k * G + g) * 2]);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v[g] = fmaxf(v[g], __shfl_xor_sync(kFull, v[g], o));
+    if (lane == 0) s_red[wid][g] = v[g];
+  }
+  __syncthreads();
+  if (tid < G) s_m[tid] = fmaxf(fmaxf(s_red[0][tid], s_red[1][tid]), fmaxf(s_red[2][tid], s_red[3][tid]));
+  __syncthreads();
+#pragma unroll
+  for (int g = 0; g < G; ++g) v[g] = 0.f;
+  for (int k = tid; k < np; k += blockDim.x)
+    if (owns(w_first + k))
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float mk = ml[(k * G + g) * 2];
+        if (mk != -INFINITY) v[g] = fmaf(exp2f(mk - s_m[g]), ml[(k * G + g) * 2 + 1], v[g]);
+      }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v[g] += __shfl_xor_sync(kFull, v[g], o);
+    if (lane == 0) s_red[wid][g] = v[g];
+  }
+  __syncthreads();
+  if (tid < G) {
+    const float den = s_red[0][tid] + s_red[1][tid] + s_red[2][tid] + s_red[3][tid];
+    s_inv[tid] = den > 0.f ? 1.f / den : 0.f;
+  }
+  __syncthreads();
+  const float *po = p.ws_o + (w_first + item) * G * D;  // partial o of warp w at po[(w - w_first) * G * D]
+  for (int i = tid; i < G * D / 2; i += blockDim.x) {
     const int g = (2 * i) / D;
     const int dd = (2 * i) % D;
-    // warps whose share is empty (more warps than tiles) wrote no partial
-    auto empty = [&](int64_t w) { return (w * total / nwarps) == ((w + 1) * total / nwarps); };
-    float mmax = -INFINITY;
-    for (int64_t w = w_first; w <= w_last; ++w)
-      if (!empty(w)) mmax = fmaxf(mmax, p.ws_ml[((w + item) * G + g) * 2]);
-    float num0 = 0.f, num1 = 0.f, den = 0.f;
-    for (int64_t w = w_first; w <= w_last; ++w) {
-      if (empty(w)) continue;
-      const int64_t slot = w + item;
-      const float ms = p.ws_ml[(slot * G + g) * 2];
-      if (ms == -INFINITY) continue;
-      const float sc = exp2f(ms - mmax);
-      const float2 ov = *reinterpret_cast<const float2 *>(p.ws_o + (slot * G + g) * D + dd);
-      num0 = fmaf(sc, ov.x, num0);
-      num1 = fmaf(sc, ov.y, num1);
-      den = fmaf(sc, p.ws_ml[(slot * G + g) * 2 + 1], den);
+    const float mg = s_m[g];
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < np; ++k) {
+      const float mk = ml[(k * G + g) * 2];
+      if (mk == -INFINITY || !owns(w_first + k)) continue;
+      const float sc = exp2f(mk - mg);
+      const float2 ov = *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(k) * G * D + g * D + dd);
+      a0 = fmaf(sc, ov.x, a0);
+      a1 = fmaf(sc, ov.y, a1);
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    const float r0 = num0 * inv, r1 = num1 * inv;
+    const float r0 = a0 * s_inv[g], r1 = a1 * s_inv[g];
     if (p.out_f32) reinterpret_cast<float2 *>(p.out)[obase / 2 + i] = make_float2(r0, r1);
     else reinterpret_cast<uint32_t *>(p.out)[obase / 2 + i] = pack2<QDT>(r0, r1);
   }

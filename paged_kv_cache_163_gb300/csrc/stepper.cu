@@ -1,0 +1,192 @@
+// Decode step executor: host block manager, one metadata transfer and every
+// layer's copy / append / decode launches in a single native call.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "append.h"
+#include "pkv.h"
+#include "status.h"
+
+struct pkv_stepper {
+  pkv_pool_desc pool;
+  int32_t max_seqs = 0, max_blocks = 0;
+  int32_t *host = nullptr;      // two halves of `half_ints` int32
+  int32_t *dev = nullptr;
+  size_t half_ints = 0;
+  void *workspace = nullptr;
+  size_t workspace_bytes = 0;
+  cudaEvent_t done[2] = {nullptr, nullptr};
+  int next = 0;
+};
+
+namespace {
+
+// Layout of one metadata half: slots[n] | cow_src[n] | cow_dst[n] | lens[n] | tables[n][mb]
+size_t meta_ints(int32_t max_seqs, int32_t max_blocks) {
+  return static_cast<size_t>(max_seqs) * 4 + static_cast<size_t>(max_seqs) * max_blocks;
+}
+
+
+pkv_status cuda_fail(cudaError_t e, const char *where) {
+  std::string msg = std::string(where) + ": " + cudaGetErrorString(e);
+  return pkv::fail(PKV_ERR_CUDA, msg.c_str());
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_stepper_host_bytes(int32_t max_seqs, int32_t max_blocks_per_seq) {
+  if (max_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
+  return 2 * meta_ints(max_seqs, max_blocks_per_seq) * sizeof(int32_t);
+}
+
+size_t pkv_stepper_device_bytes(int32_t max_seqs, int32_t max_blocks_per_seq) {
+  if (max_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
+  return meta_ints(max_seqs, max_blocks_per_seq) * sizeof(int32_t);
+}
+
+pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32_t max_blocks_per_seq,
+                              int32_t *host_staging, size_t host_staging_bytes, int32_t *dev_meta,
+                              size_t dev_meta_bytes, void *workspace, size_t workspace_bytes,
+                              pkv_stepper **out) {
+  if (!pool || !out || max_seqs <= 0 || max_seqs > PKV_MAX_SEQS_PER_CALL || max_blocks_per_seq <= 0)
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: bad argument");
+  if (pool->num_layers <= 0 || pool->num_blocks <= 0 || pool->num_kv_heads <= 0 || !pool->k_cache ||
+      !pool->v_cache || (pool->cache_dtype == PKV_FP8_E4M3 && (!pool->k_scale || !pool->v_scale)))
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: bad pool descriptor");
+  if (!host_staging || host_staging_bytes < pkv_stepper_host_bytes(max_seqs, max_blocks_per_seq) ||
+      !dev_meta || dev_meta_bytes < pkv_stepper_device_bytes(max_seqs, max_blocks_per_seq))
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: staging or metadata buffer too small");
+  size_t need = 0;
+  pkv_status s = paged_attention_workspace_bytes(max_seqs, pool->num_q_heads, pool->num_kv_heads, pool->head_dim,
+                                                 pool->q_dtype, pool->cache_dtype, &need);
+  if (s != PKV_OK) return s;
+  if (!workspace || workspace_bytes < need)
+    return pkv::fail(PKV_ERR_WORKSPACE, "pkv_stepper_create: workspace smaller than required");
+  pkv_stepper *st = new pkv_stepper();
+  st->pool = *pool;
+  st->max_seqs = max_seqs;
+  st->max_blocks = max_blocks_per_seq;
+  st->host = host_staging;
+  st->dev = dev_meta;
+  st->half_ints = meta_ints(max_seqs, max_blocks_per_seq);
+  st->workspace = workspace;
+  st->workspace_bytes = workspace_bytes;
+  for (int i = 0; i < 2; ++i) {
+    cudaError_t e = cudaEventCreateWithFlags(&st->done[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      pkv_stepper_destroy(st);
+      return cuda_fail(e, "pkv_stepper_create: cudaEventCreate");
+    }
+  }
+  *out = st;
+  return PKV_OK;
+}
+
+void pkv_stepper_destroy(pkv_stepper *st) {
+  if (!st) return;
+  for (auto &e : st->done)
+    if (e) cudaEventDestroy(e);
+  delete st;
+}
+
+pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids, int32_t n,
+                            const void *k_new, const void *v_new, int64_t kv_layer_stride,
+                            const void *q, int64_t q_layer_stride, void *out, pkv_dtype out_dtype,
+                            int64_t out_layer_stride, float scale, int32_t *cow_src, int32_t *cow_dst,
+                            int32_t *num_cow, int32_t *d_error, void *attn_begin, void *attn_end,
+                            pkv_stream_t stream) {
+  if (!st || !bm || n < 0 || n > st->max_seqs || (n > 0 && (!seq_ids || !k_new || !v_new || !q || !out)))
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: bad argument");
+  if (num_cow) *num_cow = 0;
+  if (n == 0) return PKV_OK;
+  const pkv_pool_desc &P = st->pool;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // Validate before the block manager changes: distinct sequences whose
+  // tables stay within max_blocks after this step's token.
+  int32_t mb = 1, max_len = 0;
+  {
+    std::unordered_map<int64_t, int> seen;
+    for (int32_t i = 0; i < n; ++i) {
+      if (!seen.emplace(seq_ids[i], 1).second)
+        return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: a sequence appears twice in the batch");
+      int32_t len = 0;
+      pkv_status s = pkv_seq_len(bm, seq_ids[i], &len);
+      if (s != PKV_OK) return s;
+      const int32_t after = len + 1;
+      const int32_t blocks = (after + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+      if (blocks > st->max_blocks)
+        return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: a table would exceed max_blocks_per_seq");
+      mb = std::max(mb, blocks);
+      max_len = std::max(max_len, after);
+    }
+  }
+  // Host staging half: wait until the transfer that last read it is done.
+  const int h = st->next;
+  cudaError_t e = cudaEventSynchronize(st->done[h]);
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventSynchronize");
+  int32_t *H = st->host + h * st->half_ints;
+  int32_t *slots = H, *src = H + n, *dst = H + 2 * n, *lens = H + 3 * n, *tables = H + 4 * n;
+  int32_t ncow = 0;
+  pkv_status s = pkv_seq_append_slots(bm, seq_ids, n, slots, src, dst, &ncow);
+  if (s != PKV_OK) return s;
+  s = pkv_build_block_tables(bm, seq_ids, n, mb, tables, lens);
+  if (s != PKV_OK) return s;
+  if (num_cow) *num_cow = ncow;
+  if (cow_src && ncow) std::memcpy(cow_src, src, sizeof(int32_t) * ncow);
+  if (cow_dst && ncow) std::memcpy(cow_dst, dst, sizeof(int32_t) * ncow);
+  const size_t ints = static_cast<size_t>(n) * 4 + static_cast<size_t>(n) * mb;
+  e = cudaMemcpyAsync(st->dev, H, ints * sizeof(int32_t), cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaEventRecord(st->done[h], cs);
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: metadata transfer");
+  st->next ^= 1;
+  const int32_t *d_slots = st->dev, *d_src = st->dev + n, *d_dst = st->dev + 2 * n;
+  const int32_t *d_lens = st->dev + 3 * n, *d_tables = st->dev + 4 * n;
+
+  auto layer_ptr = [](const void *base, int64_t stride, int32_t l) {
+    return static_cast<uint8_t *>(const_cast<void *>(base)) + l * stride;
+  };
+  auto scale_ptr = [&](float *base, int32_t l) {
+    return base ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(base) + l * P.scale_layer_stride) : nullptr;
+  };
+  for (int32_t l = 0; l < P.num_layers; ++l) {
+    uint8_t *kc = layer_ptr(P.k_cache, P.cache_layer_stride, l);
+    uint8_t *vc = layer_ptr(P.v_cache, P.cache_layer_stride, l);
+    float *ks = scale_ptr(P.k_scale, l), *vs = scale_ptr(P.v_scale, l);
+    if (ncow) {
+      s = paged_kv_copy_blocks(kc, vc, ks, vs, d_src, d_dst, ncow, P.num_kv_heads, P.head_dim, P.cache_dtype,
+                               P.num_blocks, d_error, stream);
+      if (s != PKV_OK) return s;
+    }
+    s = paged_kv_append(layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l), P.q_dtype, n,
+                        P.num_kv_heads, P.head_dim, d_slots, kc, vc, P.cache_dtype, ks, vs, P.num_blocks, d_error,
+                        stream);
+    if (s != PKV_OK) return s;
+  }
+  if (attn_begin) {
+    e = cudaEventRecord(static_cast<cudaEvent_t>(attn_begin), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");
+  }
+  for (int32_t l = 0; l < P.num_layers; ++l) {
+    s = paged_attention_decode(layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l),
+                               P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
+                               layer_ptr(P.v_cache, P.cache_layer_stride, l), P.cache_dtype, scale_ptr(P.k_scale, l),
+                               scale_ptr(P.v_scale, l), d_tables, mb, d_lens, max_len, n, P.num_q_heads,
+                               P.num_kv_heads, P.head_dim, P.num_blocks, scale, st->workspace, st->workspace_bytes,
+                               d_error, stream);
+    if (s != PKV_OK) return s;
+  }
+  if (attn_end) {
+    e = cudaEventRecord(static_cast<cudaEvent_t>(attn_end), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

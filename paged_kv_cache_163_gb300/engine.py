@@ -80,9 +80,15 @@ class PagedKVCache:
         self._ring = _PinnedRing()
         self._meta = torch.empty(1024, dtype=torch.int32, device=self.device)
         self._ws = {}
+        self._stepper = None
+        self._stepper_key = None
+        self._stepper_bufs = None
         self.cow_pairs = []          # every (src, dst) copy, in order
 
     def close(self):
+        if self._stepper is not None:
+            capi.pkv_stepper_destroy(self._stepper)
+            self._stepper = None
         if self.bm is not None:
             capi.pkv_bm_destroy(self.bm)
             self.bm = None
@@ -209,19 +215,58 @@ class PagedKVCache:
             marks[1].record(stream)
         return out
 
-    def step(self, seq_ids, k_rows, v_rows, q, scale=None, out=None, stream=None, marks=None):
-        """One decode step for all layers: append then attend (one metadata transfer).
+    def _stepper_for(self, n: int, num_q_heads: int, q_dtype: str):
+        """The native step executor for batches of n sequences (created on first use)."""
+        import torch
+        key = (n, num_q_heads, q_dtype)
+        if self._stepper is not None and self._stepper_key == key:
+            return self._stepper
+        if self._stepper is not None:
+            torch.cuda.synchronize(self.device)
+            capi.pkv_stepper_destroy(self._stepper)
+            self._stepper = None
+        max_blocks = self.num_blocks
+        host = torch.empty(capi.pkv_stepper_host_bytes(n, max_blocks) // 4, dtype=torch.int32, pin_memory=True)
+        dev = torch.empty(capi.pkv_stepper_device_bytes(n, max_blocks) // 4, dtype=torch.int32, device=self.device)
+        ws = self.workspace(n, num_q_heads, q_dtype)
+        kb = self.k.element_size()
+        pool = capi.PoolDesc(
+            num_layers=self.num_layers, num_blocks=self.num_blocks, num_kv_heads=self.num_kv_heads,
+            num_q_heads=num_q_heads, head_dim=self.head_dim, q_dtype=capi.DTYPE_NAMES[q_dtype],
+            cache_dtype=capi.DTYPE_NAMES[self.cache_dtype], k_cache=self.k.data_ptr(), v_cache=self.v.data_ptr(),
+            cache_layer_stride=self.k.stride(0) * kb,
+            k_scale=self.k_scale.data_ptr() if self.k_scale is not None else None,
+            v_scale=self.v_scale.data_ptr() if self.v_scale is not None else None,
+            scale_layer_stride=self.k_scale.stride(0) * 4 if self.k_scale is not None else 0)
+        self._stepper = capi.pkv_stepper_create(pool, n, max_blocks, host, dev, ws)
+        self._stepper_bufs = (host, dev, ws)
+        self._stepper_key = key
+        return self._stepper
 
-        ``marks``: optional pair of CUDA events recorded around the attention launches.
+    def step(self, seq_ids, k_rows, v_rows, q, scale=None, out=None, stream=None, marks=None):
+        """One decode step for all layers through the native executor: append then attend.
+
+        k_rows / v_rows: [num_layers, B, Hkv, D] (or [B, Hkv, D] for every layer);
+        q, out: [num_layers, B, Hq, D] (or [B, Hq, D] with one layer); out may be
+        float32 or q's dtype.  ``marks``: optional pair of CUDA events recorded
+        around the attention launches.
         """
+        import torch
         stream = self._stream(stream)
-        slots, cs, cd = capi.pkv_seq_append_slots(self.bm, seq_ids)
-        tables, ctx = self.tables(seq_ids)
-        d_slots, d_src, d_dst, d_tables, d_ctx = self._upload([slots, cs, cd, tables, ctx], stream)
-        self._apply_append(slots, cs, d_slots, d_src, d_dst, k_rows, v_rows, None, stream)
+        if scale is None:
+            scale = float(np.float32(1.0) / np.sqrt(np.float32(self.head_dim)))
+        if out is None:
+            out = torch.empty_like(q)
+        qname = {torch.float16: "f16", torch.bfloat16: "bf16"}[q.dtype]
+        st = self._stepper_for(len(seq_ids), q.shape[-2], qname)
+        if marks is not None:
+            for ev in marks:
+                if ev.cuda_event == 0:     # torch creates the event on its first record
+                    ev.record(stream)
+        cs, cd = capi.pkv_stepper_step(st, self.bm, seq_ids, k_rows, v_rows, q, out, scale, self.num_layers,
+                                       d_error=self.err, events=marks, stream=stream)
         self.cow_pairs.extend(zip(cs.tolist(), cd.tolist()))
-        return self._decode_layers(seq_ids, q, scale, out, None, d_tables.view(tables.shape), d_ctx,
-                                   int(ctx.max(initial=0)), stream, marks)
+        return out
 
     def check(self, stream=None) -> int:
         """Synchronise and return (and clear) the device error bits."""

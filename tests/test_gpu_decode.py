@@ -219,3 +219,28 @@ def test_multi_step_decode_matches_oracle(play):
             assert_close(got[s], oracle_seq_output(w, s, qh[s], step=step), f"step {step} seq {s}")
     assert cache.check() == 0
     cache.close()
+
+
+def test_copy_on_write_inside_the_step(play):
+    # every sequence's first own token lands in the shared 12-token partial block during the step
+    w = wl.custom("cow-step", lens=[1501] * 6, num_q_heads=32, num_kv_heads=8, head_dim=128, q_dtype="bf16",
+                  cache_dtype="bf16", prefix_len=1500, seed=31)
+    full_oracle_check(play, w)
+
+
+def test_stepper_rejects_bad_batches_without_changes(play):
+    from paged_kv_cache_163_gb300 import capi
+    w = wl.custom("tight", lens=[16, 16], num_q_heads=8, num_kv_heads=2, head_dim=64, q_dtype="f16",
+                  cache_dtype="f16", seed=5, slack=0.0)
+    cache, _ = play.run(w)                    # 2 sequences of 16 tokens fill the 2-block pool
+    assert capi.pkv_bm_num_free(cache.bm) == 0
+    k, v, q = play.step_inputs(w, 1)
+    before = [cache.seq_len(s) for s in w.seq_ids]
+    with pytest.raises(capi.NoBlocksError):   # the 17th tokens need new blocks
+        cache.step(w.seq_ids, k, v, q, scale=w.scale)
+    assert [cache.seq_len(s) for s in w.seq_ids] == before
+    with pytest.raises(capi.PkvError):
+        cache.step([0, 0], k, v, q, scale=w.scale)
+    assert [cache.seq_len(s) for s in w.seq_ids] == before
+    assert cache.check() == 0
+    cache.close()
