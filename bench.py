@@ -66,6 +66,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--kernel", choices=["auto", "simt", "mma"], default="auto",
+                    help="decode kernel variant (auto: tensor-core tiles for head_dim 128)")
     return ap.parse_args(argv)
 
 
@@ -74,6 +76,22 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of per-rank values (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world: int, units_per_rank: float, seconds_max: float) -> float:
+    """Units all ranks processed over the slowest rank's time (weak scaling: equal shards)."""
+    return world * units_per_rank / seconds_max
 
 
 def measured_peak():
@@ -190,6 +208,7 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     capi.load()
+    capi.pkv_set_decode_kernel(args.kernel)
     wid = WORKLOADS[args.workload]
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
     total_steps = args.warmup + args.steps + e2e_steps
@@ -242,10 +261,7 @@ def run_ours(args, world, rank, local):
     tok_total = sum(a["tokens"] for a in steps_acc)
     t_total = sum(step_ms) / 1e3
     t_attn = sum(attn_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([t_total, t_attn], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_total, t_attn = t.tolist()
+    t_total, t_attn = max_over_ranks([t_total, t_attn], device=dev)
 
     # end to end: inputs from pinned host memory, result read back, every step
     e2e = None
@@ -257,7 +273,7 @@ def run_ours(args, world, rank, local):
     per_launch_s = t_attn / (args.steps * w.num_layers)
     achieved = per_launch_bytes / per_launch_s / 1e9
     traffic = NCU_TRAFFIC.get((args.workload, kernel_hash()))
-    value = world * kv_total / t_total / 1e9
+    value = whole_job_rate(world, kv_total, t_total) / 1e9
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -271,7 +287,8 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": w.cache_dtype if w.cache_dtype != "fp8_e4m3" else "fp8_e4m3 (bf16 q, fp32 accumulate)",
         "data": "synthetic (seeded N(0,1); no dataset or weights)",
-        "config": workload_config(w, args.workload, {"parallelism": f"replicas x{world} (sequences sharded)"}),
+        "config": workload_config(w, args.workload, {"parallelism": f"replicas x{world} (sequences sharded)",
+                                                     "decode_kernel": args.kernel}),
         "hbm_frac_step": round(value / world / peak, 4),
         "seq_tokens_per_s_per_layer": round(world * tok_total / (t_total / w.num_layers), 1),
         "attn_only": {"kv_read_gbs": round(kv_total / t_attn / 1e9, 2),

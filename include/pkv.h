@@ -167,6 +167,14 @@ pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int
                            float *v_scale, int32_t num_blocks, int32_t *d_error,
                            pkv_stream_t stream);
 
+/* Which decode kernel runs.  SIMT: CUDA-core dot products (any head_dim).
+ * MMA: tensor-core mma.sync m16n8k16 tiles fed by swizzled tensor TMA
+ * (head_dim 128; other head_dims use SIMT).  AUTO (default) picks MMA for
+ * head_dim 128.  Process-wide; affects calls issued after it. */
+typedef enum { PKV_DECODE_AUTO = 0, PKV_DECODE_SIMT = 1, PKV_DECODE_MMA = 2 } pkv_decode_kernel;
+pkv_status pkv_set_decode_kernel(pkv_decode_kernel kind);
+pkv_decode_kernel pkv_get_decode_kernel(void);
+
 /* Device workspace (bytes) paged_attention_decode needs for these shapes on
  * the current device (split-KV partials).  Depends on the device's SM count. */
 pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,

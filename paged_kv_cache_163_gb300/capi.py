@@ -91,6 +91,8 @@ _PROTOS = {
                                    C.c_int64, C.c_float, _i32p, _i32p, _i32p, _vp, _vp, _vp, _vp]),
     "pkv_read_device_error": (C.c_int, [_vp, _i32p, C.c_int32, _vp]),
     "pkv_launch_count": (C.c_int64, []),
+    "pkv_set_decode_kernel": (C.c_int, [C.c_int]),
+    "pkv_get_decode_kernel": (C.c_int, []),
     "pkv_status_string": (C.c_char_p, [C.c_int]),
     "pkv_last_error": (C.c_char_p, []),
 }
@@ -379,6 +381,19 @@ def pkv_read_device_error(d_error, clear: bool = True, stream=None, raise_on_err
     if st != -5 or raise_on_error:
         _check(st, "pkv_read_device_error")
     return h.value
+
+
+DECODE_KERNELS = {"auto": 0, "simt": 1, "mma": 2}
+
+
+def pkv_set_decode_kernel(kind) -> None:
+    """Select the decode kernel process-wide: 'auto', 'simt' or 'mma'."""
+    _check(load().pkv_set_decode_kernel(DECODE_KERNELS.get(kind, kind)), "pkv_set_decode_kernel")
+
+
+def pkv_get_decode_kernel() -> str:
+    v = int(load().pkv_get_decode_kernel())
+    return {k: n for n, k in DECODE_KERNELS.items()}[v]
 
 
 def pkv_launch_count() -> int:

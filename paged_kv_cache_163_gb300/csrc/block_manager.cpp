@@ -233,8 +233,9 @@ static int64_t elem_bytes_per_token_head(int32_t head_dim, pkv_dtype dt) {
       return 2 * static_cast<int64_t>(head_dim);
     case PKV_FP8_E4M3:
       return static_cast<int64_t>(head_dim) + 4;  // codes + one fp32 scale
+    default:
+      return -1;  // not a cache type
   }
-  return -1;
 }
 
 int64_t pkv_kv_bytes(int32_t layers, int32_t kv_heads, int32_t head_dim, int64_t tokens,

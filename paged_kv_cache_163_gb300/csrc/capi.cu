@@ -1,9 +1,15 @@
 // C ABI of the device calls: argument validation, launch configuration,
 // workspace layout.  Kernels live in append.cu and decode_*.cu.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdio>
+#include <mutex>
 #include <string>
+#include <tuple>
+#include <unordered_map>
 
 #include "append.h"
 #include "decode.h"
@@ -33,7 +39,72 @@ int sm_count() {
   return n;
 }
 
+std::atomic<int> g_decode_kind{PKV_DECODE_AUTO};
+
 using DecodeFn = cudaError_t (*)(int, int, int, const DecodeParams *, int, int64_t *, int *);
+using MmaFn = cudaError_t (*)(int, int, const DecodeParams *, const CUtensorMap *, const CUtensorMap *, int,
+                              int64_t *, int *);
+
+MmaFn pick_mma(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
+  if (cache_dtype == PKV_F16 && q_dtype == PKV_F16) return decode_mma_call_f16;
+  if (cache_dtype == PKV_BF16 && q_dtype == PKV_BF16) return decode_mma_call_bf16;
+  if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_F16) return decode_mma_call_fp8_f16;
+  if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_BF16) return decode_mma_call_fp8_bf16;
+  return nullptr;
+}
+
+bool use_mma(int32_t head_dim) {
+  const int k = g_decode_kind.load();
+  return head_dim == 128 && k != PKV_DECODE_SIMT;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2D map of one layer's K or V pool: rows of 128 elements, box [64 or 128 elements][16 rows],
+// 128-byte swizzle.  Encoded maps are cached by (address, rows, element size).
+pkv_status cache_tensor_map(const void *base, int64_t rows, int esz, CUtensorMap *out) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, std::pair<int64_t, CUtensorMap>> cache;
+  const uint64_t key = reinterpret_cast<uint64_t>(base) ^ static_cast<uint64_t>(esz);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end() && it->second.first == rows) {
+      *out = it->second.second;
+      return PKV_OK;
+    }
+  }
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(PKV_ERR_CUDA, "decode: cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(128 * esz)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(esz == 1 ? 128 : 64), 16};
+  const cuuint32_t elem[2] = {1, 1};
+  CUtensorMap m;
+  CUresult r = enc(&m, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                   const_cast<void *>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "decode: cuTensorMapEncodeTiled rejected the cache layout");
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = {rows, m};
+  *out = m;
+  return PKV_OK;
+}
 
 DecodeFn pick_decode(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
   if (cache_dtype == PKV_F16 && q_dtype == PKV_F16) return decode_call_f16;
@@ -63,6 +134,12 @@ pkv_status decode_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   if (e == cudaErrorNotSupported)
     return fail(PKV_ERR_UNSUPPORTED, "decode: head_dim must be 64 or 128 and group 1, 2, 4 or 8");
   if (e != cudaSuccess) return cuda_fail(e, "decode: kernel setup");
+  if (head_dim == 128) {  // the workspace serves either kernel variant
+    int ctas_mma = 0;
+    e = pick_mma(q_dtype, cache_dtype)(group, kDecodePrepare, nullptr, nullptr, nullptr, 0, nullptr, &ctas_mma);
+    if (e != cudaSuccess) return cuda_fail(e, "decode: tensor-core kernel setup");
+    if (ctas_mma > ctas) ctas = ctas_mma;
+  }
   const int sms = sm_count();
   if (sms <= 0) return fail(PKV_ERR_CUDA, "decode: cannot query the SM count");
   lay->max_ctas = sms * ctas;
@@ -90,6 +167,15 @@ using namespace pkv;
 extern "C" {
 
 int64_t pkv_launch_count(void) { return t_launches; }
+
+pkv_status pkv_set_decode_kernel(pkv_decode_kernel kind) {
+  if (kind != PKV_DECODE_AUTO && kind != PKV_DECODE_SIMT && kind != PKV_DECODE_MMA)
+    return fail(PKV_ERR_INVALID, "pkv_set_decode_kernel: unknown kind");
+  g_decode_kind.store(kind);
+  return PKV_OK;
+}
+
+pkv_decode_kernel pkv_get_decode_kernel(void) { return static_cast<pkv_decode_kernel>(g_decode_kind.load()); }
 
 pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                                 const int32_t *src, const int32_t *dst, int32_t num_pairs,
@@ -223,9 +309,23 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
   if (grid < 1) grid = 1;
   if (grid > lay.max_ctas) grid = lay.max_ctas;
 
-  DecodeFn fn = pick_decode(q_dtype, cache_dtype);
-  cudaError_t e = fn(head_dim, num_q_heads / num_kv_heads, kDecodeLaunch, &p, static_cast<int>(grid),
-                     &t_launches, nullptr);
+  cudaError_t e;
+  if (use_mma(head_dim)) {
+    const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
+    if (rows >= (int64_t(1) << 31))
+      return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: pool larger than 2^31 token rows");
+    const int esz = cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
+    CUtensorMap tmk, tmv;
+    s = cache_tensor_map(k_cache, rows, esz, &tmk);
+    if (s != PKV_OK) return s;
+    s = cache_tensor_map(v_cache, rows, esz, &tmv);
+    if (s != PKV_OK) return s;
+    e = pick_mma(q_dtype, cache_dtype)(num_q_heads / num_kv_heads, kDecodeLaunch, &p, &tmk, &tmv,
+                                       static_cast<int>(grid), &t_launches, nullptr);
+  } else {
+    DecodeFn fn = pick_decode(q_dtype, cache_dtype);
+    e = fn(head_dim, num_q_heads / num_kv_heads, kDecodeLaunch, &p, static_cast<int>(grid), &t_launches, nullptr);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode");
   return PKV_OK;
 }

@@ -124,6 +124,68 @@ __device__ __forceinline__ int2 tile_desc(const DecodeParams &p, const int32_t *
   return make_int2(blk, (item << 7) | ((lb == 0) << 6) | ((lb == nb - 1) << 5) | ntok);
 }
 
+// CTA prologue shared by the decode kernels: blocks per sequence (validating
+// every context length), their exclusive prefix sum cum[0..num_seqs] in shared
+// memory (CTA 0 also stores it to the workspace for the reduce kernel), and
+// the initialisation of each warp's kStages stage barriers.
+template <int kWarps, int kStages>
+__device__ __forceinline__ void scan_blocks_and_init(const DecodeParams &p, int32_t *cum, int32_t *misc,
+                                                     uint64_t *bars_all) {
+  constexpr int kThreads = kWarps * 32;
+  constexpr int PER = (PKV_MAX_SEQS_PER_CALL + kThreads - 1) / kThreads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int nbk[PER];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int s = tid * PER + i;
+    int nb = 0;
+    if (s < p.num_seqs) {
+      const int L = p.context_lens[s];
+      if (L < 0 || L > p.max_context_len ||
+          static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBS) {
+        report(p.d_error, PKV_DEVERR_BAD_CONTEXT_LEN);
+      } else {
+        nb = (L + kBS - 1) / kBS;
+      }
+    }
+    nbk[i] = nb;
+    sum += nb;
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) misc[warp] = incl;
+  if (lane < kStages) mbar_init(bars_all + warp * kStages + lane, 1);
+  __syncthreads();
+  if (warp == 0) {
+    int x = lane < kWarps ? misc[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += n;
+    }
+    if (lane < kWarps) misc[16 + lane] = x;  // inclusive warp totals
+  }
+  __syncthreads();
+  int run = incl - sum + (warp > 0 ? misc[16 + warp - 1] : 0);
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int s = tid * PER + i;
+    if (s < p.num_seqs) cum[s] = run;
+    run += nbk[i];
+  }
+  if (tid == 0) cum[p.num_seqs] = misc[16 + kWarps - 1];
+  fence_barrier_init();
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int s = tid; s <= p.num_seqs; s += kThreads) p.ws_cum[s] = cum[s];
+  }
+}
+
 template <int D, int G, int CDT, int QDT>
 __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
     paged_decode_kernel(const DecodeParams p) {
@@ -139,60 +201,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // ---- prologue: blocks per sequence and their exclusive prefix sum -------
-  {
-    constexpr int PER = (PKV_MAX_SEQS_PER_CALL + C::kThreads - 1) / C::kThreads;
-    int nbk[PER];
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int s = tid * PER + i;
-      int nb = 0;
-      if (s < p.num_seqs) {
-        const int L = p.context_lens[s];
-        if (L < 0 || L > p.max_context_len ||
-            static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBS) {
-          report(p.d_error, PKV_DEVERR_BAD_CONTEXT_LEN);
-        } else {
-          nb = (L + kBS - 1) / kBS;
-        }
-      }
-      nbk[i] = nb;
-      sum += nb;
-    }
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += n;
-    }
-    if (lane == 31) misc[warp] = incl;
-    if (lane < C::kStages) mbar_init(bars_all + warp * C::kStages + lane, 1);
-    __syncthreads();
-    if (warp == 0) {
-      int x = lane < C::kWarps ? misc[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += n;
-      }
-      if (lane < C::kWarps) misc[16 + lane] = x;  // inclusive warp totals
-    }
-    __syncthreads();
-    int run = incl - sum + (warp > 0 ? misc[16 + warp - 1] : 0);
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int s = tid * PER + i;
-      if (s < p.num_seqs) cum[s] = run;
-      run += nbk[i];
-    }
-    if (tid == 0) cum[p.num_seqs] = misc[16 + C::kWarps - 1];
-    fence_barrier_init();
-    __syncthreads();
-    if (blockIdx.x == 0) {
-      for (int s = tid; s <= p.num_seqs; s += C::kThreads) p.ws_cum[s] = cum[s];
-    }
-  }
+  scan_blocks_and_init<C::kWarps, C::kStages>(p, cum, misc, bars_all);
 
   // ---- this warp's share of the tiles --------------------------------------
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * C::kWarps;

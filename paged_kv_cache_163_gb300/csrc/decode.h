@@ -1,6 +1,7 @@
 // Launch interface of the decode kernels (arguments already validated).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -46,5 +47,16 @@ cudaError_t decode_call_fp8_f16(int head_dim, int group, int op, const DecodePar
                                 int64_t *launches, int *ctas_per_sm);
 cudaError_t decode_call_fp8_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
                                  int64_t *launches, int *ctas_per_sm);
+
+// Tensor-core variant (head_dim 128 only); tmk / tmv map the K and V pools as
+// 2D [rows = num_blocks * num_kv_heads * 16][128 elements] with 128-byte swizzle.
+cudaError_t decode_mma_call_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
+cudaError_t decode_mma_call_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                 const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
+cudaError_t decode_mma_call_fp8_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                    const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
+cudaError_t decode_mma_call_fp8_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                     const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
 
 }  // namespace pkv

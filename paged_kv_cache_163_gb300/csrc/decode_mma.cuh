@@ -1,0 +1,478 @@
+// Tensor-core variant of the paged decode partial kernel (head_dim 128).
+//
+// Same work split, staging ring, partial format and reduce kernel as
+// paged_decode_kernel; the arithmetic of one (block, KV head) tile moves to
+// mma.sync m16n8k16 (fp32 accumulate):
+//   S^T[16 tokens x 8 heads] = K[16 x 128] . Q^T[128 x 8]      (8 MMAs)
+//   O^T[128 x 8]            += V^T[128 x 16] . P^T[16 x 8]     (8 MMAs, 16 for bf16)
+// The GQA group (G <= 8 heads, zero-padded to 8) is the MMA's N.  K and V
+// tiles arrive by tensor TMA with the 128-byte swizzle; every lane's reads
+// are conflict-free because the head_dim order inside the MMAs is permuted
+// (a dot product and the output rows do not depend on the order, only on
+// using the same order for K and Q, and writing O with the matching d).
+// FP8 codes become fp16 in registers (exact); a bf16 P is split into a
+// high and a low bf16 half so the probabilities keep fp16-class precision.
+#pragma once
+
+#include <cuda.h>
+
+#include "decode.cuh"
+
+namespace pkv {
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                          bool bf16) {
+  if (bf16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// Transpose of an 8x8 16-bit matrix held in the standard fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Four E4M3 codes (byte 0 first) -> two f16x2 (codes 0,1 and 2,3); exact.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4 &v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Tensor-map bulk load of a 2D box into shared memory (complete_tx on bar).
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+template <int G, int CDT, int QDT>
+struct MmaCfg {
+  static constexpr int kD = 128;
+  static constexpr int kWarps = 8;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr bool kFp8 = CDT == PKV_FP8_E4M3;
+  static constexpr bool kBf16 = !kFp8 && CDT == PKV_BF16;  // MMA operand type: bf16, else f16
+  static constexpr int kEsz = kFp8 ? 1 : 2;
+  static constexpr int kTile = kBS * kD * kEsz;  // K or V tile bytes (1024-aligned in shared memory)
+  static constexpr int kKV = 2 * kTile;
+  static constexpr int kScale = kFp8 ? kBS * 4 : 0;
+  static constexpr int kQ = G * kD * 2;
+  static constexpr int kAux = round_up_c(2 * kScale + kQ, 128);  // [k scales][v scales][q rows]
+  static constexpr int kStages = clamp_c(27900 / (kKV + kAux), 2, 6);
+  static constexpr int kCumBytes = round_up_c((PKV_MAX_SEQS_PER_CALL + 1) * 4, 128);
+  static constexpr int kMiscBytes = 128;
+  static constexpr int kBarBytes = round_up_c(kWarps * kStages * 8, 128);
+  static constexpr int kDescBytes = kWarps * 64 * 8;
+  static constexpr int kHead = kCumBytes + kMiscBytes + kBarBytes + kDescBytes;
+  static constexpr int kTilesOff = round_up_c(kHead, 1024);
+  static constexpr int kSmem = 1024 + kTilesOff + kWarps * kStages * (kKV + kAux);
+  static_assert(G >= 1 && G <= 8, "group size");
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+// head_dim index of output row m (0..15) of m-tile i for lane group g (see kernel comment).
+template <bool FP8>
+__device__ __forceinline__ int out_d(int g, int i, int hrow) {
+  return FP8 ? 16 * g + 2 * i + hrow : 64 * (i >> 2) + 8 * g + 2 * (i & 3) + hrow;
+}
+
+template <int G, int CDT, int QDT>
+__global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, 1)
+    paged_decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                            const __grid_constant__ CUtensorMap tmv) {
+  using C = MmaCfg<G, CDT, QDT>;
+  constexpr int D = C::kD;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);  // 1024-aligned base
+  int32_t *cum = reinterpret_cast<int32_t *>(smem);
+  int32_t *misc = reinterpret_cast<int32_t *>(smem + C::kCumBytes);
+  uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + C::kCumBytes + C::kMiscBytes);
+  int2 *desc_all = reinterpret_cast<int2 *>(smem + C::kCumBytes + C::kMiscBytes + C::kBarBytes);
+  uint8_t *tiles_all = smem + C::kTilesOff;
+  uint8_t *aux_all = tiles_all + C::kWarps * C::kStages * C::kKV;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int g = lane >> 2;   // MMA row group
+  const int q4 = lane & 3;   // thread within the group
+
+  scan_blocks_and_init<C::kWarps, C::kStages>(p, cum, misc, bars_all);
+
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * C::kWarps;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * C::kWarps + warp;
+  const int64_t total = static_cast<int64_t>(cum[p.num_seqs]) * p.num_kv_heads;
+  const int64_t t0 = gw * total / nwarps;
+  const int64_t t1 = (gw + 1) * total / nwarps;
+  const int count = static_cast<int>(t1 - t0);
+  if (count <= 0) return;
+
+  uint64_t *bars = bars_all + warp * C::kStages;
+  int2 *desc = desc_all + warp * 64;
+  uint8_t *tiles = tiles_all + warp * C::kStages * C::kKV;
+  uint8_t *aux = aux_all + warp * C::kStages * C::kAux;
+  const uint64_t pol = policy_evict_first();
+
+  auto fill_window = [&](int w) {
+    const int64_t t = t0 + 32 * static_cast<int64_t>(w) + lane;
+    int2 d = make_int2(-1, 0);
+    if (t < t1) d = tile_desc(p, cum, t);
+    desc[(w & 1) * 32 + lane] = d;
+  };
+
+  auto issue = [&](int m) {
+    const int2 d = desc[((m >> 5) & 1) * 32 + (m & 31)];
+    if (lane == 0) {
+      const int st = m % C::kStages;
+      uint8_t *tb = tiles + st * C::kKV;
+      uint8_t *ab = aux + st * C::kAux;
+      const int item = d.y >> 7;
+      const bool need_q = (m == 0) || ((d.y >> 6) & 1);
+      const uint32_t bytes = (d.x >= 0 ? C::kKV + 2 * C::kScale : 0) + (need_q ? C::kQ : 0);
+      fence_proxy_async_smem();
+      if (bytes == 0) {
+        mbar_arrive(bars + st);
+      } else {
+        mbar_arrive_expect_tx(bars + st, bytes);
+        if (d.x >= 0) {
+          const int kvh = item % p.num_kv_heads;
+          const int64_t tile = static_cast<int64_t>(d.x) * p.num_kv_heads + kvh;
+          const int row = static_cast<int>(tile * kBS);
+          if constexpr (C::kFp8) {
+            tma_load_2d(tb, &tmk, 0, row, bars + st, pol);
+            tma_load_2d(tb + C::kTile, &tmv, 0, row, bars + st, pol);
+            bulk_g2s(ab, p.k_scale + tile * kBS, C::kScale, bars + st, pol);
+            bulk_g2s(ab + C::kScale, p.v_scale + tile * kBS, C::kScale, bars + st, pol);
+          } else {
+            tma_load_2d(tb, &tmk, 0, row, bars + st, pol);
+            tma_load_2d(tb + 2048, &tmk, 64, row, bars + st, pol);
+            tma_load_2d(tb + C::kTile, &tmv, 0, row, bars + st, pol);
+            tma_load_2d(tb + C::kTile + 2048, &tmv, 64, row, bars + st, pol);
+          }
+        }
+        if (need_q) bulk_g2s(ab + 2 * C::kScale, p.q + static_cast<size_t>(item) * C::kQ, C::kQ, bars + st);
+      }
+    }
+  };
+
+  fill_window(0);
+  fill_window(1);
+  __syncwarp();
+#pragma unroll 1
+  for (int i = 0; i < C::kStages && i < count; ++i) issue(i);
+
+  uint32_t qb[8][2];   // Q^T B fragments (8 k-steps)
+  float oacc[8][4];    // O^T accumulators (8 m-tiles of 16 head_dim rows x 8 heads)
+  float m_run[2], l_run[2];  // heads 2 q4 and 2 q4 + 1 (running max: base-2 domain)
+  int cur_item = -1;
+  bool whole_start = false, saw_last = false;
+
+  auto flush = [&](int item, bool whole) {
+    float lt[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float v = l_run[j];
+      v += __shfl_xor_sync(kFull, v, 4);
+      v += __shfl_xor_sync(kFull, v, 8);
+      v += __shfl_xor_sync(kFull, v, 16);
+      lt[j] = v;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int n = 2 * q4 + j;
+      if (n >= G) continue;
+      if (whole) {
+        const float inv = lt[j] > 0.f ? 1.f / lt[j] : 0.f;
+        const size_t row = (static_cast<size_t>(item) * G + n) * D;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int d0 = out_d<C::kFp8>(g, i, 0);
+          const float r0 = oacc[i][j] * inv, r1 = oacc[i][2 + j] * inv;
+          if (p.out_f32) {
+            *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.out) + row + d0) = make_float2(r0, r1);
+          } else {
+            *reinterpret_cast<uint32_t *>(p.out + (row + d0) * 2) = pack2<QDT>(r0, r1);
+          }
+        }
+      } else {
+        const int64_t slot = gw + item;
+        float *op = p.ws_o + (slot * G + n) * D;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float2 *>(op + out_d<C::kFp8>(g, i, 0)) = make_float2(oacc[i][j], oacc[i][2 + j]);
+        if (g == 0) {
+          p.ws_ml[(slot * G + n) * 2] = m_run[j];
+          p.ws_ml[(slot * G + n) * 2 + 1] = lt[j];
+        }
+      }
+    }
+  };
+
+  // tokens whose V rows this lane reads (B-fragment k rows of P^T)
+  const int tk0 = 2 * q4, tk1 = 2 * q4 + 1, tk2 = 2 * q4 + 8, tk3 = 2 * q4 + 9;
+
+#pragma unroll 1
+  for (int n = 0; n < count; ++n) {
+    if (n > 0 && (n & 31) == 0) {
+      __syncwarp();
+      fill_window((n >> 5) + 1);
+      __syncwarp();
+    }
+    const int2 d = desc[((n >> 5) & 1) * 32 + (n & 31)];
+    const int st = n % C::kStages;
+    const uint8_t *kt = tiles + st * C::kKV;
+    const uint8_t *vt = kt + C::kTile;
+    const uint8_t *ab = aux + st * C::kAux;
+    const bool ok = __all_sync(kFull, mbar_wait(bars + st, (n / C::kStages) & 1));
+    if (!ok) {
+      if (lane == 0) report(p.d_error, PKV_DEVERR_WAIT_TIMEOUT);
+      for (int k = n + 1; k < count && k < n + C::kStages; ++k)
+        mbar_wait(bars + k % C::kStages, (k / C::kStages) & 1);
+      return;
+    }
+    const int item = d.y >> 7;
+    const int ntok = d.y & 31;
+    if (item != cur_item) {
+      if (cur_item >= 0) flush(cur_item, whole_start && saw_last);
+      cur_item = item;
+      whole_start = (d.y >> 6) & 1;
+      const uint8_t *qs = ab + 2 * C::kScale;  // [G][128] rows in the query dtype
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int d0 = C::kFp8 ? 32 * q4 + 4 * s : 64 * (s >> 2) + 16 * q4 + 4 * (s & 3);
+        uint2 raw = make_uint2(0u, 0u);
+        if (g < G) raw = *reinterpret_cast<const uint2 *>(qs + (g * D + d0) * 2);
+        if constexpr (C::kFp8 && QDT == PKV_BF16) {  // f16 MMA operands
+          const float2 a = unpack2<QDT>(raw.x), b = unpack2<QDT>(raw.y);
+          qb[s][0] = pack2<PKV_F16>(a.x, a.y);
+          qb[s][1] = pack2<PKV_F16>(b.x, b.y);
+        } else {
+          qb[s][0] = raw.x;
+          qb[s][1] = raw.y;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) oacc[i][c] = 0.f;
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
+    }
+    saw_last = (d.y >> 5) & 1;
+
+    if (d.x >= 0) {
+      // ---- S^T = K Q^T: lane rows g and g + 8, head columns 2 q4, 2 q4 + 1 ----
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (C::kFp8) {
+        uint4 kr[2][2];  // [row g, g + 8][chunk 2 q4 + j]
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int row = g + 8 * r, c = 2 * q4 + j;
+            kr[r][j] = *reinterpret_cast<const uint4 *>(kt + row * 128 + ((c ^ (row & 7)) << 4));
+          }
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          uint32_t a[4];
+          e4m3x4_to_f16(word(kr[0][s >> 2], s & 3), a[0], a[2]);
+          e4m3x4_to_f16(word(kr[1][s >> 2], s & 3), a[1], a[3]);
+          mma_16816(sacc, a, qb[s][0], qb[s][1], false);
+        }
+      } else {
+        uint4 kr[2][2][2];  // [row][half][chunk 2 q4 + j]
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int row = g + 8 * r, c = 2 * q4 + j;
+              kr[r][h][j] = *reinterpret_cast<const uint4 *>(kt + h * 2048 + row * 128 + ((c ^ (row & 7)) << 4));
+            }
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const int h = s >> 2, j = (s & 3) >> 1, t = s & 1;
+          uint32_t a[4] = {word(kr[0][h][j], 2 * t), word(kr[1][h][j], 2 * t), word(kr[0][h][j], 2 * t + 1),
+                           word(kr[1][h][j], 2 * t + 1)};
+          mma_16816(sacc, a, qb[s][0], qb[s][1], C::kBf16);
+        }
+      }
+      // ---- scale, mask, online softmax (base 2) ----
+      float sc0 = p.scale_log2, sc1 = p.scale_log2;
+      if constexpr (C::kFp8) {
+        const float *ksc = reinterpret_cast<const float *>(ab);
+        sc0 *= ksc[g];
+        sc1 *= ksc[g + 8];
+      }
+      const bool v0 = g < ntok, v1 = g + 8 < ntok;
+      float s00 = v0 ? sacc[0] * sc0 : -INFINITY;  // token g,     head 2 q4
+      float s01 = v0 ? sacc[1] * sc0 : -INFINITY;  // token g,     head 2 q4 + 1
+      float s10 = v1 ? sacc[2] * sc1 : -INFINITY;  // token g + 8, head 2 q4
+      float s11 = v1 ? sacc[3] * sc1 : -INFINITY;  // token g + 8, head 2 q4 + 1
+      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+      }
+      const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+      const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
+      m_run[0] = mn0;
+      m_run[1] = mn1;
+      float p00 = exp2f(s00 - mn0), p01 = exp2f(s01 - mn1), p10 = exp2f(s10 - mn0), p11 = exp2f(s11 - mn1);
+      l_run[0] = l_run[0] * al0 + (p00 + p10);
+      l_run[1] = l_run[1] * al1 + (p01 + p11);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        oacc[i][0] *= al0;
+        oacc[i][1] *= al1;
+        oacc[i][2] *= al0;
+        oacc[i][3] *= al1;
+      }
+      if constexpr (C::kFp8) {  // fold the per-token V scale into P
+        const float *vsc = reinterpret_cast<const float *>(ab + C::kScale);
+        const float w0 = v0 ? vsc[g] : 0.f, w1 = v1 ? vsc[g + 8] : 0.f;
+        p00 *= w0;
+        p01 *= w0;
+        p10 *= w1;
+        p11 *= w1;
+      }
+      // ---- P^T B fragments (k rows = tokens, n columns = heads) ----
+      uint32_t pb[2][2];  // [hi / lo][b0, b1]
+      if constexpr (C::kBf16) {
+        const uint32_t h0 = pack2<PKV_BF16>(p00, p01), h1 = pack2<PKV_BF16>(p10, p11);
+        const float2 r0 = unpack2<PKV_BF16>(h0), r1 = unpack2<PKV_BF16>(h1);
+        const uint32_t l0 = pack2<PKV_BF16>(p00 - r0.x, p01 - r0.y), l1 = pack2<PKV_BF16>(p10 - r1.x, p11 - r1.y);
+        pb[0][0] = movmatrix_t(h0);
+        pb[0][1] = movmatrix_t(h1);
+        pb[1][0] = movmatrix_t(l0);
+        pb[1][1] = movmatrix_t(l1);
+      } else {
+        pb[0][0] = movmatrix_t(pack2<PKV_F16>(p00, p01));
+        pb[0][1] = movmatrix_t(pack2<PKV_F16>(p10, p11));
+      }
+      // ---- O^T += V^T P^T ----
+      const bool tail = ntok < kBS;
+      if constexpr (C::kFp8) {
+        uint4 vr[4];  // tokens tk0..tk3, chunk g (head_dim 16 g .. 16 g + 15)
+        const int tks[4] = {tk0, tk1, tk2, tk3};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          vr[k] = *reinterpret_cast<const uint4 *>(vt + tks[k] * 128 + ((g ^ (tks[k] & 7)) << 4));
+          if (tail && tks[k] >= ntok) vr[k] = make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t x0 = word(vr[0], w), y0 = word(vr[1], w), x1 = word(vr[2], w), y1 = word(vr[3], w);
+          uint32_t a[4], b[4];
+          e4m3x4_to_f16(prmt(x0, y0, 0x5140), a[0], a[1]);
+          e4m3x4_to_f16(prmt(x1, y1, 0x5140), a[2], a[3]);
+          e4m3x4_to_f16(prmt(x0, y0, 0x7362), b[0], b[1]);
+          e4m3x4_to_f16(prmt(x1, y1, 0x7362), b[2], b[3]);
+          mma_16816(oacc[2 * w], a, pb[0][0], pb[0][1], false);
+          mma_16816(oacc[2 * w + 1], b, pb[0][0], pb[0][1], false);
+        }
+      } else {
+        uint4 vr[4][2];  // [token][half], chunk g
+        const int tks[4] = {tk0, tk1, tk2, tk3};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            vr[k][h] = *reinterpret_cast<const uint4 *>(vt + h * 2048 + tks[k] * 128 + ((g ^ (tks[k] & 7)) << 4));
+            if (tail && tks[k] >= ntok) vr[k][h] = make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int h = i >> 2, w = i & 3;
+          const uint32_t x0 = word(vr[0][h], w), y0 = word(vr[1][h], w);
+          const uint32_t x1 = word(vr[2][h], w), y1 = word(vr[3][h], w);
+          const uint32_t a[4] = {prmt(x0, y0, 0x5410), prmt(x0, y0, 0x7632), prmt(x1, y1, 0x5410),
+                                 prmt(x1, y1, 0x7632)};
+          mma_16816(oacc[i], a, pb[0][0], pb[0][1], C::kBf16);
+          if constexpr (C::kBf16) mma_16816(oacc[i], a, pb[1][0], pb[1][1], true);
+        }
+      }
+    }
+    __syncwarp();  // the stage is free again
+    if (n + C::kStages < count) issue(n + C::kStages);
+  }
+  flush(cur_item, whole_start && saw_last);
+}
+
+template <int G, int CDT, int QDT>
+struct MmaInstance {
+  using C = MmaCfg<G, CDT, QDT>;
+  static cudaError_t prepare(int *ctas_per_sm) {
+    static int cached = -1;
+    if (cached < 0) {
+      cudaError_t e = cudaFuncSetAttribute(paged_decode_mma_kernel<G, CDT, QDT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+      if (e != cudaSuccess) return e;
+      int n = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_mma_kernel<G, CDT, QDT>, C::kThreads,
+                                                        C::kSmem);
+      if (e != cudaSuccess) return e;
+      cached = n > 0 ? n : 1;
+    }
+    *ctas_per_sm = cached;
+    return cudaSuccess;
+  }
+  static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                            int64_t *launches) {
+    paged_decode_mma_kernel<G, CDT, QDT><<<grid, C::kThreads, C::kSmem, p.stream>>>(p, tmk, tmv);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    paged_reduce_kernel<C::kD, G, QDT><<<p.num_seqs * p.num_kv_heads, 128, 0, p.stream>>>(
+        p, static_cast<int64_t>(grid) * C::kWarps);
+    *launches += 2;
+    return cudaGetLastError();
+  }
+};
+
+template <int CDT, int QDT>
+cudaError_t decode_mma_family(int G, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                              const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas) {
+  switch (G) {
+#define PKV_MMA_CASE(GG)                                                   \
+  case GG:                                                                 \
+    if (op == kDecodePrepare) return MmaInstance<GG, CDT, QDT>::prepare(ctas); \
+    return MmaInstance<GG, CDT, QDT>::launch(*p, *tmk, *tmv, grid, launches);
+    PKV_MMA_CASE(1)
+    PKV_MMA_CASE(2)
+    PKV_MMA_CASE(4)
+    PKV_MMA_CASE(8)
+#undef PKV_MMA_CASE
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace pkv

@@ -30,6 +30,15 @@ def play():
     return p
 
 
+@pytest.fixture
+def kernel_kind(request):
+    """Run a test under one decode kernel variant, then restore the default."""
+    from paged_kv_cache_163_gb300 import capi
+    capi.pkv_set_decode_kernel(request.param)
+    yield request.param
+    capi.pkv_set_decode_kernel("auto")
+
+
 def check_tables(cache, o, seqs):
     t, lens = cache.tables(seqs)
     mt, ml = o.alloc.block_tables(seqs, t.shape[1])
@@ -73,16 +82,19 @@ def test_tiny_gqa_fp16(play):
     full_oracle_check(play, wl.make(1))
 
 
-def test_llama3_8b_shape_bf16(play):
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
+def test_llama3_8b_shape_bf16(play, kernel_kind):
     full_oracle_check(play, wl.make(2))
 
 
-def test_prefix_sharing_bf16(play):
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
+def test_prefix_sharing_bf16(play, kernel_kind):
     w = wl.make(4)
     full_oracle_check(play, w)
 
 
-def test_mha_40_layers_fp16(play):
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
+def test_mha_40_layers_fp16(play, kernel_kind):
     w = wl.make(3)
     cache, out = play.run(w, poison=False, out_dtype="f32")
     assert cache.check() == 0
@@ -107,7 +119,8 @@ def test_mha_40_layers_fp16(play):
     cache.close()
 
 
-def test_long_context_fp8_sampled(play):
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
+def test_long_context_fp8_sampled(play, kernel_kind):
     w = wl.make(5)
     cache, out = play.run(w, poison=False, out_dtype="f32")
     assert cache.check() == 0
@@ -140,11 +153,12 @@ def test_long_context_fp8_sampled(play):
     cache.close()
 
 
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
 @pytest.mark.parametrize("q_dtype,cache_dtype", [("f16", "f16"), ("bf16", "bf16"),
                                                  ("bf16", "fp8_e4m3"), ("f16", "fp8_e4m3")])
-def test_every_instance_ragged(play, d, group, q_dtype, cache_dtype):
+def test_every_instance_ragged(play, kernel_kind, d, group, q_dtype, cache_dtype):
     hkv = 2
     lens = [1, 15, 16, 17, 31, 33, 200, 777, 2]
     w = wl.custom(f"inst-{d}-{group}-{cache_dtype}", lens=lens, num_q_heads=hkv * group, num_kv_heads=hkv,
@@ -153,7 +167,8 @@ def test_every_instance_ragged(play, d, group, q_dtype, cache_dtype):
     full_oracle_check(play, w)
 
 
-def test_one_long_sequence_among_short(play):
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
+def test_one_long_sequence_among_short(play, kernel_kind):
     # one sequence holds most tiles: its (sequence, head) pairs are split across many warps
     lens = [40000, 3, 16, 1, 100]
     w = wl.custom("split-heavy", lens=lens, num_q_heads=32, num_kv_heads=8, head_dim=128,
