@@ -176,7 +176,12 @@ pkv_status pkv_set_decode_kernel(pkv_decode_kernel kind);
 pkv_decode_kernel pkv_get_decode_kernel(void);
 
 /* Device workspace (bytes) paged_attention_decode needs for these shapes on
- * the current device (split-KV partials).  Depends on the device's SM count. */
+ * the current device (split-KV partials and per-(sequence, KV head)
+ * counters).  Depends on the device's SM count.  Fill a new workspace with
+ * zeros once before its first use; after that it can be reused by any
+ * number of calls (serialised on the GPU) without clearing, also with other
+ * shapes (a call whose shapes differ from the previous call on the same
+ * workspace clears the counters itself with one cudaMemsetAsync). */
 pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                            int32_t num_kv_heads, int32_t head_dim,
                                            pkv_dtype q_dtype, pkv_dtype cache_dtype,
@@ -197,7 +202,9 @@ pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads
  * A context_len of 0 gives a zero output.  Work is split across the GPU
  * in equal shares of (sequence, KV head, 16-token block) tiles; shares that
  * cover part of a sequence leave fp32 partials in `workspace` (at least
- * paged_attention_workspace_bytes) merged by a log-sum-exp reduce kernel.
+ * paged_attention_workspace_bytes, zero-filled before its first use); the
+ * warp that stores the last partial of a (sequence, KV head) merges them by
+ * log-sum-exp in the same kernel.
  * Supported: head_dim 64 or 128; G in {1, 2, 4, 8}; num_seqs <=
  * PKV_MAX_SEQS_PER_CALL. */
 pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
@@ -222,9 +229,10 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
  * PKV_ERR_WORKSPACE with the size in pkv_last_error().  The call allocates
  * nothing.  Its first call on a device looks up the buffer's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls on a device share the buffer and it
- * keeps the last call's contents (nothing in it needs to start at zero);
- * calls whose kernels overlap on the GPU race, so serialise them. */
+ * before any stream capture; it also zero-fills the buffer once.  All calls
+ * on a device share the buffer and it keeps the last call's contents, which
+ * the next call can start from; calls whose kernels overlap on the GPU race,
+ * so serialise them. */
 #define PKV_STATIC_SCRATCH_BYTES (16u << 20)
 pkv_status paged_attention_decode_static(void *out, pkv_dtype out_dtype, const void *q,
                                          pkv_dtype q_dtype, const void *k_cache, const void *v_cache,

@@ -40,6 +40,25 @@ int sm_count() {
 }
 
 std::atomic<int> g_decode_kind{PKV_DECODE_AUTO};
+std::atomic<uint32_t> g_epoch{0};  // per decode call; its low bit picks the split-item counter bank
+
+// The counter banks sit at a shape-dependent offset of the workspace.  The
+// first call on a workspace, and any call whose shape differs from the last
+// call on it, clears them (the kernels keep them clear from then on).
+pkv_status prepare_counters(void *workspace, int32_t num_seqs, int32_t num_kv_heads, const void *ctr, size_t bytes,
+                            cudaStream_t st) {
+  static std::mutex mu;
+  static std::unordered_map<uintptr_t, int64_t> shapes;
+  const int64_t shape = (static_cast<int64_t>(num_seqs) << 32) | static_cast<uint32_t>(num_kv_heads);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = shapes.find(reinterpret_cast<uintptr_t>(workspace));
+  if (it != shapes.end() && it->second == shape) return PKV_OK;
+  cudaError_t e = cudaMemsetAsync(const_cast<void *>(ctr), 0, bytes, st);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "paged_attention_decode: clearing the split counters failed");
+  if (shapes.size() > 4096) shapes.clear();
+  shapes[reinterpret_cast<uintptr_t>(workspace)] = shape;
+  return PKV_OK;
+}
 
 using DecodeFn = cudaError_t (*)(int, int, int, const DecodeParams *, int, int64_t *, int *);
 using MmaFn = cudaError_t (*)(int, int, const DecodeParams *, const CUtensorMap *, const CUtensorMap *, int,
@@ -117,7 +136,7 @@ DecodeFn pick_decode(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 struct DecodeLayout {
-  int64_t cum_bytes, ml_bytes, o_bytes, total;
+  int64_t cum_bytes, ctr_bytes, ml_bytes, o_bytes, total;
   int max_ctas;
 };
 
@@ -146,9 +165,10 @@ pkv_status decode_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   const int64_t slots = static_cast<int64_t>(lay->max_ctas) * kDecodeWarps +
                         static_cast<int64_t>(num_seqs) * num_kv_heads;
   lay->cum_bytes = round256((static_cast<int64_t>(num_seqs) + 1) * 4);
+  lay->ctr_bytes = round256(2 * static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
   lay->ml_bytes = round256(slots * group * 2 * 4);
   lay->o_bytes = round256(slots * group * head_dim * 4);
-  lay->total = lay->cum_bytes + lay->ml_bytes + lay->o_bytes;
+  lay->total = lay->cum_bytes + lay->ctr_bytes + lay->ml_bytes + lay->o_bytes;
   return PKV_OK;
 }
 
@@ -278,7 +298,7 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
     return fail(PKV_ERR_WORKSPACE, "paged_attention_decode: workspace smaller than required");
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  DecodeParams p;
+  DecodeParams p{};
   p.out = static_cast<uint8_t *>(out);
   p.out_f32 = out_dtype == PKV_F32 ? 1 : 0;
   p.q = static_cast<const uint8_t *>(q);
@@ -295,10 +315,14 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.ws_cum = reinterpret_cast<int32_t *>(ws);
-  p.ws_ml = reinterpret_cast<float *>(ws + lay.cum_bytes);
-  p.ws_o = reinterpret_cast<float *>(ws + lay.cum_bytes + lay.ml_bytes);
+  p.ws_ctr = reinterpret_cast<uint32_t *>(ws + lay.cum_bytes);
+  p.ws_ml = reinterpret_cast<float *>(ws + lay.cum_bytes + lay.ctr_bytes);
+  p.ws_o = reinterpret_cast<float *>(ws + lay.cum_bytes + lay.ctr_bytes + lay.ml_bytes);
+  p.epoch = ++g_epoch;
   p.d_error = d_error;
   p.stream = reinterpret_cast<cudaStream_t>(stream);
+  s = prepare_counters(workspace, num_seqs, num_kv_heads, p.ws_ctr, static_cast<size_t>(lay.ctr_bytes), p.stream);
+  if (s != PKV_OK) return s;
 
   // Grid: enough warps that each gets a few tiles of the largest possible
   // share, capped at one wave of resident CTAs.

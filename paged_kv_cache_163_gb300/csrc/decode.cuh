@@ -12,8 +12,9 @@
 //    persistent grid takes an equal contiguous share, so ragged lengths load
 //    balance to one tile.  A share that covers a whole (sequence, KV head)
 //    writes the output; one that covers part of it writes an fp32 partial
-//    (o, m, l) and the reduce kernel merges partials by log-sum-exp
-//    (flash-decoding style split-KV).
+//    (o, m, l) and counts it in on a per-item counter (one atomic add); the
+//    warp that stores the item's last partial merges them by log-sum-exp
+//    (flash-decoding style split-KV without a second kernel; nothing waits).
 //  * Each warp streams its tiles through a private ring of shared-memory
 //    stages filled by bulk asynchronous copies (cp.async.bulk, mbarrier
 //    completion), so ~100 KB per SM is in flight with no CTA-wide sync.
@@ -130,7 +131,7 @@ __device__ __forceinline__ int2 tile_desc(const DecodeParams &p, const int32_t *
 // the initialisation of each warp's kStages stage barriers.
 template <int kWarps, int kStages>
 __device__ __forceinline__ void scan_blocks_and_init(const DecodeParams &p, int32_t *cum, int32_t *misc,
-                                                     uint64_t *bars_all) {
+                                                     uint64_t *bars_all, int out_row_elems) {
   constexpr int kThreads = kWarps * 32;
   constexpr int PER = (PKV_MAX_SEQS_PER_CALL + kThreads - 1) / kThreads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -179,11 +180,172 @@ __device__ __forceinline__ void scan_blocks_and_init(const DecodeParams &p, int3
     run += nbk[i];
   }
   if (tid == 0) cum[p.num_seqs] = misc[16 + kWarps - 1];
+  {  // the next call's counter bank starts from zero
+    const int items = p.num_seqs * p.num_kv_heads;
+    uint32_t *other = p.ws_ctr + ((p.epoch & 1) ^ 1) * items;
+    for (int i = blockIdx.x * kThreads + tid; i < items; i += gridDim.x * kThreads) other[i] = 0u;
+  }
   fence_barrier_init();
   __syncthreads();
   if (blockIdx.x == 0) {
     for (int s = tid; s <= p.num_seqs; s += kThreads) p.ws_cum[s] = cum[s];
+    // sequences without tokens (or with an invalid length) read nothing: zero output
+    for (int s = tid; s < p.num_seqs; s += kThreads) {
+      if (cum[s + 1] != cum[s]) continue;
+      const size_t base = static_cast<size_t>(s) * out_row_elems;
+      for (int e = 0; e < out_row_elems; e += 2) {
+        if (p.out_f32) *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.out) + base + e) = make_float2(0.f, 0.f);
+        else *reinterpret_cast<uint32_t *>(p.out + (base + e) * 2) = 0u;
+      }
+    }
   }
+}
+
+// Warps in [w_first, w_last] (the warps whose shares meet an item) that own
+// at least one tile; with fewer tiles than warps some own none.
+__device__ __forceinline__ int owning_warps(int64_t w_first, int64_t w_last, int64_t total, int64_t nwarps) {
+  if (total >= nwarps) return static_cast<int>(w_last - w_first + 1);
+  int n = 0;
+  for (int64_t w = w_first; w <= w_last; ++w) n += (w * total / nwarps) != ((w + 1) * total / nwarps);
+  return n;
+}
+
+// First and last warp whose shares meet `item` (tiles start .. start + nb - 1).
+__device__ __forceinline__ void item_warps(const int32_t *cum, int hkv, int item, int64_t total, int64_t nwarps,
+                                           int64_t &w_first, int64_t &w_last) {
+  const int b = item / hkv;
+  const int kvh = item - b * hkv;
+  const int nb = cum[b + 1] - cum[b];
+  const int64_t start = static_cast<int64_t>(hkv) * cum[b] + static_cast<int64_t>(kvh) * nb;
+  // warp owning tile t: the w with floor(w T / W) <= t < floor((w + 1) T / W)
+  w_first = ((start + 1) * nwarps - 1) / total;
+  w_last = ((start + nb) * nwarps - 1) / total;
+}
+
+// Called by a whole warp after it stored a partial of `item`: counts it in
+// with one atomic add and returns (on every lane) whether this warp stored
+// the item's last one.  Counters come in two banks used by alternate calls
+// (bank = epoch & 1); every call clears the other bank in its prologue, so
+// the next call starts from zero even if this one is cut short.
+__device__ __forceinline__ bool count_partial(const DecodeParams &p, int item, int expected) {
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if ((threadIdx.x & 31) == 0) {
+    const int items = p.num_seqs * p.num_kv_heads;
+    const uint32_t old = atomicAdd(p.ws_ctr + (p.epoch & 1) * items + item, 1u);
+    last = static_cast<int>(old) + 1 == expected;
+  }
+  last = __shfl_sync(kFull, last, 0);
+  if (last) __threadfence();
+  return last != 0;
+}
+
+// One warp merges the partials of `item`:
+// out = sum_w 2^(m_w - M) o_w / sum_w 2^(m_w - M) l_w, M = max_w m_w.
+// Partials of other CTAs are read through L2 (ld.global.cg).  Lanes first
+// take one partial each (weights, maxima, sums by shuffles), then every lane
+// accumulates its head_dim slice over all partials with independent loads.
+template <int D, int G, int QDT>
+__device__ __noinline__ void merge_item(const DecodeParams &p, int item, int64_t w_first, int64_t w_last,
+                                        int64_t total, int64_t nwarps) {
+  constexpr int DPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const bool all_own = total >= nwarps;
+  auto owns = [&](int64_t w) { return all_own || (w * total / nwarps) != ((w + 1) * total / nwarps); };
+  const int np = static_cast<int>(w_last - w_first + 1);
+  const float *ml = p.ws_ml + (w_first + item) * G * 2;  // partial of warp w_first + k at ml[k * 2G]
+  const float *po = p.ws_o + (w_first + item) * G * D;
+  float acc[G][DPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[g][e] = 0.f;
+  float mx[G], den[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    mx[g] = -INFINITY;
+    den[g] = 0.f;
+  }
+  // maxima over all partials (lanes stride over the partials)
+  for (int k0 = 0; k0 < np; k0 += 32) {
+    const int k = k0 + lane;
+    if (k < np && owns(w_first + k))
+#pragma unroll
+      for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], __ldcg(ml + (k * G + g) * 2));
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(kFull, mx[g], o));
+  for (int k0 = 0; k0 < np; k0 += 32) {
+    // this lane's partial: its weight per head (0 when empty or all-masked)
+    const int k = k0 + lane;
+    float wk[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      wk[g] = 0.f;
+      if (k < np && owns(w_first + k)) {
+        const float mk = __ldcg(ml + (k * G + g) * 2);
+        if (mk != -INFINITY) {
+          wk[g] = exp2f(mk - mx[g]);
+          den[g] = fmaf(wk[g], __ldcg(ml + (k * G + g) * 2 + 1), den[g]);
+        }
+      }
+    }
+    const int nk = min(32, np - k0);
+#pragma unroll 4
+    for (int j = 0; j < nk; ++j) {
+      const float *src = po + (static_cast<int64_t>(k0 + j) * G) * D + lane * DPL;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float w = __shfl_sync(kFull, wk[g], j);
+        if (w != 0.f) {
+          if constexpr (DPL == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + g * D));
+            acc[g][0] = fmaf(w, v.x, acc[g][0]);
+            acc[g][1] = fmaf(w, v.y, acc[g][1]);
+            acc[g][2] = fmaf(w, v.z, acc[g][2]);
+            acc[g][3] = fmaf(w, v.w, acc[g][3]);
+          } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + g * D));
+            acc[g][0] = fmaf(w, v.x, acc[g][0]);
+            acc[g][1] = fmaf(w, v.y, acc[g][1]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) den[g] += __shfl_xor_sync(kFull, den[g], o);
+  const size_t obase = static_cast<size_t>(item) * G * D + lane * DPL;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float inv = den[g] > 0.f ? 1.f / den[g] : 0.f;
+    const size_t at = obase + g * D;
+    if (p.out_f32) {
+      float *dst = reinterpret_cast<float *>(p.out) + at;
+#pragma unroll
+      for (int e = 0; e < DPL; e += 2)
+        *reinterpret_cast<float2 *>(dst + e) = make_float2(acc[g][e] * inv, acc[g][e + 1] * inv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < DPL; e += 2)
+        *reinterpret_cast<uint32_t *>(p.out + (at + e) * 2) = pack2<QDT>(acc[g][e] * inv, acc[g][e + 1] * inv);
+    }
+  }
+}
+
+// After a warp stored its partial of `item`: count it in; the last one merges.
+template <int D, int G, int QDT>
+__device__ __forceinline__ void finish_partial(const DecodeParams &p, const int32_t *cum, int item, int64_t total,
+                                               int64_t nwarps) {
+  int64_t w_first, w_last;
+  item_warps(cum, p.num_kv_heads, item, total, nwarps, w_first, w_last);
+  if (count_partial(p, item, owning_warps(w_first, w_last, total, nwarps)))
+    merge_item<D, G, QDT>(p, item, w_first, w_last, total, nwarps);
 }
 
 template <int D, int G, int CDT, int QDT>
@@ -201,7 +363,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  scan_blocks_and_init<C::kWarps, C::kStages>(p, cum, misc, bars_all);
+  scan_blocks_and_init<C::kWarps, C::kStages>(p, cum, misc, bars_all, G * D * p.num_kv_heads);
 
   // ---- this warp's share of the tiles --------------------------------------
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * C::kWarps;
@@ -311,6 +473,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
           p.ws_ml[(slot * G + g) * 2 + 1] = l[g];
         }
       }
+      finish_partial<D, G, QDT>(p, cum, item, total, nwarps);
     }
   };
 
@@ -450,101 +613,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
   flush(cur_item, whole_start && saw_last);
 }
 
-// One CTA per (sequence, KV head): merge the partials of the warps that
-// shared it, out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
-// The partial maxima and sums are reduced across the CTA first; then each
-// thread accumulates its output elements over the partials with independent,
-// coalesced loads.
-template <int D, int G, int QDT>
-__global__ void __launch_bounds__(128) paged_reduce_kernel(const DecodeParams p, int64_t nwarps) {
-  __shared__ float s_red[4][G];
-  __shared__ float s_m[G];
-  __shared__ float s_inv[G];
-  const int item = blockIdx.x;
-  const int b = item / p.num_kv_heads;
-  const int kvh = item - b * p.num_kv_heads;
-  const int32_t *cum = p.ws_cum;
-  const int nb = cum[b + 1] - cum[b];
-  const size_t obase = static_cast<size_t>(item) * G * D;  // element index of this item's output
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (nb == 0) {
-    for (int i = tid; i < G * D / 2; i += blockDim.x) {
-      if (p.out_f32) reinterpret_cast<float2 *>(p.out)[obase / 2 + i] = make_float2(0.f, 0.f);
-      else reinterpret_cast<uint32_t *>(p.out)[obase / 2 + i] = 0u;
-    }
-    return;
-  }
-  const int64_t total = static_cast<int64_t>(cum[p.num_seqs]) * p.num_kv_heads;
-  const int64_t start = static_cast<int64_t>(p.num_kv_heads) * cum[b] + static_cast<int64_t>(kvh) * nb;
-  const int64_t last = start + nb - 1;
-  // warp owning tile t: the w with floor(w T / W) <= t < floor((w + 1) T / W)
-  const int64_t w_first = ((start + 1) * nwarps - 1) / total;
-  const int64_t w_last = ((last + 1) * nwarps - 1) / total;
-  if (w_first == w_last) return;  // written by the decode kernel
-  // With fewer tiles than warps some warps own nothing and wrote no partial.
-  const bool all_own = total >= nwarps;
-  auto owns = [&](int64_t w) { return all_own || (w * total / nwarps) != ((w + 1) * total / nwarps); };
-  const float *ml = p.ws_ml + (w_first + item) * G * 2;  // partial of warp w at ml[(w - w_first) * 2G]
-  const int np = static_cast<int>(w_last - w_first + 1);
-
-  float v[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) v[g] = -INFINITY;
-  for (int k = tid; k < np; k += blockDim.x)
-    if (owns(w_first + k))
-#pragma unroll
-      for (int g = 0; g < G; ++g) v[g] = fmaxf(v[g], ml[(k * G + g) * 2]);
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v[g] = fmaxf(v[g], __shfl_xor_sync(kFull, v[g], o));
-    if (lane == 0) s_red[wid][g] = v[g];
-  }
-  __syncthreads();
-  if (tid < G) s_m[tid] = fmaxf(fmaxf(s_red[0][tid], s_red[1][tid]), fmaxf(s_red[2][tid], s_red[3][tid]));
-  __syncthreads();
-#pragma unroll
-  for (int g = 0; g < G; ++g) v[g] = 0.f;
-  for (int k = tid; k < np; k += blockDim.x)
-    if (owns(w_first + k))
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float mk = ml[(k * G + g) * 2];
-        if (mk != -INFINITY) v[g] = fmaf(exp2f(mk - s_m[g]), ml[(k * G + g) * 2 + 1], v[g]);
-      }
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v[g] += __shfl_xor_sync(kFull, v[g], o);
-    if (lane == 0) s_red[wid][g] = v[g];
-  }
-  __syncthreads();
-  if (tid < G) {
-    const float den = s_red[0][tid] + s_red[1][tid] + s_red[2][tid] + s_red[3][tid];
-    s_inv[tid] = den > 0.f ? 1.f / den : 0.f;
-  }
-  __syncthreads();
-  const float *po = p.ws_o + (w_first + item) * G * D;  // partial o of warp w at po[(w - w_first) * G * D]
-  for (int i = tid; i < G * D / 2; i += blockDim.x) {
-    const int g = (2 * i) / D;
-    const int dd = (2 * i) % D;
-    const float mg = s_m[g];
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < np; ++k) {
-      const float mk = ml[(k * G + g) * 2];
-      if (mk == -INFINITY || !owns(w_first + k)) continue;
-      const float sc = exp2f(mk - mg);
-      const float2 ov = *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(k) * G * D + g * D + dd);
-      a0 = fmaf(sc, ov.x, a0);
-      a1 = fmaf(sc, ov.y, a1);
-    }
-    const float r0 = a0 * s_inv[g], r1 = a1 * s_inv[g];
-    if (p.out_f32) reinterpret_cast<float2 *>(p.out)[obase / 2 + i] = make_float2(r0, r1);
-    else reinterpret_cast<uint32_t *>(p.out)[obase / 2 + i] = pack2<QDT>(r0, r1);
-  }
-}
-
 template <int D, int G, int CDT, int QDT>
 struct DecodeInstance {
   using C = DecodeCfg<D, G, CDT, QDT>;
@@ -565,11 +633,7 @@ struct DecodeInstance {
   }
   static cudaError_t launch(const DecodeParams &p, int grid, int64_t *launches) {
     paged_decode_kernel<D, G, CDT, QDT><<<grid, C::kThreads, C::kSmem, p.stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    paged_reduce_kernel<D, G, QDT><<<p.num_seqs * p.num_kv_heads, 128, 0, p.stream>>>(
-        p, static_cast<int64_t>(grid) * C::kWarps);
-    *launches += 2;
+    *launches += 1;
     return cudaGetLastError();
   }
 };

@@ -28,6 +28,8 @@ struct DecodeParams {
   int32_t num_blocks;
   float scale_log2;  // scale * log2(e)
   int32_t *ws_cum;   // [num_seqs + 1] exclusive prefix sum of blocks per sequence
+  uint32_t *ws_ctr;  // [2][num_seqs * num_kv_heads] partials stored per item; bank epoch & 1
+  uint32_t epoch;    // one value per decode call; consecutive calls alternate banks
   float *ws_ml;      // [slots][G][2] partial (max, sum), base-2 domain
   float *ws_o;       // [slots][G][head_dim] partial unnormalised outputs
   int32_t *d_error;
@@ -37,7 +39,7 @@ struct DecodeParams {
 enum DecodeOp { kDecodePrepare = 0, kDecodeLaunch = 1 };
 
 // op == kDecodePrepare: *ctas_per_sm = resident CTAs per SM of the instance.
-// op == kDecodeLaunch: launch the partial kernel on `grid` CTAs, then the reduce.
+// op == kDecodeLaunch: launch the decode kernel on `grid` CTAs (it merges split items itself).
 // Returns cudaErrorNotSupported when (head_dim, group) has no instance.
 cudaError_t decode_call_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
                             int64_t *launches, int *ctas_per_sm);

@@ -1,6 +1,6 @@
 // Tensor-core variant of the paged decode partial kernel (head_dim 128).
 //
-// Same work split, staging ring, partial format and reduce kernel as
+// Same work split, staging ring, partial format and in-kernel merge as
 // paged_decode_kernel; the arithmetic of one (block, KV head) tile moves to
 // mma.sync m16n8k16 (fp32 accumulate):
 //   S^T[16 tokens x 8 heads] = K[16 x 128] . Q^T[128 x 8]      (8 MMAs)
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, 1)
   const int g = lane >> 2;   // MMA row group
   const int q4 = lane & 3;   // thread within the group
 
-  scan_blocks_and_init<C::kWarps, C::kStages>(p, cum, misc, bars_all);
+  scan_blocks_and_init<C::kWarps, C::kStages>(p, cum, misc, bars_all, G * D * p.num_kv_heads);
 
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * C::kWarps;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * C::kWarps + warp;
@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, 1)
         }
       }
     }
+    if (!whole) finish_partial<D, G, QDT>(p, cum, item, total, nwarps);
   };
 
   // tokens whose V rows this lane reads (B-fragment k rows of P^T)
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, 1)
 
     if (d.x >= 0) {
       // ---- S^T = K Q^T: lane rows g and g + 8, head columns 2 q4, 2 q4 + 1 ----
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      float sacc4[4][4] = {};  // four independent accumulation chains over the 8 k-steps
       if constexpr (C::kFp8) {
         uint4 kr[2][2];  // [row g, g + 8][chunk 2 q4 + j]
 #pragma unroll
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, 1)
           uint32_t a[4];
           e4m3x4_to_f16(word(kr[0][s >> 2], s & 3), a[0], a[2]);
           e4m3x4_to_f16(word(kr[1][s >> 2], s & 3), a[1], a[3]);
-          mma_16816(sacc, a, qb[s][0], qb[s][1], false);
+          mma_16816(sacc4[s & 3], a, qb[s][0], qb[s][1], false);
         }
       } else {
         uint4 kr[2][2][2];  // [row][half][chunk 2 q4 + j]
@@ -322,9 +323,12 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, 1)
           const int h = s >> 2, j = (s & 3) >> 1, t = s & 1;
           uint32_t a[4] = {word(kr[0][h][j], 2 * t), word(kr[1][h][j], 2 * t), word(kr[0][h][j], 2 * t + 1),
                            word(kr[1][h][j], 2 * t + 1)};
-          mma_16816(sacc, a, qb[s][0], qb[s][1], C::kBf16);
+          mma_16816(sacc4[s & 3], a, qb[s][0], qb[s][1], C::kBf16);
         }
       }
+      float sacc[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sacc[c] = (sacc4[0][c] + sacc4[1][c]) + (sacc4[2][c] + sacc4[3][c]);
       // ---- scale, mask, online softmax (base 2) ----
       float sc0 = p.scale_log2, sc1 = p.scale_log2;
       if constexpr (C::kFp8) {
@@ -449,11 +453,7 @@ struct MmaInstance {
   static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                             int64_t *launches) {
     paged_decode_mma_kernel<G, CDT, QDT><<<grid, C::kThreads, C::kSmem, p.stream>>>(p, tmk, tmv);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    paged_reduce_kernel<C::kD, G, QDT><<<p.num_seqs * p.num_kv_heads, 128, 0, p.stream>>>(
-        p, static_cast<int64_t>(grid) * C::kWarps);
-    *launches += 2;
+    *launches += 1;
     return cudaGetLastError();
   }
 };

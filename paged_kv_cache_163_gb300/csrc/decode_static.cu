@@ -16,9 +16,11 @@
 // any stream capture.
 //
 // Every call on a device shares the one buffer, and the buffer keeps the last
-// call's contents.  Nothing in it has to start at zero: each call writes
-// every word it later reads.  Calls whose kernels overlap on the GPU (for
-// example on two concurrent streams) race on the buffer, so serialise them.
+// call's contents.  The decode's per-item counters must start at zero or at
+// a value an earlier call left, so the set-up also zero-fills the buffer
+// once (cudaMemset, no allocation).  Calls whose kernels overlap on the GPU
+// (for example on two concurrent streams) race on the buffer, so serialise
+// them.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -55,6 +57,11 @@ pkv_status scratch_for_current_device(void **out) {
     if (e != cudaSuccess || p == nullptr) {
       std::string msg = std::string("paged_attention_decode_static: cudaGetSymbolAddress: ") +
                         cudaGetErrorString(e);
+      return fail(PKV_ERR_CUDA, msg.c_str());
+    }
+    e = cudaMemset(p, 0, kStaticScratchBytes);
+    if (e != cudaSuccess) {
+      std::string msg = std::string("paged_attention_decode_static: cudaMemset: ") + cudaGetErrorString(e);
       return fail(PKV_ERR_CUDA, msg.c_str());
     }
     g_scratch_ptr[dev] = p;

@@ -180,7 +180,7 @@ class PagedKVCache:
         if key not in self._ws:
             n = capi.paged_attention_workspace_bytes(num_seqs, num_q_heads, self.num_kv_heads, self.head_dim,
                                                      q_dtype, self.cache_dtype)
-            self._ws[key] = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+            self._ws[key] = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.device)  # zero once
         return self._ws[key]
 
     def decode(self, seq_ids, q, scale=None, out=None, layers=None, stream=None):

@@ -259,3 +259,34 @@ def test_stepper_rejects_bad_batches_without_changes(play):
     assert [cache.seq_len(s) for s in w.seq_ids] == before
     assert cache.check() == 0
     cache.close()
+
+
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
+def test_more_warps_than_tiles(play, kernel_kind):
+    # the grid is sized from the longest context, so one long sequence among many
+    # one-token ones leaves some warps without a tile (and items split across few)
+    lens = [3000] + [1] * 40 + [17] * 23
+    w = wl.custom("sparse", lens=lens, num_q_heads=4, num_kv_heads=2, head_dim=128, q_dtype="bf16",
+                  cache_dtype="bf16", seed=41)
+    cache, out = play.run(w, out_dtype="f32")
+    assert cache.check() == 0
+    q = w.q_rows(0)
+    got = to_f64(out[0])
+    for s in (0, 1, 20, 41, 63):
+        assert_close(got[s], oracle_seq_output(w, s, q[s]), f"sequence {s}")
+    cache.close()
+
+
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
+def test_repeated_calls_reuse_the_workspace(play, kernel_kind):
+    # split items are merged through per-item counters kept in the workspace across calls
+    w = wl.make(2, num_seqs=8)
+    cache, out = play.run(w, out_dtype="f32")
+    q = play.to_device(w.q_rows(0), w.q_dtype, "cuda")
+    first = cache.decode(w.seq_ids, q, scale=w.scale, out=torch.empty(q.shape, device="cuda"))
+    for _ in range(5):
+        again = cache.decode(w.seq_ids, q, scale=w.scale, out=torch.empty(q.shape, device="cuda"))
+        assert torch.equal(first, again)
+    assert torch.equal(first, out[0])
+    assert cache.check() == 0
+    cache.close()
