@@ -45,12 +45,16 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per decode call (dram__bytes_read.sum + dram__bytes_write.sum, one
 # ncu capture), keyed by workload and by the hash of the decode kernel source it
 # was taken on; reported only while the source is unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # decode kernel source 377da658dbf8e89c (tensor-core kernel, in-kernel merge), default "auto" variant
+    ("long-fp8", "377da658dbf8e89c"): 813_211_392,    # 810.06 MB read + 3.15 MB written
+    ("llama3-8b", "377da658dbf8e89c"): 146_095_360,   # 142.70 MB read + 3.39 MB written
+}
 
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cuh", "common.cuh"):
+    for f in ("decode.cuh", "decode_mma.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_163_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -115,9 +119,14 @@ def step_accounting(w: wl.Workload, step: int):
     table_bytes = int(sum(-(-int(L) // 16) for L in lens)) * 4
     lens_bytes = w.num_seqs * 4
     out_bytes = q_bytes
-    return {"tokens": tokens, "kv_bytes": kv,
-            "algo_bytes": kv + q_bytes + table_bytes + lens_bytes + out_bytes,
-            "roofline_bytes": kv + q_bytes + table_bytes + lens_bytes}
+    # Bytes in HBM: a shared prefix's full blocks are held (and need reading) once;
+    # every sequence holds its own copy of the partial block and its suffix.
+    shared = (w.prefix_len // 16) * 16
+    unique_tokens = shared + int((lens - shared).sum()) if shared else tokens
+    kv_unique = kv * unique_tokens // tokens
+    return {"tokens": tokens, "kv_bytes": kv, "kv_unique_bytes": kv_unique,
+            "algo_bytes": kv_unique + q_bytes + table_bytes + lens_bytes + out_bytes,
+            "roofline_bytes": kv_unique + q_bytes + table_bytes + lens_bytes}
 
 
 def workload_config(w: wl.Workload, name: str, extra=None):
@@ -272,7 +281,7 @@ def run_ours(args, world, rank, local):
     per_launch_bytes = statistics.mean(a["roofline_bytes"] for a in steps_acc)
     per_launch_s = t_attn / (args.steps * w.num_layers)
     achieved = per_launch_bytes / per_launch_s / 1e9
-    traffic = NCU_TRAFFIC.get((args.workload, kernel_hash()))
+    traffic = NCU_TRAFFIC.get((args.workload, kernel_hash())) if args.kernel == "auto" else None
     value = whole_job_rate(world, kv_total, t_total) / 1e9
     result = {
         "metric": METRIC,
@@ -292,6 +301,8 @@ def run_ours(args, world, rank, local):
         "hbm_frac_step": round(value / world / peak, 4),
         "seq_tokens_per_s_per_layer": round(world * tok_total / (t_total / w.num_layers), 1),
         "attn_only": {"kv_read_gbs": round(kv_total / t_attn / 1e9, 2),
+                      "kv_unique_gbs": round(sum(a["kv_unique_bytes"] for a in steps_acc) * w.num_layers
+                                             / t_attn / 1e9, 2),
                       "ms_per_step": round(t_attn * 1e3 / args.steps, 4)},
         "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel + paged_reduce_kernel (one decode call)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": f"{peak_kind} copy GB/s",

@@ -85,7 +85,12 @@ struct MmaCfg {
   static constexpr int kScale = kFp8 ? kBS * 4 : 0;
   static constexpr int kQ = G * kD * 2;
   static constexpr int kAux = round_up_c(2 * kScale + kQ, 128);  // [k scales][v scales][q rows]
-  static constexpr int kStages = clamp_c(27900 / (kKV + kAux), 2, 6);
+  // Two stages per warp: measured faster than deeper rings on GB300 (more
+  // copies in flight than HBM needs only lengthen the queues).
+  static constexpr int kStages = 2;
+  // FP8 tiles are half the bytes: two CTAs (16 warps) per SM, at most 128
+  // registers a thread, measured faster than one; 16-bit tiles keep one.
+  static constexpr int kMinBlocks = kFp8 ? 2 : 1;
   static constexpr int kCumBytes = round_up_c((PKV_MAX_SEQS_PER_CALL + 1) * 4, 128);
   static constexpr int kMiscBytes = 128;
   static constexpr int kBarBytes = round_up_c(kWarps * kStages * 8, 128);
@@ -94,7 +99,7 @@ struct MmaCfg {
   static constexpr int kTilesOff = round_up_c(kHead, 1024);
   static constexpr int kSmem = 1024 + kTilesOff + kWarps * kStages * (kKV + kAux);
   static_assert(G >= 1 && G <= 8, "group size");
-  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kSmem * kMinBlocks <= 232448, "shared memory budget");
 };
 
 // head_dim index of output row m (0..15) of m-tile i for lane group g (see kernel comment).
@@ -104,7 +109,7 @@ __device__ __forceinline__ int out_d(int g, int i, int hrow) {
 }
 
 template <int G, int CDT, int QDT>
-__global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, 1)
+__global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, QDT>::kMinBlocks)
     paged_decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv) {
   using C = MmaCfg<G, CDT, QDT>;
