@@ -46,9 +46,9 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu capture), keyed by workload and by the hash of the decode kernel source it
 # was taken on; reported only while the source is unchanged.
 NCU_TRAFFIC = {
-    # decode kernel source 377da658dbf8e89c (tensor-core kernel, in-kernel merge), default "auto" variant
-    ("long-fp8", "377da658dbf8e89c"): 813_211_392,    # 810.06 MB read + 3.15 MB written
-    ("llama3-8b", "377da658dbf8e89c"): 146_095_360,   # 142.70 MB read + 3.39 MB written
+    # decode kernel source 0e9e55bcdd3685bb (tensor-core kernel, two-stage rings), default "auto" variant
+    ("long-fp8", "0e9e55bcdd3685bb"): 814_920_960,    # 810.41 MB read + 4.51 MB written
+    ("llama3-8b", "0e9e55bcdd3685bb"): 145_818_880,   # 142.71 MB read + 3.11 MB written
 }
 
 
