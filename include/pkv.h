@@ -265,15 +265,18 @@ typedef struct {
 typedef struct pkv_stepper pkv_stepper;
 
 /* Bytes of pinned host staging and of device metadata a stepper needs for
- * batches of up to max_seqs sequences of up to max_blocks_per_seq blocks. */
+ * batches of up to max_seqs sequences of up to max_blocks_per_seq blocks
+ * (both double-buffered). */
 size_t pkv_stepper_host_bytes(int32_t max_seqs, int32_t max_blocks_per_seq);
 size_t pkv_stepper_device_bytes(int32_t max_seqs, int32_t max_blocks_per_seq);
 
 /* All buffers are caller-owned and must outlive the stepper: host_staging
- * pinned host memory of pkv_stepper_host_bytes (double-buffered, each half
- * guarded by an event), dev_meta device memory of pkv_stepper_device_bytes,
- * workspace of paged_attention_workspace_bytes(max_seqs, ...).  The pool
- * descriptor is copied.  The stepper creates two CUDA events, nothing else. */
+ * pinned host memory of pkv_stepper_host_bytes, dev_meta device memory of
+ * pkv_stepper_device_bytes, workspace of paged_attention_workspace_bytes(
+ * max_seqs, ...) (zero-filled once).  The pool descriptor is copied.  The
+ * stepper creates one non-blocking stream for the metadata transfers (so
+ * they overlap the caller stream's earlier work) and four events; nothing
+ * else.  The caller's stream waits for each transfer with an event. */
 pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32_t max_blocks_per_seq,
                               int32_t *host_staging, size_t host_staging_bytes, int32_t *dev_meta,
                               size_t dev_meta_bytes, void *workspace, size_t workspace_bytes,

@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
                                                      float *__restrict__ v_scale,
                                                      int32_t num_blocks, int32_t *err) {
   constexpr int EPL = D / 32;  // elements per lane
+  // A decode launched after this kernel as a programmatic dependent may start
+  // its prologue now; it waits for this grid to finish before reading K / V.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads * 2;

@@ -136,7 +136,7 @@ DecodeFn pick_decode(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 struct DecodeLayout {
-  int64_t cum_bytes, ctr_bytes, ml_bytes, o_bytes, total;
+  int64_t ctr_bytes, ml_bytes, o_bytes, total;
   int max_ctas;
 };
 
@@ -164,11 +164,10 @@ pkv_status decode_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   lay->max_ctas = sms * ctas;
   const int64_t slots = static_cast<int64_t>(lay->max_ctas) * kDecodeWarps +
                         static_cast<int64_t>(num_seqs) * num_kv_heads;
-  lay->cum_bytes = round256((static_cast<int64_t>(num_seqs) + 1) * 4);
   lay->ctr_bytes = round256(2 * static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
   lay->ml_bytes = round256(slots * group * 2 * 4);
   lay->o_bytes = round256(slots * group * head_dim * 4);
-  lay->total = lay->cum_bytes + lay->ctr_bytes + lay->ml_bytes + lay->o_bytes;
+  lay->total = lay->ctr_bytes + lay->ml_bytes + lay->o_bytes;
   return PKV_OK;
 }
 
@@ -264,15 +263,17 @@ pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads
   return PKV_OK;
 }
 
-pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
-                                  const void *k_cache,
-                                  const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
-                                  const float *v_scale, const int32_t *block_tables,
-                                  int32_t max_blocks_per_seq, const int32_t *context_lens,
-                                  int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
-                                  int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
-                                  float scale, void *workspace, size_t workspace_bytes,
-                                  int32_t *d_error, pkv_stream_t stream) {
+}  // extern "C"
+
+namespace pkv {
+
+pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                            const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
+                            const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                            float scale, void *workspace, size_t workspace_bytes, int32_t *d_error,
+                            pkv_stream_t stream) {
   if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS_PER_CALL)
     return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: num_seqs must be in [0, 1024]");
   pkv_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
@@ -314,13 +315,13 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
   p.num_kv_heads = num_kv_heads;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.ws_cum = reinterpret_cast<int32_t *>(ws);
-  p.ws_ctr = reinterpret_cast<uint32_t *>(ws + lay.cum_bytes);
-  p.ws_ml = reinterpret_cast<float *>(ws + lay.cum_bytes + lay.ctr_bytes);
-  p.ws_o = reinterpret_cast<float *>(ws + lay.cum_bytes + lay.ctr_bytes + lay.ml_bytes);
+  p.ws_ctr = reinterpret_cast<uint32_t *>(ws);
+  p.ws_ml = reinterpret_cast<float *>(ws + lay.ctr_bytes);
+  p.ws_o = reinterpret_cast<float *>(ws + lay.ctr_bytes + lay.ml_bytes);
   p.epoch = ++g_epoch;
   p.d_error = d_error;
   p.stream = reinterpret_cast<cudaStream_t>(stream);
+  p.programmatic = programmatic ? 1 : 0;
   s = prepare_counters(workspace, num_seqs, num_kv_heads, p.ws_ctr, static_cast<size_t>(lay.ctr_bytes), p.stream);
   if (s != PKV_OK) return s;
 
@@ -352,6 +353,25 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
   }
   if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode");
   return PKV_OK;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                  const void *k_cache,
+                                  const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
+                                  const float *v_scale, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                  int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                                  float scale, void *workspace, size_t workspace_bytes,
+                                  int32_t *d_error, pkv_stream_t stream) {
+  return pkv::attention_decode(false, out, out_dtype, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
+                               block_tables, max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                               num_q_heads, num_kv_heads, head_dim, num_blocks, scale, workspace,
+                               workspace_bytes, d_error, stream);
 }
 
 pkv_status pkv_read_device_error(int32_t *d_error, int32_t *h_error, int32_t clear,

@@ -125,13 +125,11 @@ __device__ __forceinline__ int2 tile_desc(const DecodeParams &p, const int32_t *
   return make_int2(blk, (item << 7) | ((lb == 0) << 6) | ((lb == nb - 1) << 5) | ntok);
 }
 
-// CTA prologue shared by the decode kernels: blocks per sequence (validating
-// every context length), their exclusive prefix sum cum[0..num_seqs] in shared
-// memory (CTA 0 also stores it to the workspace for the reduce kernel), and
-// the initialisation of each warp's kStages stage barriers.
+// CTA prologue shared by the decode kernels, reading only the context lengths:
+// blocks per sequence (validating every length), their exclusive prefix sum
+// cum[0..num_seqs] in shared memory, and each warp's kStages stage barriers.
 template <int kWarps, int kStages>
-__device__ __forceinline__ void scan_blocks_and_init(const DecodeParams &p, int32_t *cum, int32_t *misc,
-                                                     uint64_t *bars_all, int out_row_elems) {
+__device__ __forceinline__ void scan_blocks(const DecodeParams &p, int32_t *cum, int32_t *misc, uint64_t *bars_all) {
   constexpr int kThreads = kWarps * 32;
   constexpr int PER = (PKV_MAX_SEQS_PER_CALL + kThreads - 1) / kThreads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -180,16 +178,21 @@ __device__ __forceinline__ void scan_blocks_and_init(const DecodeParams &p, int3
     run += nbk[i];
   }
   if (tid == 0) cum[p.num_seqs] = misc[16 + kWarps - 1];
-  {  // the next call's counter bank starts from zero
-    const int items = p.num_seqs * p.num_kv_heads;
-    uint32_t *other = p.ws_ctr + ((p.epoch & 1) ^ 1) * items;
-    for (int i = blockIdx.x * kThreads + tid; i < items; i += gridDim.x * kThreads) other[i] = 0u;
-  }
   fence_barrier_init();
   __syncthreads();
+}
+
+// Global writes of the prologue, after griddep_wait(): the next call's
+// counter bank starts from zero (all CTAs share the clearing), and CTA 0
+// writes zero output for sequences without tokens (or with an invalid
+// length), which read nothing.
+template <int kThreads>
+__device__ __forceinline__ void publish_scan(const DecodeParams &p, const int32_t *cum, int out_row_elems) {
+  const int tid = threadIdx.x;
+  const int items = p.num_seqs * p.num_kv_heads;
+  uint32_t *other = p.ws_ctr + ((p.epoch & 1) ^ 1) * items;
+  for (int i = blockIdx.x * kThreads + tid; i < items; i += gridDim.x * kThreads) other[i] = 0u;
   if (blockIdx.x == 0) {
-    for (int s = tid; s <= p.num_seqs; s += kThreads) p.ws_cum[s] = cum[s];
-    // sequences without tokens (or with an invalid length) read nothing: zero output
     for (int s = tid; s < p.num_seqs; s += kThreads) {
       if (cum[s + 1] != cum[s]) continue;
       const size_t base = static_cast<size_t>(s) * out_row_elems;
@@ -199,6 +202,14 @@ __device__ __forceinline__ void scan_blocks_and_init(const DecodeParams &p, int3
       }
     }
   }
+}
+
+// Programmatic dependent launch: a decode kernel launched as a dependent may
+// start while the previous kernel on the stream finishes; it reads only the
+// lengths and tables (which that kernel does not write) before waiting here.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Warps in [w_first, w_last] (the warps whose shares meet an item) that own
@@ -363,7 +374,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  scan_blocks_and_init<C::kWarps, C::kStages>(p, cum, misc, bars_all, G * D * p.num_kv_heads);
+  scan_blocks<C::kWarps, C::kStages>(p, cum, misc, bars_all);
 
   // ---- this warp's share of the tiles --------------------------------------
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * C::kWarps;
@@ -372,7 +383,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
   const int64_t t0 = gw * total / nwarps;
   const int64_t t1 = (gw + 1) * total / nwarps;
   const int count = static_cast<int>(t1 - t0);
-  if (count <= 0) return;
 
   uint64_t *bars = bars_all + warp * C::kStages;
   int2 *desc = desc_all + warp * 64;
@@ -415,8 +425,16 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
     }
   };
 
-  fill_window(0);
-  fill_window(1);
+  if (count > 0) {
+    fill_window(0);
+    fill_window(1);
+  }
+  griddep_wait();  // from here the previous kernel's writes are visible
+  publish_scan<C::kThreads>(p, cum, G * D * p.num_kv_heads);
+  if (count <= 0) {
+    griddep_launch_dependents();
+    return;
+  }
   __syncwarp();
 #pragma unroll 1
   for (int i = 0; i < C::kStages && i < count; ++i) issue(i);
@@ -610,6 +628,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
     __syncwarp();  // the stage is free again
     if (n + C::kStages < count) issue(n + C::kStages);
   }
+  griddep_launch_dependents();
   flush(cur_item, whole_start && saw_last);
 }
 
@@ -632,9 +651,10 @@ struct DecodeInstance {
     return cudaSuccess;
   }
   static cudaError_t launch(const DecodeParams &p, int grid, int64_t *launches) {
-    paged_decode_kernel<D, G, CDT, QDT><<<grid, C::kThreads, C::kSmem, p.stream>>>(p);
-    *launches += 1;
-    return cudaGetLastError();
+    const cudaError_t e = launch_decode(paged_decode_kernel<D, G, CDT, QDT>, grid, C::kThreads, C::kSmem, p.stream,
+                                        p.programmatic, p);
+    if (e == cudaSuccess) *launches += 1;
+    return e;
   }
 };
 

@@ -27,14 +27,33 @@ struct DecodeParams {
   int32_t num_kv_heads;
   int32_t num_blocks;
   float scale_log2;  // scale * log2(e)
-  int32_t *ws_cum;   // [num_seqs + 1] exclusive prefix sum of blocks per sequence
   uint32_t *ws_ctr;  // [2][num_seqs * num_kv_heads] partials stored per item; bank epoch & 1
   uint32_t epoch;    // one value per decode call; consecutive calls alternate banks
   float *ws_ml;      // [slots][G][2] partial (max, sum), base-2 domain
   float *ws_o;       // [slots][G][head_dim] partial unnormalised outputs
   int32_t *d_error;
   cudaStream_t stream;
+  int32_t programmatic;  // 1: launch as a programmatic dependent of the stream's previous kernel
 };
+
+// Launch `kernel` on `stream`; with programmatic != 0 the launch may begin
+// before the previous kernel on the stream has finished (the kernel waits on
+// griddepcontrol.wait before it reads what that kernel writes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_decode(void (*kernel)(KArgs...), int grid, int threads, int smem, cudaStream_t stream,
+                          int programmatic, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = programmatic ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
 
 enum DecodeOp { kDecodePrepare = 0, kDecodeLaunch = 1 };
 
@@ -60,5 +79,17 @@ cudaError_t decode_mma_call_fp8_f16(int group, int op, const DecodeParams *p, co
                                     const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
 cudaError_t decode_mma_call_fp8_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                      const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
+
+// paged_attention_decode with a choice of launch: programmatic == true lets
+// the kernel start while the stream's previous kernel finishes.  Only for
+// callers that know that kernel writes neither the block tables nor the
+// context lengths (the decode kernel reads those before it waits).
+pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                            const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
+                            const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                            float scale, void *workspace, size_t workspace_bytes, int32_t *d_error,
+                            pkv_stream_t stream);
 
 }  // namespace pkv

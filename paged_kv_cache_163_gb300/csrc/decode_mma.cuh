@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
   const int g = lane >> 2;   // MMA row group
   const int q4 = lane & 3;   // thread within the group
 
-  scan_blocks_and_init<C::kWarps, C::kStages>(p, cum, misc, bars_all, G * D * p.num_kv_heads);
+  scan_blocks<C::kWarps, C::kStages>(p, cum, misc, bars_all);
 
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * C::kWarps;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * C::kWarps + warp;
@@ -137,7 +137,6 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
   const int64_t t0 = gw * total / nwarps;
   const int64_t t1 = (gw + 1) * total / nwarps;
   const int count = static_cast<int>(t1 - t0);
-  if (count <= 0) return;
 
   uint64_t *bars = bars_all + warp * C::kStages;
   int2 *desc = desc_all + warp * 64;
@@ -187,8 +186,16 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
     }
   };
 
-  fill_window(0);
-  fill_window(1);
+  if (count > 0) {
+    fill_window(0);
+    fill_window(1);
+  }
+  griddep_wait();  // from here the previous kernel's writes are visible
+  publish_scan<C::kThreads>(p, cum, G * D * p.num_kv_heads);
+  if (count <= 0) {
+    griddep_launch_dependents();
+    return;
+  }
   __syncwarp();
 #pragma unroll 1
   for (int i = 0; i < C::kStages && i < count; ++i) issue(i);
@@ -434,6 +441,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
     __syncwarp();  // the stage is free again
     if (n + C::kStages < count) issue(n + C::kStages);
   }
+  griddep_launch_dependents();
   flush(cur_item, whole_start && saw_last);
 }
 
@@ -457,9 +465,10 @@ struct MmaInstance {
   }
   static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                             int64_t *launches) {
-    paged_decode_mma_kernel<G, CDT, QDT><<<grid, C::kThreads, C::kSmem, p.stream>>>(p, tmk, tmv);
-    *launches += 1;
-    return cudaGetLastError();
+    const cudaError_t e = launch_decode(paged_decode_mma_kernel<G, CDT, QDT>, grid, C::kThreads, C::kSmem,
+                                        p.stream, p.programmatic, p, tmk, tmv);
+    if (e == cudaSuccess) *launches += 1;
+    return e;
   }
 };
 

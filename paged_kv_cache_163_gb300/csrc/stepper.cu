@@ -1,5 +1,12 @@
 // Decode step executor: host block manager, one metadata transfer and every
 // layer's copy / append / decode launches in a single native call.
+//
+// The metadata transfer runs on the executor's own copy stream, so its
+// latency overlaps whatever the caller's stream is still doing (the previous
+// step); the caller's stream waits for it with an event.  Host staging and
+// device metadata are both double-buffered: half h is refilled only after the
+// copy that last read it (host) and the kernels that last read it (device)
+// are done.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -9,6 +16,7 @@
 #include <vector>
 
 #include "append.h"
+#include "decode.h"
 #include "pkv.h"
 #include "status.h"
 
@@ -16,11 +24,13 @@ struct pkv_stepper {
   pkv_pool_desc pool;
   int32_t max_seqs = 0, max_blocks = 0;
   int32_t *host = nullptr;      // two halves of `half_ints` int32
-  int32_t *dev = nullptr;
+  int32_t *dev = nullptr;       // two halves of `half_ints` int32
   size_t half_ints = 0;
   void *workspace = nullptr;
   size_t workspace_bytes = 0;
-  cudaEvent_t done[2] = {nullptr, nullptr};
+  cudaStream_t copy = nullptr;  // metadata transfers
+  cudaEvent_t copied[2] = {nullptr, nullptr};  // transfer of half h done
+  cudaEvent_t used[2] = {nullptr, nullptr};    // kernels reading device half h done
   int next = 0;
 };
 
@@ -48,7 +58,7 @@ size_t pkv_stepper_host_bytes(int32_t max_seqs, int32_t max_blocks_per_seq) {
 
 size_t pkv_stepper_device_bytes(int32_t max_seqs, int32_t max_blocks_per_seq) {
   if (max_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
-  return meta_ints(max_seqs, max_blocks_per_seq) * sizeof(int32_t);
+  return 2 * meta_ints(max_seqs, max_blocks_per_seq) * sizeof(int32_t);
 }
 
 pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32_t max_blocks_per_seq,
@@ -78,12 +88,14 @@ pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32
   st->half_ints = meta_ints(max_seqs, max_blocks_per_seq);
   st->workspace = workspace;
   st->workspace_bytes = workspace_bytes;
-  for (int i = 0; i < 2; ++i) {
-    cudaError_t e = cudaEventCreateWithFlags(&st->done[i], cudaEventDisableTiming);
-    if (e != cudaSuccess) {
-      pkv_stepper_destroy(st);
-      return cuda_fail(e, "pkv_stepper_create: cudaEventCreate");
-    }
+  cudaError_t e = cudaStreamCreateWithFlags(&st->copy, cudaStreamNonBlocking);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&st->copied[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->used[i], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {
+    pkv_stepper_destroy(st);
+    return cuda_fail(e, "pkv_stepper_create: stream or event creation");
   }
   *out = st;
   return PKV_OK;
@@ -91,8 +103,12 @@ pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32
 
 void pkv_stepper_destroy(pkv_stepper *st) {
   if (!st) return;
-  for (auto &e : st->done)
+  if (st->copy) cudaStreamSynchronize(st->copy);
+  for (auto &e : st->copied)
     if (e) cudaEventDestroy(e);
+  for (auto &e : st->used)
+    if (e) cudaEventDestroy(e);
+  if (st->copy) cudaStreamDestroy(st->copy);
   delete st;
 }
 
@@ -129,7 +145,7 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   }
   // Host staging half: wait until the transfer that last read it is done.
   const int h = st->next;
-  cudaError_t e = cudaEventSynchronize(st->done[h]);
+  cudaError_t e = cudaEventSynchronize(st->copied[h]);
   if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventSynchronize");
   int32_t *H = st->host + h * st->half_ints;
   int32_t *slots = H, *src = H + n, *dst = H + 2 * n, *lens = H + 3 * n, *tables = H + 4 * n;
@@ -142,12 +158,15 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   if (cow_src && ncow) std::memcpy(cow_src, src, sizeof(int32_t) * ncow);
   if (cow_dst && ncow) std::memcpy(cow_dst, dst, sizeof(int32_t) * ncow);
   const size_t ints = static_cast<size_t>(n) * 4 + static_cast<size_t>(n) * mb;
-  e = cudaMemcpyAsync(st->dev, H, ints * sizeof(int32_t), cudaMemcpyHostToDevice, cs);
-  if (e == cudaSuccess) e = cudaEventRecord(st->done[h], cs);
+  int32_t *Dh = st->dev + h * st->half_ints;
+  e = cudaStreamWaitEvent(st->copy, st->used[h], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(Dh, H, ints * sizeof(int32_t), cudaMemcpyHostToDevice, st->copy);
+  if (e == cudaSuccess) e = cudaEventRecord(st->copied[h], st->copy);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, st->copied[h], 0);
   if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: metadata transfer");
   st->next ^= 1;
-  const int32_t *d_slots = st->dev, *d_src = st->dev + n, *d_dst = st->dev + 2 * n;
-  const int32_t *d_lens = st->dev + 3 * n, *d_tables = st->dev + 4 * n;
+  const int32_t *d_slots = Dh, *d_src = Dh + n, *d_dst = Dh + 2 * n;
+  const int32_t *d_lens = Dh + 3 * n, *d_tables = Dh + 4 * n;
 
   auto layer_ptr = [](const void *base, int64_t stride, int32_t l) {
     return static_cast<uint8_t *>(const_cast<void *>(base)) + l * stride;
@@ -174,18 +193,23 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");
   }
   for (int32_t l = 0; l < P.num_layers; ++l) {
-    s = paged_attention_decode(layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l),
-                               P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
-                               layer_ptr(P.v_cache, P.cache_layer_stride, l), P.cache_dtype, scale_ptr(P.k_scale, l),
-                               scale_ptr(P.v_scale, l), d_tables, mb, d_lens, max_len, n, P.num_q_heads,
-                               P.num_kv_heads, P.head_dim, P.num_blocks, scale, st->workspace, st->workspace_bytes,
-                               d_error, stream);
+    // The kernels before each decode on this stream are this step's appends
+    // and decodes, which write neither the tables nor the lengths: the decode
+    // may start early and overlap its prologue with their tail.
+    s = pkv::attention_decode(true, layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l),
+                              P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
+                              layer_ptr(P.v_cache, P.cache_layer_stride, l), P.cache_dtype, scale_ptr(P.k_scale, l),
+                              scale_ptr(P.v_scale, l), d_tables, mb, d_lens, max_len, n, P.num_q_heads,
+                              P.num_kv_heads, P.head_dim, P.num_blocks, scale, st->workspace, st->workspace_bytes,
+                              d_error, stream);
     if (s != PKV_OK) return s;
   }
   if (attn_end) {
     e = cudaEventRecord(static_cast<cudaEvent_t>(attn_end), cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");
   }
+  e = cudaEventRecord(st->used[h], cs);
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");
   return PKV_OK;
 }
 
