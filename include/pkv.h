@@ -248,10 +248,12 @@ pkv_status paged_attention_decode_static(void *out, pkv_dtype out_dtype, const v
 /* Decode step executor: one call runs a whole decode step of a batch        */
 /* ("KV Cache 与 vLLM" §3.1-§3.4, "企业官网建设流程全解析" §3.2): the block    */
 /* manager gives every sequence a slot (taking or copying blocks), the slot   */
-/* mapping, copy pairs, lengths and block tables go to the device in one      */
-/* transfer, and for every layer the shared blocks are copied, the new K/V    */
-/* rows are written and the new queries attend.  Host work is O(batch +       */
-/* table size); all device work is enqueued on `stream`.                      */
+/* mapping, copy pairs, lengths and block tables are written to page-locked   */
+/* host staging that the first layer's kernels read in place (its append      */
+/* also copies them to device memory for the later layers), and for every     */
+/* layer the shared blocks are copied, the new K/V rows are written and the   */
+/* new queries attend.  Host work is O(batch + table size); all device work   */
+/* is enqueued on `stream`.                                                   */
 /* ------------------------------------------------------------------------ */
 typedef struct {
   int32_t num_layers, num_blocks, num_kv_heads, num_q_heads, head_dim;
@@ -271,12 +273,16 @@ size_t pkv_stepper_host_bytes(int32_t max_seqs, int32_t max_blocks_per_seq);
 size_t pkv_stepper_device_bytes(int32_t max_seqs, int32_t max_blocks_per_seq);
 
 /* All buffers are caller-owned and must outlive the stepper: host_staging
- * pinned host memory of pkv_stepper_host_bytes, dev_meta device memory of
- * pkv_stepper_device_bytes, workspace of paged_attention_workspace_bytes(
- * max_seqs, ...) (zero-filled once).  The pool descriptor is copied.  The
- * stepper creates one non-blocking stream for the metadata transfers (so
- * they overlap the caller stream's earlier work) and four events; nothing
- * else.  The caller's stream waits for each transfer with an event. */
+ * page-locked host memory (cudaHostAlloc / cudaHostRegister, or a pinned
+ * tensor) of pkv_stepper_host_bytes, read by kernels in place through its
+ * device address; dev_meta device memory of pkv_stepper_device_bytes; both
+ * 16-byte aligned; workspace of paged_attention_workspace_bytes(max_seqs, ...)
+ * (zero-filled once).  The pool descriptor is copied.  The stepper creates
+ * two events and nothing else.  Each step uses one half of the staging and of
+ * dev_meta, alternating; a step waits (on the host) until the step two calls
+ * earlier, which used the same half, has finished on the device, and (when
+ * that step ran on another stream) makes `stream` wait for it too.
+ * pkv_stepper_destroy waits for the last steps before it returns. */
 pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32_t max_blocks_per_seq,
                               int32_t *host_staging, size_t host_staging_bytes, int32_t *dev_meta,
                               size_t dev_meta_bytes, void *workspace, size_t workspace_bytes,

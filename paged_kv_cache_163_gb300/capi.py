@@ -87,8 +87,9 @@ _PROTOS = {
     "pkv_stepper_create": (C.c_int, [C.POINTER(PoolDesc), C.c_int32, C.c_int32, _vp, C.c_size_t, _vp, C.c_size_t,
                                      _vp, C.c_size_t, C.POINTER(_vp)]),
     "pkv_stepper_destroy": (None, [_vp]),
-    "pkv_stepper_step": (C.c_int, [_vp, _vp, _i64p, C.c_int32, _vp, _vp, C.c_int64, _vp, C.c_int64, _vp, C.c_int,
-                                   C.c_int64, C.c_float, _i32p, _i32p, _i32p, _vp, _vp, _vp, _vp]),
+    # pointer arguments as addresses (ints): the per-step call marshals no ctypes pointer objects
+    "pkv_stepper_step": (C.c_int, [_vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int64, _vp, C.c_int64, _vp, C.c_int,
+                                   C.c_int64, C.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "pkv_read_device_error": (C.c_int, [_vp, _i32p, C.c_int32, _vp]),
     "pkv_launch_count": (C.c_int64, []),
     "pkv_set_decode_kernel": (C.c_int, [C.c_int]),
@@ -356,23 +357,74 @@ def _layer_stride(t, layers):
     return t.stride(0) * t.element_size() if t.dim() == 4 and layers > 1 else 0
 
 
+class StepScratch:
+    """Host arrays a step writes its copy pairs into, allocated once per stepper."""
+
+    def __init__(self, max_seqs: int):
+        self.src = np.empty(max(max_seqs, 1), np.int32)
+        self.dst = np.empty(max(max_seqs, 1), np.int32)
+        self.ncow = np.zeros(1, np.int32)
+        self.addr = (self.src.ctypes.data, self.dst.ctypes.data, self.ncow.ctypes.data)
+
+
+def current_stream_handle(device_index: int) -> int:
+    """cudaStream_t of torch's current stream on a device."""
+    import torch
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(device_index)
+    return torch.cuda.current_stream(device_index).cuda_stream
+
+
+_TORCH_DT = None
+
+
+def _dt_torch(dtype) -> int:
+    global _TORCH_DT
+    if _TORCH_DT is None:
+        import torch
+        _TORCH_DT = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.float32: PKV_F32,
+                     torch.uint8: PKV_FP8_E4M3}
+    return _TORCH_DT[dtype]
+
+
 def pkv_stepper_step(st, bm, seq_ids, k_new, v_new, q, out, scale, layers, d_error=None, events=None,
-                     stream=None):
-    """One decode step; returns (cow_src, cow_dst) of the step."""
-    ids = _i64(seq_ids)
-    n = len(ids)
-    src = np.empty(max(n, 1), np.int32)
-    dst = np.empty(max(n, 1), np.int32)
-    ncow = C.c_int32()
+                     stream=None, scratch: StepScratch | None = None):
+    """One decode step; returns (cow_src, cow_dst) of the step.
+
+    ``stream``: a torch stream, a cudaStream_t address, or None for the current
+    stream of q's device.  ``scratch``: reusable host arrays (else allocated).
+    """
+    ids = seq_ids if isinstance(seq_ids, np.ndarray) and seq_ids.dtype == np.int64 else \
+        np.asarray(seq_ids, dtype=np.int64)
+    if not ids.flags.c_contiguous:
+        ids = np.ascontiguousarray(ids)
+    n = ids.shape[0]
+    if scratch is None or scratch.src.shape[0] < n:
+        scratch = StepScratch(n)
     ev0 = ev1 = None
     if events is not None:
-        ev0, ev1 = (e.cuda_event for e in events)
-    _check(load().pkv_stepper_step(
-        st, bm, _ptr(ids, C.c_int64), n, _dp(k_new), _dp(v_new), _layer_stride(k_new, layers), _dp(q),
-        _layer_stride(q, layers), _dp(out), _dt(out.dtype), _layer_stride(out, layers), float(scale),
-        _ptr(src, C.c_int32), _ptr(dst, C.c_int32), C.byref(ncow), _dp(d_error), ev0, ev1, _stream(stream)),
-        "pkv_stepper_step")
-    return src[:ncow.value].copy(), dst[:ncow.value].copy()
+        ev0, ev1 = events[0].cuda_event, events[1].cuda_event
+    if stream is None:
+        sh = current_stream_handle(q.device.index)
+    elif isinstance(stream, int):
+        sh = stream
+    else:
+        sh = stream.cuda_stream
+    a_src, a_dst, a_n = scratch.addr
+    status = load().pkv_stepper_step(
+        st, bm, ids.ctypes.data, n, k_new.data_ptr(), v_new.data_ptr(), _layer_stride(k_new, layers),
+        q.data_ptr(), _layer_stride(q, layers), out.data_ptr(), _dt_torch(out.dtype), _layer_stride(out, layers),
+        float(scale), a_src, a_dst, a_n, _dp(d_error), ev0, ev1, sh)
+    if status != 0:
+        _check(status, "pkv_stepper_step")
+    ncow = int(scratch.ncow[0])
+    if ncow == 0:
+        return _EMPTY_I32, _EMPTY_I32
+    return scratch.src[:ncow].copy(), scratch.dst[:ncow].copy()
+
+
+_EMPTY_I32 = np.empty(0, np.int32)
 
 
 def pkv_read_device_error(d_error, clear: bool = True, stream=None, raise_on_error: bool = False) -> int:

@@ -24,11 +24,19 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
                                                      uint8_t *__restrict__ v_cache,
                                                      float *__restrict__ k_scale,
                                                      float *__restrict__ v_scale,
-                                                     int32_t num_blocks, int32_t *err) {
+                                                     int32_t num_blocks, int32_t *err,
+                                                     const int4 *__restrict__ meta_src,
+                                                     int4 *__restrict__ meta_dst, int64_t meta_vecs) {
   constexpr int EPL = D / 32;  // elements per lane
   // A decode launched after this kernel as a programmatic dependent may start
   // its prologue now; it waits for this grid to finish before reading K / V.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  {  // step metadata: host staging -> device (grid-stride, independent loads)
+    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+#pragma unroll 4
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < meta_vecs; i += nth)
+      meta_dst[i] = meta_src[i];
+  }
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads * 2;
@@ -118,7 +126,9 @@ static cudaError_t launch_append(const AppendArgs &a) {
   append_kernel<D, IDT, CDT><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
       static_cast<const uint8_t *>(a.k), static_cast<const uint8_t *>(a.v), a.slot_mapping,
       a.num_tokens, a.num_kv_heads, static_cast<uint8_t *>(a.k_cache),
-      static_cast<uint8_t *>(a.v_cache), a.k_scale, a.v_scale, a.num_blocks, a.d_error);
+      static_cast<uint8_t *>(a.v_cache), a.k_scale, a.v_scale, a.num_blocks, a.d_error,
+      reinterpret_cast<const int4 *>(a.meta_src), reinterpret_cast<int4 *>(a.meta_dst),
+      a.meta_src ? (a.meta_ints + 3) / 4 : 0);
   return cudaGetLastError();
 }
 

@@ -18,6 +18,12 @@ struct AppendArgs {
   int32_t num_blocks;
   int32_t *d_error;
   cudaStream_t stream;
+  // Optional: the kernel also copies meta_ints int32 from meta_src (page-locked
+  // host memory, read in place) to meta_dst (device), 16-byte vectors, with
+  // both pointers 16-byte aligned and room for meta_ints rounded up to 4.
+  const int32_t *meta_src;
+  int32_t *meta_dst;
+  int64_t meta_ints;
 };
 
 struct CopyArgs {
@@ -33,5 +39,9 @@ struct CopyArgs {
 
 cudaError_t run_append(const AppendArgs &a);
 cudaError_t run_copy_blocks(const CopyArgs &a);
+
+// Launch with the caller's validation (the step executor's); count the launch.
+pkv_status append_unchecked(const AppendArgs &a);
+pkv_status copy_blocks_unchecked(const CopyArgs &a);
 
 }  // namespace pkv

@@ -267,6 +267,20 @@ pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads
 
 namespace pkv {
 
+pkv_status append_unchecked(const AppendArgs &a) {
+  cudaError_t e = run_append(a);
+  if (e != cudaSuccess) return cuda_fail(e, "paged_kv_append");
+  ++t_launches;
+  return PKV_OK;
+}
+
+pkv_status copy_blocks_unchecked(const CopyArgs &a) {
+  cudaError_t e = run_copy_blocks(a);
+  if (e != cudaSuccess) return cuda_fail(e, "paged_kv_copy_blocks");
+  ++t_launches;
+  return PKV_OK;
+}
+
 pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
                             const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
                             const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,

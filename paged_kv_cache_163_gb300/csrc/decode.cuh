@@ -26,6 +26,8 @@
 //    the score and the per-token V scale folds into the probability.
 #pragma once
 
+#include <type_traits>
+
 #include <math.h>
 
 #include "common.cuh"
@@ -254,75 +256,74 @@ __device__ __forceinline__ bool count_partial(const DecodeParams &p, int item, i
 
 // One warp merges the partials of `item`:
 // out = sum_w 2^(m_w - M) o_w / sum_w 2^(m_w - M) l_w, M = max_w m_w.
-// Partials of other CTAs are read through L2 (ld.global.cg).  Lanes first
-// take one partial each (weights, maxima, sums by shuffles), then every lane
-// accumulates its head_dim slice over all partials with independent loads.
-template <int D, int G, int QDT>
+// Partials of other CTAs are read through L2 (ld.global.cg).  One pass over
+// chunks of 32 partials: each lane takes one partial's (m, l) per head, the
+// chunk maximum updates the running maximum M (earlier sums are rescaled by
+// 2^(M_old - M_new)), and then every lane accumulates its head_dim slice of
+// the chunk's o rows, kBatch partials at a time with all their loads issued
+// before the first use (kLoads vector loads a lane, sized to the caller's
+// register budget).  A warp that owns no tile (possible when there are fewer
+// tiles than warps) has weight 0 and its slot's contents are ignored.
+template <int D, int G, int QDT, int kLoads>
 __device__ __noinline__ void merge_item(const DecodeParams &p, int item, int64_t w_first, int64_t w_last,
                                         int64_t total, int64_t nwarps) {
   constexpr int DPL = D / 32;
+  constexpr int kBatch = kLoads / G > 0 ? kLoads / G : 1;  // partials in flight per batch
   const int lane = threadIdx.x & 31;
   const bool all_own = total >= nwarps;
   auto owns = [&](int64_t w) { return all_own || (w * total / nwarps) != ((w + 1) * total / nwarps); };
   const int np = static_cast<int>(w_last - w_first + 1);
-  const float *ml = p.ws_ml + (w_first + item) * G * 2;  // partial of warp w_first + k at ml[k * 2G]
-  const float *po = p.ws_o + (w_first + item) * G * D;
-  float acc[G][DPL];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[g][e] = 0.f;
-  float mx[G], den[G];
+  const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + (w_first + item) * G;  // [k][g] = (m, l)
+  const float *po = p.ws_o + (w_first + item) * G * D;                                 // [k][g][D]
+  float acc[G][DPL], run_m[G], den[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    mx[g] = -INFINITY;
+    run_m[g] = -INFINITY;
     den[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[g][e] = 0.f;
   }
-  // maxima over all partials (lanes stride over the partials)
   for (int k0 = 0; k0 < np; k0 += 32) {
     const int k = k0 + lane;
-    if (k < np && owns(w_first + k))
+    const bool mine = k < np && owns(w_first + k);
+    float2 mlk[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], __ldcg(ml + (k * G + g) * 2));
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(kFull, mx[g], o));
-  for (int k0 = 0; k0 < np; k0 += 32) {
-    // this lane's partial: its weight per head (0 when empty or all-masked)
-    const int k = k0 + lane;
+    for (int g = 0; g < G; ++g) mlk[g] = mine ? __ldcg(ml + static_cast<int64_t>(k) * G + g) : make_float2(-INFINITY, 0.f);
     float wk[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      wk[g] = 0.f;
-      if (k < np && owns(w_first + k)) {
-        const float mk = __ldcg(ml + (k * G + g) * 2);
-        if (mk != -INFINITY) {
-          wk[g] = exp2f(mk - mx[g]);
-          den[g] = fmaf(wk[g], __ldcg(ml + (k * G + g) * 2 + 1), den[g]);
-        }
-      }
+      float cm = mlk[g].x;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, o));
+      const float nm = fmaxf(run_m[g], cm);
+      const float rescale = run_m[g] == -INFINITY ? 0.f : exp2f(run_m[g] - nm);
+      run_m[g] = nm;
+      den[g] *= rescale;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[g][e] *= rescale;
+      wk[g] = mlk[g].x == -INFINITY ? 0.f : exp2f(mlk[g].x - nm);
+      den[g] = fmaf(wk[g], mlk[g].y, den[g]);
     }
     const int nk = min(32, np - k0);
-#pragma unroll 4
-    for (int j = 0; j < nk; ++j) {
-      const float *src = po + (static_cast<int64_t>(k0 + j) * G) * D + lane * DPL;
+    for (int j0 = 0; j0 < nk; j0 += kBatch) {
+      using Vec = typename std::conditional<DPL == 4, float4, float2>::type;
+      Vec v[kBatch][G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float w = __shfl_sync(kFull, wk[g], j);
-        if (w != 0.f) {
-          if constexpr (DPL == 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + g * D));
-            acc[g][0] = fmaf(w, v.x, acc[g][0]);
-            acc[g][1] = fmaf(w, v.y, acc[g][1]);
-            acc[g][2] = fmaf(w, v.z, acc[g][2]);
-            acc[g][3] = fmaf(w, v.w, acc[g][3]);
-          } else {
-            const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + g * D));
-            acc[g][0] = fmaf(w, v.x, acc[g][0]);
-            acc[g][1] = fmaf(w, v.y, acc[g][1]);
-          }
+      for (int b = 0; b < kBatch; ++b) {
+        const int kk = k0 + min(j0 + b, nk - 1);  // stays inside the item's slots
+        const float *src = po + static_cast<int64_t>(kk) * G * D + lane * DPL;
+#pragma unroll
+        for (int g = 0; g < G; ++g) v[b][g] = __ldcg(reinterpret_cast<const Vec *>(src + g * D));
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float w = __shfl_sync(kFull, wk[g], (j0 + b) & 31);
+          if (j0 + b >= nk) w = 0.f;
+          const float *x = reinterpret_cast<const float *>(&v[b][g]);
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) acc[g][e] = fmaf(w, w != 0.f ? x[e] : 0.f, acc[g][e]);
         }
       }
     }
@@ -350,13 +351,13 @@ __device__ __noinline__ void merge_item(const DecodeParams &p, int item, int64_t
 }
 
 // After a warp stored its partial of `item`: count it in; the last one merges.
-template <int D, int G, int QDT>
+template <int D, int G, int QDT, int kLoads = 16>
 __device__ __forceinline__ void finish_partial(const DecodeParams &p, const int32_t *cum, int item, int64_t total,
                                                int64_t nwarps) {
   int64_t w_first, w_last;
   item_warps(cum, p.num_kv_heads, item, total, nwarps, w_first, w_last);
   if (count_partial(p, item, owning_warps(w_first, w_last, total, nwarps)))
-    merge_item<D, G, QDT>(p, item, w_first, w_last, total, nwarps);
+    merge_item<D, G, QDT, kLoads>(p, item, w_first, w_last, total, nwarps);
 }
 
 template <int D, int G, int CDT, int QDT>

@@ -245,7 +245,8 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
         }
       }
     }
-    if (!whole) finish_partial<D, G, QDT>(p, cum, item, total, nwarps);
+    // the FP8 instances run two CTAs an SM (128 registers a thread): fewer loads in flight
+    if (!whole) finish_partial<D, G, QDT, C::kFp8 ? 8 : 16>(p, cum, item, total, nwarps);
   };
 
   // tokens whose V rows this lane reads (B-fragment k rows of P^T)

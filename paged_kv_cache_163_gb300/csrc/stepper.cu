@@ -1,18 +1,17 @@
-// Decode step executor: host block manager, one metadata transfer and every
-// layer's copy / append / decode launches in a single native call.
+// Decode step executor: host block manager and every layer's copy / append /
+// decode launches in a single native call, with no separate metadata transfer.
 //
-// The metadata transfer runs on the executor's own copy stream, so its
-// latency overlaps whatever the caller's stream is still doing (the previous
-// step); the caller's stream waits for it with an event.  Host staging and
-// device metadata are both double-buffered: half h is refilled only after the
-// copy that last read it (host) and the kernels that last read it (device)
-// are done.
+// The step's metadata (slot mapping, copy pairs, lengths, block tables) is
+// written to page-locked host staging, which kernels read in place: layer 0's
+// block copies and append read it directly, and layer 0's append also copies
+// it to device memory for the later layers and the decode kernels.  Staging
+// and device metadata are double-buffered; half h is rewritten only after the
+// kernels of the step that last used it are done (one event per half).
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstring>
 #include <string>
-#include <unordered_map>
 #include <vector>
 
 #include "append.h"
@@ -23,22 +22,26 @@
 struct pkv_stepper {
   pkv_pool_desc pool;
   int32_t max_seqs = 0, max_blocks = 0;
-  int32_t *host = nullptr;      // two halves of `half_ints` int32
-  int32_t *dev = nullptr;       // two halves of `half_ints` int32
+  int32_t *host = nullptr;        // two halves of `half_ints` int32 (host addresses)
+  const int32_t *host_dev = nullptr;  // the same staging as kernels address it
+  int32_t *dev = nullptr;         // two halves of `half_ints` int32
   size_t half_ints = 0;
   void *workspace = nullptr;
   size_t workspace_bytes = 0;
-  cudaStream_t copy = nullptr;  // metadata transfers
-  cudaEvent_t copied[2] = {nullptr, nullptr};  // transfer of half h done
-  cudaEvent_t used[2] = {nullptr, nullptr};    // kernels reading device half h done
+  cudaEvent_t used[2] = {nullptr, nullptr};   // the last step that used half h is done
+  cudaStream_t used_on[2] = {nullptr, nullptr};  // stream that step ran on
+  bool recorded[2] = {false, false};
+  std::vector<int64_t> ids;      // scratch for the duplicate check
   int next = 0;
 };
 
 namespace {
 
-// Layout of one metadata half: slots[n] | cow_src[n] | cow_dst[n] | lens[n] | tables[n][mb]
+// Layout of one metadata half: slots[n] | cow_src[n] | cow_dst[n] | lens[n] | tables[n][mb],
+// padded to whole 16-byte vectors (the append kernel copies it in vectors).
 size_t meta_ints(int32_t max_seqs, int32_t max_blocks) {
-  return static_cast<size_t>(max_seqs) * 4 + static_cast<size_t>(max_seqs) * max_blocks;
+  const size_t ints = static_cast<size_t>(max_seqs) * 4 + static_cast<size_t>(max_seqs) * max_blocks;
+  return (ints + 3) / 4 * 4;
 }
 
 
@@ -79,23 +82,32 @@ pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32
   if (s != PKV_OK) return s;
   if (!workspace || workspace_bytes < need)
     return pkv::fail(PKV_ERR_WORKSPACE, "pkv_stepper_create: workspace smaller than required");
+  // Kernels read the staging in place: it must be page-locked host memory
+  // with a device address (unified addressing makes it the host address).
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, host_staging);
+  if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || !attr.devicePointer) {
+    cudaGetLastError();
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: host_staging is not page-locked host memory");
+  }
+  if ((reinterpret_cast<uintptr_t>(host_staging) & 15u) || (reinterpret_cast<uintptr_t>(attr.devicePointer) & 15u) ||
+      (reinterpret_cast<uintptr_t>(dev_meta) & 15u))
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: staging and metadata must be 16-byte aligned");
   pkv_stepper *st = new pkv_stepper();
   st->pool = *pool;
   st->max_seqs = max_seqs;
   st->max_blocks = max_blocks_per_seq;
   st->host = host_staging;
+  st->host_dev = static_cast<const int32_t *>(attr.devicePointer);
   st->dev = dev_meta;
   st->half_ints = meta_ints(max_seqs, max_blocks_per_seq);
   st->workspace = workspace;
   st->workspace_bytes = workspace_bytes;
-  cudaError_t e = cudaStreamCreateWithFlags(&st->copy, cudaStreamNonBlocking);
-  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
-    e = cudaEventCreateWithFlags(&st->copied[i], cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->used[i], cudaEventDisableTiming);
-  }
+  st->ids.reserve(static_cast<size_t>(max_seqs));
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&st->used[i], cudaEventDisableTiming);
   if (e != cudaSuccess) {
     pkv_stepper_destroy(st);
-    return cuda_fail(e, "pkv_stepper_create: stream or event creation");
+    return cuda_fail(e, "pkv_stepper_create: event creation");
   }
   *out = st;
   return PKV_OK;
@@ -103,12 +115,11 @@ pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32
 
 void pkv_stepper_destroy(pkv_stepper *st) {
   if (!st) return;
-  if (st->copy) cudaStreamSynchronize(st->copy);
-  for (auto &e : st->copied)
-    if (e) cudaEventDestroy(e);
   for (auto &e : st->used)
-    if (e) cudaEventDestroy(e);
-  if (st->copy) cudaStreamDestroy(st->copy);
+    if (e) {
+      cudaEventSynchronize(e);  // the buffers may be freed after this returns
+      cudaEventDestroy(e);
+    }
   delete st;
 }
 
@@ -122,31 +133,40 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: bad argument");
   if (num_cow) *num_cow = 0;
   if (n == 0) return PKV_OK;
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+       static_cast<uintptr_t>(kv_layer_stride)) & 15u)
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: k_new, v_new and their layer stride must be 16-byte aligned");
   const pkv_pool_desc &P = st->pool;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // Validate before the block manager changes: distinct sequences whose
   // tables stay within max_blocks after this step's token.
   int32_t mb = 1, max_len = 0;
-  {
-    std::unordered_map<int64_t, int> seen;
-    for (int32_t i = 0; i < n; ++i) {
-      if (!seen.emplace(seq_ids[i], 1).second)
-        return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: a sequence appears twice in the batch");
-      int32_t len = 0;
-      pkv_status s = pkv_seq_len(bm, seq_ids[i], &len);
-      if (s != PKV_OK) return s;
-      const int32_t after = len + 1;
-      const int32_t blocks = (after + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
-      if (blocks > st->max_blocks)
-        return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: a table would exceed max_blocks_per_seq");
-      mb = std::max(mb, blocks);
-      max_len = std::max(max_len, after);
-    }
+  st->ids.assign(seq_ids, seq_ids + n);
+  std::sort(st->ids.begin(), st->ids.end());
+  if (std::adjacent_find(st->ids.begin(), st->ids.end()) != st->ids.end())
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: a sequence appears twice in the batch");
+  for (int32_t i = 0; i < n; ++i) {
+    int32_t len = 0;
+    pkv_status s = pkv_seq_len(bm, seq_ids[i], &len);
+    if (s != PKV_OK) return s;
+    const int32_t after = len + 1;
+    const int32_t blocks = (after + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+    if (blocks > st->max_blocks)
+      return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: a table would exceed max_blocks_per_seq");
+    mb = std::max(mb, blocks);
+    max_len = std::max(max_len, after);
   }
-  // Host staging half: wait until the transfer that last read it is done.
+  // Half h was last used two steps ago: its kernels must be done before the
+  // host rewrites the staging, and (on another stream) before this step's
+  // kernels rewrite the device half.
   const int h = st->next;
-  cudaError_t e = cudaEventSynchronize(st->copied[h]);
-  if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventSynchronize");
+  cudaError_t e = cudaSuccess;
+  if (st->recorded[h]) {
+    e = cudaEventQuery(st->used[h]);
+    if (e == cudaErrorNotReady) e = cudaEventSynchronize(st->used[h]);
+    if (e == cudaSuccess && st->used_on[h] != cs) e = cudaStreamWaitEvent(cs, st->used[h], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: waiting for the metadata half");
+  }
   int32_t *H = st->host + h * st->half_ints;
   int32_t *slots = H, *src = H + n, *dst = H + 2 * n, *lens = H + 3 * n, *tables = H + 4 * n;
   int32_t ncow = 0;
@@ -157,15 +177,10 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   if (num_cow) *num_cow = ncow;
   if (cow_src && ncow) std::memcpy(cow_src, src, sizeof(int32_t) * ncow);
   if (cow_dst && ncow) std::memcpy(cow_dst, dst, sizeof(int32_t) * ncow);
-  const size_t ints = static_cast<size_t>(n) * 4 + static_cast<size_t>(n) * mb;
-  int32_t *Dh = st->dev + h * st->half_ints;
-  e = cudaStreamWaitEvent(st->copy, st->used[h], 0);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(Dh, H, ints * sizeof(int32_t), cudaMemcpyHostToDevice, st->copy);
-  if (e == cudaSuccess) e = cudaEventRecord(st->copied[h], st->copy);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, st->copied[h], 0);
-  if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: metadata transfer");
   st->next ^= 1;
-  const int32_t *d_slots = Dh, *d_src = Dh + n, *d_dst = Dh + 2 * n;
+  const int64_t ints = static_cast<int64_t>(n) * 4 + static_cast<int64_t>(n) * mb;
+  const int32_t *Hd = st->host_dev + h * st->half_ints;  // staging as the kernels see it
+  int32_t *Dh = st->dev + h * st->half_ints;
   const int32_t *d_lens = Dh + 3 * n, *d_tables = Dh + 4 * n;
 
   auto layer_ptr = [](const void *base, int64_t stride, int32_t l) {
@@ -175,17 +190,21 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     return base ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(base) + l * P.scale_layer_stride) : nullptr;
   };
   for (int32_t l = 0; l < P.num_layers; ++l) {
+    // layer 0 reads the staging in place; its append copies it to Dh for the rest
+    const int32_t *meta = l == 0 ? Hd : Dh;
     uint8_t *kc = layer_ptr(P.k_cache, P.cache_layer_stride, l);
     uint8_t *vc = layer_ptr(P.v_cache, P.cache_layer_stride, l);
     float *ks = scale_ptr(P.k_scale, l), *vs = scale_ptr(P.v_scale, l);
     if (ncow) {
-      s = paged_kv_copy_blocks(kc, vc, ks, vs, d_src, d_dst, ncow, P.num_kv_heads, P.head_dim, P.cache_dtype,
-                               P.num_blocks, d_error, stream);
+      pkv::CopyArgs c{kc, vc, ks, vs, meta + n, meta + 2 * n, ncow, P.num_kv_heads, P.head_dim, P.cache_dtype,
+                      P.num_blocks, d_error, cs};
+      s = pkv::copy_blocks_unchecked(c);
       if (s != PKV_OK) return s;
     }
-    s = paged_kv_append(layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l), P.q_dtype, n,
-                        P.num_kv_heads, P.head_dim, d_slots, kc, vc, P.cache_dtype, ks, vs, P.num_blocks, d_error,
-                        stream);
+    pkv::AppendArgs a{layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l), P.q_dtype, n,
+                      P.num_kv_heads, P.head_dim, meta, kc, vc, P.cache_dtype, ks, vs, P.num_blocks, d_error, cs,
+                      l == 0 ? Hd : nullptr, l == 0 ? Dh : nullptr, l == 0 ? ints : 0};
+    s = pkv::append_unchecked(a);
     if (s != PKV_OK) return s;
   }
   if (attn_begin) {
@@ -193,13 +212,17 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");
   }
   for (int32_t l = 0; l < P.num_layers; ++l) {
-    // The kernels before each decode on this stream are this step's appends
-    // and decodes, which write neither the tables nor the lengths: the decode
-    // may start early and overlap its prologue with their tail.
-    s = pkv::attention_decode(true, layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l),
-                              P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
+    // A decode reads the lengths and tables before it waits for the kernel
+    // launched just before it, so it may start early (programmatic launch).
+    // With one layer that kernel is the append that copies them to Dh, so
+    // that decode reads them from the staging instead.
+    const bool from_staging = l == 0 && P.num_layers == 1;
+    const int32_t *t_lens = from_staging ? Hd + 3 * n : d_lens;
+    const int32_t *t_tables = from_staging ? Hd + 4 * n : d_tables;
+    s = pkv::attention_decode(true, layer_ptr(out, out_layer_stride, l), out_dtype,
+                              layer_ptr(q, q_layer_stride, l), P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
                               layer_ptr(P.v_cache, P.cache_layer_stride, l), P.cache_dtype, scale_ptr(P.k_scale, l),
-                              scale_ptr(P.v_scale, l), d_tables, mb, d_lens, max_len, n, P.num_q_heads,
+                              scale_ptr(P.v_scale, l), t_tables, mb, t_lens, max_len, n, P.num_q_heads,
                               P.num_kv_heads, P.head_dim, P.num_blocks, scale, st->workspace, st->workspace_bytes,
                               d_error, stream);
     if (s != PKV_OK) return s;
@@ -210,6 +233,8 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   }
   e = cudaEventRecord(st->used[h], cs);
   if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");
+  st->used_on[h] = cs;
+  st->recorded[h] = true;
   return PKV_OK;
 }
 

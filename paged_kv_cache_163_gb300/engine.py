@@ -83,6 +83,9 @@ class PagedKVCache:
         self._stepper = None
         self._stepper_key = None
         self._stepper_bufs = None
+        self._scratch = None
+        self._device_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
+        self._default_scale = float(np.float32(1.0) / np.sqrt(np.float32(head_dim)))
         self.cow_pairs = []          # every (src, dst) copy, in order
 
     def close(self):
@@ -215,10 +218,11 @@ class PagedKVCache:
             marks[1].record(stream)
         return out
 
-    def _stepper_for(self, n: int, num_q_heads: int, q_dtype: str):
+    def _stepper_for(self, n: int, num_q_heads: int, q_torch_dtype):
         """The native step executor for batches of n sequences (created on first use)."""
         import torch
-        key = (n, num_q_heads, q_dtype)
+        key = (n, num_q_heads, q_torch_dtype)
+        q_dtype = {torch.float16: "f16", torch.bfloat16: "bf16"}[q_torch_dtype]
         if self._stepper is not None and self._stepper_key == key:
             return self._stepper
         if self._stepper is not None:
@@ -241,6 +245,7 @@ class PagedKVCache:
         self._stepper = capi.pkv_stepper_create(pool, n, max_blocks, host, dev, ws)
         self._stepper_bufs = (host, dev, ws)
         self._stepper_key = key
+        self._scratch = capi.StepScratch(n)
         return self._stepper
 
     def step(self, seq_ids, k_rows, v_rows, q, scale=None, out=None, stream=None, marks=None):
@@ -251,21 +256,22 @@ class PagedKVCache:
         float32 or q's dtype.  ``marks``: optional pair of CUDA events recorded
         around the attention launches.
         """
-        import torch
-        stream = self._stream(stream)
         if scale is None:
-            scale = float(np.float32(1.0) / np.sqrt(np.float32(self.head_dim)))
+            scale = self._default_scale
         if out is None:
+            import torch
             out = torch.empty_like(q)
-        qname = {torch.float16: "f16", torch.bfloat16: "bf16"}[q.dtype]
-        st = self._stepper_for(len(seq_ids), q.shape[-2], qname)
+        key = (len(seq_ids), q.shape[-2], q.dtype)
+        st = self._stepper if key == self._stepper_key else self._stepper_for(*key)
         if marks is not None:
             for ev in marks:
                 if ev.cuda_event == 0:     # torch creates the event on its first record
-                    ev.record(stream)
+                    ev.record(self._stream(stream))
+        sh = capi.current_stream_handle(self._device_index) if stream is None else stream
         cs, cd = capi.pkv_stepper_step(st, self.bm, seq_ids, k_rows, v_rows, q, out, scale, self.num_layers,
-                                       d_error=self.err, events=marks, stream=stream)
-        self.cow_pairs.extend(zip(cs.tolist(), cd.tolist()))
+                                       d_error=self.err, events=marks, stream=sh, scratch=self._scratch)
+        if len(cs):
+            self.cow_pairs.extend(zip(cs.tolist(), cd.tolist()))
         return out
 
     def check(self, stream=None) -> int:
