@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <mutex>
@@ -60,9 +61,9 @@ pkv_status prepare_counters(void *workspace, int32_t num_seqs, int32_t num_kv_he
   return PKV_OK;
 }
 
-using DecodeFn = cudaError_t (*)(int, int, int, const DecodeParams *, int, int64_t *, int *);
+using DecodeFn = cudaError_t (*)(int, int, int, const DecodeParams *, int, int64_t *, DecodeShape *);
 using MmaFn = cudaError_t (*)(int, int, const DecodeParams *, const CUtensorMap *, const CUtensorMap *, int,
-                              int64_t *, int *);
+                              int64_t *, DecodeShape *);
 
 MmaFn pick_mma(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
   if (cache_dtype == PKV_F16 && q_dtype == PKV_F16) return decode_mma_call_f16;
@@ -137,33 +138,34 @@ int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 struct DecodeLayout {
   int64_t ctr_bytes, ml_bytes, o_bytes, total;
-  int max_ctas;
+  DecodeShape simt, mma;  // residency of the two kernel variants (mma: head_dim 128 only)
+  int sms;
 };
 
-// Shapes and dtypes checked by the caller.  Fills the workspace layout and
-// the largest grid the instance runs with on this device.
+// Shapes and dtypes checked by the caller.  Fills the workspace layout (its
+// partial slots cover every warp either variant can run at once, plus one per
+// item) and the residency of each variant on this device.
 pkv_status decode_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                          int32_t head_dim, pkv_dtype q_dtype, pkv_dtype cache_dtype,
                          DecodeLayout *lay) {
   DecodeFn fn = pick_decode(q_dtype, cache_dtype);
   if (!fn) return fail(PKV_ERR_UNSUPPORTED, "decode: unsupported q / cache dtype pair");
   const int group = num_q_heads / num_kv_heads;
-  int ctas = 0;
-  cudaError_t e = fn(head_dim, group, kDecodePrepare, nullptr, 0, nullptr, &ctas);
+  lay->simt = DecodeShape{0, 0};
+  lay->mma = DecodeShape{0, 0};
+  cudaError_t e = fn(head_dim, group, kDecodePrepare, nullptr, 0, nullptr, &lay->simt);
   if (e == cudaErrorNotSupported)
     return fail(PKV_ERR_UNSUPPORTED, "decode: head_dim must be 64 or 128 and group 1, 2, 4 or 8");
   if (e != cudaSuccess) return cuda_fail(e, "decode: kernel setup");
+  int64_t warps_per_sm = static_cast<int64_t>(lay->simt.ctas_per_sm) * lay->simt.warps_per_cta;
   if (head_dim == 128) {  // the workspace serves either kernel variant
-    int ctas_mma = 0;
-    e = pick_mma(q_dtype, cache_dtype)(group, kDecodePrepare, nullptr, nullptr, nullptr, 0, nullptr, &ctas_mma);
+    e = pick_mma(q_dtype, cache_dtype)(group, kDecodePrepare, nullptr, nullptr, nullptr, 0, nullptr, &lay->mma);
     if (e != cudaSuccess) return cuda_fail(e, "decode: tensor-core kernel setup");
-    if (ctas_mma > ctas) ctas = ctas_mma;
+    warps_per_sm = std::max<int64_t>(warps_per_sm, static_cast<int64_t>(lay->mma.ctas_per_sm) * lay->mma.warps_per_cta);
   }
-  const int sms = sm_count();
-  if (sms <= 0) return fail(PKV_ERR_CUDA, "decode: cannot query the SM count");
-  lay->max_ctas = sms * ctas;
-  const int64_t slots = static_cast<int64_t>(lay->max_ctas) * kDecodeWarps +
-                        static_cast<int64_t>(num_seqs) * num_kv_heads;
+  lay->sms = sm_count();
+  if (lay->sms <= 0) return fail(PKV_ERR_CUDA, "decode: cannot query the SM count");
+  const int64_t slots = lay->sms * warps_per_sm + static_cast<int64_t>(num_seqs) * num_kv_heads;
   lay->ctr_bytes = round256(2 * static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
   lay->ml_bytes = round256(slots * group * 2 * 4);
   lay->o_bytes = round256(slots * group * head_dim * 4);
@@ -340,16 +342,19 @@ pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, c
   if (s != PKV_OK) return s;
 
   // Grid: enough warps that each gets a few tiles of the largest possible
-  // share, capped at one wave of resident CTAs.
+  // share, capped at one wave of resident CTAs of the variant that runs.
+  const bool mma = use_mma(head_dim);
+  const DecodeShape shape = mma ? lay.mma : lay.simt;
   constexpr int64_t kMinTilesPerWarp = 4;
   const int64_t max_tiles = static_cast<int64_t>(num_seqs) * num_kv_heads *
                             ((static_cast<int64_t>(max_context_len) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE);
-  int64_t grid = (max_tiles + kDecodeWarps * kMinTilesPerWarp - 1) / (kDecodeWarps * kMinTilesPerWarp);
+  const int64_t per_cta = shape.warps_per_cta * kMinTilesPerWarp;
+  int64_t grid = (max_tiles + per_cta - 1) / per_cta;
   if (grid < 1) grid = 1;
-  if (grid > lay.max_ctas) grid = lay.max_ctas;
+  if (grid > static_cast<int64_t>(lay.sms) * shape.ctas_per_sm) grid = static_cast<int64_t>(lay.sms) * shape.ctas_per_sm;
 
   cudaError_t e;
-  if (use_mma(head_dim)) {
+  if (mma) {
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
     if (rows >= (int64_t(1) << 31))
       return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: pool larger than 2^31 token rows");

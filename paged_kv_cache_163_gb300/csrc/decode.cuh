@@ -283,12 +283,26 @@ __device__ __noinline__ void merge_item(const DecodeParams &p, int item, int64_t
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[g][e] = 0.f;
   }
+  using Vec = typename std::conditional<DPL == 4, float4, float2>::type;
+  Vec v[kBatch][G];
+  // o rows of partials k0 + j0 .. k0 + j0 + kBatch - 1 (clamped to the chunk's last)
+  auto load_batch = [&](int k0, int j0, int nk) {
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int kk = k0 + min(j0 + b, nk - 1);  // stays inside the item's slots
+      const float *src = po + static_cast<int64_t>(kk) * G * D + lane * DPL;
+#pragma unroll
+      for (int g = 0; g < G; ++g) v[b][g] = __ldcg(reinterpret_cast<const Vec *>(src + g * D));
+    }
+  };
   for (int k0 = 0; k0 < np; k0 += 32) {
     const int k = k0 + lane;
+    const int nk = min(32, np - k0);
     const bool mine = k < np && owns(w_first + k);
     float2 mlk[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) mlk[g] = mine ? __ldcg(ml + static_cast<int64_t>(k) * G + g) : make_float2(-INFINITY, 0.f);
+    load_batch(k0, 0, nk);  // in flight while the weights are formed
     float wk[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -304,17 +318,8 @@ __device__ __noinline__ void merge_item(const DecodeParams &p, int item, int64_t
       wk[g] = mlk[g].x == -INFINITY ? 0.f : exp2f(mlk[g].x - nm);
       den[g] = fmaf(wk[g], mlk[g].y, den[g]);
     }
-    const int nk = min(32, np - k0);
     for (int j0 = 0; j0 < nk; j0 += kBatch) {
-      using Vec = typename std::conditional<DPL == 4, float4, float2>::type;
-      Vec v[kBatch][G];
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int kk = k0 + min(j0 + b, nk - 1);  // stays inside the item's slots
-        const float *src = po + static_cast<int64_t>(kk) * G * D + lane * DPL;
-#pragma unroll
-        for (int g = 0; g < G; ++g) v[b][g] = __ldcg(reinterpret_cast<const Vec *>(src + g * D));
-      }
+      if (j0 > 0) load_batch(k0, j0, nk);
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
 #pragma unroll
@@ -636,7 +641,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
 template <int D, int G, int CDT, int QDT>
 struct DecodeInstance {
   using C = DecodeCfg<D, G, CDT, QDT>;
-  static cudaError_t prepare(int *ctas_per_sm) {
+  static cudaError_t prepare(DecodeShape *shape) {
     static int cached = -1;
     if (cached < 0) {
       cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, G, CDT, QDT>,
@@ -648,7 +653,7 @@ struct DecodeInstance {
       if (e != cudaSuccess) return e;
       cached = n > 0 ? n : 1;
     }
-    *ctas_per_sm = cached;
+    *shape = DecodeShape{cached, C::kWarps};
     return cudaSuccess;
   }
   static cudaError_t launch(const DecodeParams &p, int grid, int64_t *launches) {
@@ -664,28 +669,28 @@ struct DecodeInstance {
 namespace pkv {
 
 template <int D, int G, int CDT, int QDT>
-cudaError_t decode_op(int op, const DecodeParams *p, int grid, int64_t *launches, int *ctas) {
+cudaError_t decode_op(int op, const DecodeParams *p, int grid, int64_t *launches, DecodeShape *shape) {
   using I = DecodeInstance<D, G, CDT, QDT>;
-  if (op == kDecodePrepare) return I::prepare(ctas);
+  if (op == kDecodePrepare) return I::prepare(shape);
   return I::launch(*p, grid, launches);
 }
 
 template <int CDT, int QDT>
 cudaError_t decode_family(int D, int G, int op, const DecodeParams *p, int grid, int64_t *launches,
-                          int *ctas) {
+                          DecodeShape *shape) {
   if (D == 128) {
     switch (G) {
-      case 1: return decode_op<128, 1, CDT, QDT>(op, p, grid, launches, ctas);
-      case 2: return decode_op<128, 2, CDT, QDT>(op, p, grid, launches, ctas);
-      case 4: return decode_op<128, 4, CDT, QDT>(op, p, grid, launches, ctas);
-      case 8: return decode_op<128, 8, CDT, QDT>(op, p, grid, launches, ctas);
+      case 1: return decode_op<128, 1, CDT, QDT>(op, p, grid, launches, shape);
+      case 2: return decode_op<128, 2, CDT, QDT>(op, p, grid, launches, shape);
+      case 4: return decode_op<128, 4, CDT, QDT>(op, p, grid, launches, shape);
+      case 8: return decode_op<128, 8, CDT, QDT>(op, p, grid, launches, shape);
     }
   } else if (D == 64) {
     switch (G) {
-      case 1: return decode_op<64, 1, CDT, QDT>(op, p, grid, launches, ctas);
-      case 2: return decode_op<64, 2, CDT, QDT>(op, p, grid, launches, ctas);
-      case 4: return decode_op<64, 4, CDT, QDT>(op, p, grid, launches, ctas);
-      case 8: return decode_op<64, 8, CDT, QDT>(op, p, grid, launches, ctas);
+      case 1: return decode_op<64, 1, CDT, QDT>(op, p, grid, launches, shape);
+      case 2: return decode_op<64, 2, CDT, QDT>(op, p, grid, launches, shape);
+      case 4: return decode_op<64, 4, CDT, QDT>(op, p, grid, launches, shape);
+      case 8: return decode_op<64, 8, CDT, QDT>(op, p, grid, launches, shape);
     }
   }
   return cudaErrorNotSupported;

@@ -9,7 +9,11 @@
 
 namespace pkv {
 
-constexpr int kDecodeWarps = 8;  // warps per CTA of the decode kernel
+// Residency of one decode kernel instance: CTAs per SM and warps per CTA.
+struct DecodeShape {
+  int ctas_per_sm;
+  int warps_per_cta;
+};
 
 struct DecodeParams {
   uint8_t *out;
@@ -57,28 +61,28 @@ cudaError_t launch_decode(void (*kernel)(KArgs...), int grid, int threads, int s
 
 enum DecodeOp { kDecodePrepare = 0, kDecodeLaunch = 1 };
 
-// op == kDecodePrepare: *ctas_per_sm = resident CTAs per SM of the instance.
+// op == kDecodePrepare: *shape = the instance's resident CTAs per SM and warps per CTA.
 // op == kDecodeLaunch: launch the decode kernel on `grid` CTAs (it merges split items itself).
 // Returns cudaErrorNotSupported when (head_dim, group) has no instance.
 cudaError_t decode_call_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
-                            int64_t *launches, int *ctas_per_sm);
+                            int64_t *launches, DecodeShape *shape);
 cudaError_t decode_call_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
-                             int64_t *launches, int *ctas_per_sm);
+                             int64_t *launches, DecodeShape *shape);
 cudaError_t decode_call_fp8_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
-                                int64_t *launches, int *ctas_per_sm);
+                                int64_t *launches, DecodeShape *shape);
 cudaError_t decode_call_fp8_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
-                                 int64_t *launches, int *ctas_per_sm);
+                                 int64_t *launches, DecodeShape *shape);
 
 // Tensor-core variant (head_dim 128 only); tmk / tmv map the K and V pools as
 // 2D [rows = num_blocks * num_kv_heads * 16][128 elements] with 128-byte swizzle.
 cudaError_t decode_mma_call_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
-                                const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
+                                const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 cudaError_t decode_mma_call_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
-                                 const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
+                                 const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 cudaError_t decode_mma_call_fp8_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
-                                    const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
+                                    const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 cudaError_t decode_mma_call_fp8_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
-                                     const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm);
+                                     const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 
 // paged_attention_decode with a choice of launch: programmatic == true lets
 // the kernel start while the stream's previous kernel finishes.  Only for

@@ -5,13 +5,13 @@
 namespace pkv {
 
 cudaError_t decode_call_fp8_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
-                            int64_t *launches, int *ctas_per_sm) {
-  return decode_family<PKV_FP8_E4M3, PKV_F16>(head_dim, group, op, p, grid, launches, ctas_per_sm);
+                            int64_t *launches, DecodeShape *shape) {
+  return decode_family<PKV_FP8_E4M3, PKV_F16>(head_dim, group, op, p, grid, launches, shape);
 }
 
 cudaError_t decode_mma_call_fp8_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
-                                const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas_per_sm) {
-  return decode_mma_family<PKV_FP8_E4M3, PKV_F16>(group, op, p, tmk, tmv, grid, launches, ctas_per_sm);
+                                const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape) {
+  return decode_mma_family<PKV_FP8_E4M3, PKV_F16>(group, op, p, tmk, tmv, grid, launches, shape);
 }
 
 }  // namespace pkv

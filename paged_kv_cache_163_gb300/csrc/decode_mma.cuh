@@ -75,9 +75,13 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 template <int G, int CDT, int QDT>
 struct MmaCfg {
   static constexpr int kD = 128;
-  static constexpr int kWarps = 8;
-  static constexpr int kThreads = kWarps * 32;
   static constexpr bool kFp8 = CDT == PKV_FP8_E4M3;
+  // FP8 tiles are half the bytes, so an SM holds twice the warps (with at
+  // most 128 registers a thread).  They form one 16-warp CTA: two 8-warp CTAs
+  // on an SM were measured to run unevenly (the CTA launched first streamed
+  // ~13% faster), leaving the SM half idle at the end of a call.
+  static constexpr int kWarps = kFp8 ? 16 : 8;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr bool kBf16 = !kFp8 && CDT == PKV_BF16;  // MMA operand type: bf16, else f16
   static constexpr int kEsz = kFp8 ? 1 : 2;
   static constexpr int kTile = kBS * kD * kEsz;  // K or V tile bytes (1024-aligned in shared memory)
@@ -88,9 +92,7 @@ struct MmaCfg {
   // Two stages per warp: measured faster than deeper rings on GB300 (more
   // copies in flight than HBM needs only lengthen the queues).
   static constexpr int kStages = 2;
-  // FP8 tiles are half the bytes: two CTAs (16 warps) per SM, at most 128
-  // registers a thread, measured faster than one; 16-bit tiles keep one.
-  static constexpr int kMinBlocks = kFp8 ? 2 : 1;
+  static constexpr int kMinBlocks = 1;
   static constexpr int kCumBytes = round_up_c((PKV_MAX_SEQS_PER_CALL + 1) * 4, 128);
   static constexpr int kMiscBytes = 128;
   static constexpr int kBarBytes = round_up_c(kWarps * kStages * 8, 128);
@@ -99,7 +101,7 @@ struct MmaCfg {
   static constexpr int kTilesOff = round_up_c(kHead, 1024);
   static constexpr int kSmem = 1024 + kTilesOff + kWarps * kStages * (kKV + kAux);
   static_assert(G >= 1 && G <= 8, "group size");
-  static_assert(kSmem * kMinBlocks <= 232448, "shared memory budget");
+  static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 // head_dim index of output row m (0..15) of m-tile i for lane group g (see kernel comment).
@@ -245,8 +247,8 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
         }
       }
     }
-    // the FP8 instances run two CTAs an SM (128 registers a thread): fewer loads in flight
-    if (!whole) finish_partial<D, G, QDT, C::kFp8 ? 8 : 16>(p, cum, item, total, nwarps);
+    // merge batches sized to the register budget (FP8 instances: 128 a thread)
+    if (!whole) finish_partial<D, G, QDT, C::kFp8 ? 8 : 32>(p, cum, item, total, nwarps);
   };
 
   // tokens whose V rows this lane reads (B-fragment k rows of P^T)
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
 template <int G, int CDT, int QDT>
 struct MmaInstance {
   using C = MmaCfg<G, CDT, QDT>;
-  static cudaError_t prepare(int *ctas_per_sm) {
+  static cudaError_t prepare(DecodeShape *shape) {
     static int cached = -1;
     if (cached < 0) {
       cudaError_t e = cudaFuncSetAttribute(paged_decode_mma_kernel<G, CDT, QDT>,
@@ -461,7 +463,7 @@ struct MmaInstance {
       if (e != cudaSuccess) return e;
       cached = n > 0 ? n : 1;
     }
-    *ctas_per_sm = cached;
+    *shape = DecodeShape{cached, C::kWarps};
     return cudaSuccess;
   }
   static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
@@ -475,11 +477,11 @@ struct MmaInstance {
 
 template <int CDT, int QDT>
 cudaError_t decode_mma_family(int G, int op, const DecodeParams *p, const CUtensorMap *tmk,
-                              const CUtensorMap *tmv, int grid, int64_t *launches, int *ctas) {
+                              const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape) {
   switch (G) {
 #define PKV_MMA_CASE(GG)                                                   \
   case GG:                                                                 \
-    if (op == kDecodePrepare) return MmaInstance<GG, CDT, QDT>::prepare(ctas); \
+    if (op == kDecodePrepare) return MmaInstance<GG, CDT, QDT>::prepare(shape); \
     return MmaInstance<GG, CDT, QDT>::launch(*p, *tmk, *tmv, grid, launches);
     PKV_MMA_CASE(1)
     PKV_MMA_CASE(2)
