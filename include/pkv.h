@@ -27,7 +27,8 @@
  *  - Device arrays are dense and row-major in the shapes stated, and every
  *    device pointer must be 16-byte aligned.
  *  - Cache layout, per layer: k_cache, v_cache [num_blocks][num_kv_heads][16][head_dim];
- *    FP8 scales k_scale, v_scale float32 [num_blocks][num_kv_heads][16].
+ *    one-byte caches (FP8_E4M3, FP8_E5M2, INT8) also have scales k_scale,
+ *    v_scale float32 [num_blocks][num_kv_heads][16].
  *    Token n of a sequence lives at slot table[n / 16] * 16 + n % 16.
  *  - Several layers are several calls with per-layer cache pointers.
  *  - Not thread-safe per block manager handle.
@@ -55,7 +56,19 @@ typedef enum {
   PKV_ERR_WORKSPACE = -6     /* workspace smaller than paged_attention_workspace_bytes */
 } pkv_status;
 
-typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2, PKV_F32 = 3 } pkv_dtype;
+/* Element types.  F16 / BF16: queries, new K/V rows, 16-bit caches.  F32:
+ * decode output only.  FP8_E4M3, FP8_E5M2, INT8: one-byte cache codes with
+ * one fp32 scale per (token, KV head) ("KV Cache优化实战" §3.2-§3.3 names
+ * fp8_e4m3, fp8_e5m2 and 8-bit integer caches, and prefers per-token /
+ * per-head scales to one scale per tensor). */
+typedef enum {
+  PKV_F16 = 0,
+  PKV_BF16 = 1,
+  PKV_FP8_E4M3 = 2,
+  PKV_F32 = 3,
+  PKV_FP8_E5M2 = 4,
+  PKV_INT8 = 5
+} pkv_dtype;
 
 /* Bits a kernel ORs into *d_error. */
 #define PKV_DEVERR_BAD_SLOT 1        /* append: slot >= num_blocks * 16 */
@@ -127,8 +140,8 @@ pkv_status pkv_seq_len(const pkv_bm *bm, int64_t seq_id, int32_t *len);
 
 /* ------------------------------------------------------------------------ */
 /* Sizing ("KV Cache优化实战" §2.1: bytes = 2 x layers x kv_heads x head_dim */
-/* x tokens x bytes per element).  FP8 adds one fp32 scale per (token, KV   */
-/* head) for K and for V.  Returns -1 on a bad argument.                     */
+/* x tokens x bytes per element).  One-byte caches add one fp32 scale per   */
+/* (token, KV head) for K and for V.  Returns -1 on a bad argument.          */
 /* ------------------------------------------------------------------------ */
 int64_t pkv_kv_bytes(int32_t layers, int32_t kv_heads, int32_t head_dim, int64_t tokens,
                      pkv_dtype cache_dtype);
@@ -142,7 +155,7 @@ int64_t pkv_pool_blocks(int64_t budget_bytes, int32_t layers, int32_t kv_heads, 
 
 /* Copy-on-write block copy ("KV Cache 与 vLLM" §3.3): for each pair i, copy
  * all 16 slots of physical block src[i] to dst[i] in k_cache and v_cache
- * (and k_scale / v_scale when cache_dtype is FP8; NULL otherwise).
+ * (and k_scale / v_scale for one-byte caches; NULL otherwise).
  * src, dst: device int32 [num_pairs]; ids outside [0, num_blocks) set
  * PKV_DEVERR_BAD_BLOCK and that pair is skipped. */
 pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
@@ -156,11 +169,15 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
  * [num_tokens]; -1 skips the token; >= num_blocks * 16 sets
  * PKV_DEVERR_BAD_SLOT and skips it).
  * 16-bit caches: cache_dtype must equal in_dtype; the copy is exact.
- * FP8 E4M3 cache ("KV Cache优化实战" §3.2-§3.3, per-token per-head scale):
- * per (token, KV head) amax = max |x| over head_dim, scale = amax / 448 in
- * IEEE fp32 (1 when amax == 0), code = E4M3(x / scale) with an IEEE fp32
- * division, round to nearest even, saturating to +-448; scale goes to
- * k_scale / v_scale at the same slot. */
+ * One-byte caches ("KV Cache优化实战" §3.2-§3.3, per-token per-head scale):
+ * per (token, KV head) amax = max |x| over head_dim, scale = amax / R in
+ * IEEE fp32 (1 when amax == 0) and code = Q(x / scale) with an IEEE fp32
+ * division, where
+ *   FP8_E4M3: R = 448,   Q = nearest E4M3 code, ties to even, saturating;
+ *   FP8_E5M2: R = 57344, Q = nearest E5M2 code, ties to even, saturating;
+ *   INT8:     R = 127,   Q = nearest integer, ties to even, clamped to
+ *             [-127, 127] (two's complement byte);
+ * the scale goes to k_scale / v_scale at the same slot. */
 pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int32_t num_tokens,
                            int32_t num_kv_heads, int32_t head_dim, const int32_t *slot_mapping,
                            void *k_cache, void *v_cache, pkv_dtype cache_dtype, float *k_scale,
@@ -196,7 +213,8 @@ pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads
  * q: [num_seqs][num_q_heads][head_dim] in q_dtype (F16 / BF16); out: same
  * shape in out_dtype, either F32 (the fp32 accumulator result) or q_dtype
  * (that result rounded once to nearest even).  Caches F16 or BF16 (q_dtype must match) or
- * FP8_E4M3 (dequantised in the kernel with k_scale / v_scale).
+ * one byte (FP8_E4M3, FP8_E5M2, INT8: code value x scale, dequantised in the
+ * kernel with k_scale / v_scale).
  * block_tables: device int32 [num_seqs][max_blocks_per_seq]; context_lens:
  * device int32 [num_seqs]; max_context_len bounds every context_len.
  * A context_len of 0 gives a zero output.  Work is split across the GPU
@@ -260,7 +278,7 @@ typedef struct {
   pkv_dtype q_dtype, cache_dtype;
   void *k_cache, *v_cache;          /* layer 0; layer l at + l * cache_layer_stride bytes */
   int64_t cache_layer_stride;
-  float *k_scale, *v_scale;         /* FP8 only (else NULL); layer l at + l * scale_layer_stride bytes */
+  float *k_scale, *v_scale;         /* one-byte caches only (else NULL); layer l at + l * scale_layer_stride bytes */
   int64_t scale_layer_stride;
 } pkv_pool_desc;
 

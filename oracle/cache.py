@@ -12,37 +12,56 @@ Storage types:
 
 * ``f16`` / ``bf16``: the value is stored as is (the inputs are already in
   that type, so the write is an exact copy);
-* ``fp8_e4m3``: per (token, KV head) -- the finer granularity the pages
+* one-byte codes, per (token, KV head) -- the finer granularity the pages
   recommend over one scale per tensor ("KV Cache优化实战" §3.2, §7.3) --
-  ``amax = max |x|`` over head_dim, ``s = amax / 448`` (``1`` when
-  ``amax == 0``), code = E4M3(x / s).  ``s`` and ``x / s`` are IEEE fp32
+  ``amax = max |x|`` over head_dim, ``s = amax / R`` (``1`` when
+  ``amax == 0``), code = Q(x / s); ``s`` and ``x / s`` are IEEE fp32
   round-to-nearest divisions (reading: the pages give no formula; this is
-  the plain absmax one, fixed so that codes compare bit for bit).  The
-  dequantised value is ``decode(code) * s`` in fp64.
+  the plain absmax one, fixed so that codes compare bit for bit):
 
-Slots never written hold NaN in this model (fp32 storage) or a NaN code
-(FP8), so that a gather that strays onto one shows up at once.
+  - ``fp8_e4m3``: R = 448, Q = nearest E4M3 code (``fp8.encode``);
+  - ``fp8_e5m2``: R = 57344, Q = nearest E5M2 code (``fp8.e5m2_encode``);
+  - ``int8``: R = 127, Q = nearest integer in [-127, 127] (``int8.encode``).
+
+  The dequantised value is ``value(code) * s`` in fp64.
+
+Slots never written hold NaN in this model (fp32 storage, and an fp32 NaN
+scale for one-byte codes), so that a gather that strays onto one shows up
+at once.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import fp8
+from . import fp8, int8
 
-DTYPES = ("f16", "bf16", "fp8_e4m3")
+DTYPES = ("f16", "bf16", "fp8_e4m3", "fp8_e5m2", "int8")
+# one-byte cache types: (R, encode float32 quotients -> codes, decode codes -> fp64)
+CODE_TYPES = {
+    "fp8_e4m3": (fp8.MAX_FINITE, fp8.encode, fp8.decode),
+    "fp8_e5m2": (fp8.E5M2_MAX_FINITE, fp8.e5m2_encode, fp8.e5m2_decode),
+    "int8": (int8.MAX_CODE, lambda y: int8.encode(y).view(np.uint8), int8.decode),
+}
 
 
-def quantize_rows(x: np.ndarray):
-    """Per-row FP8 quantisation of float32 rows ``[..., head_dim]``.
+def quantize_rows(x: np.ndarray, dtype: str = "fp8_e4m3"):
+    """Per-row quantisation of float32 rows ``[..., head_dim]`` to one-byte codes.
 
-    Returns (codes uint8 [..., head_dim], scale float32 [...]).
+    Returns (codes uint8 [..., head_dim] -- an int8 code as its byte --,
+    scale float32 [...]).
     """
+    r, enc, _ = CODE_TYPES[dtype]
     x = np.asarray(x, dtype=np.float32)
     amax = np.max(np.abs(x), axis=-1)
     scale = np.where(amax == 0, np.float32(1.0),
-                     amax.astype(np.float32) / np.float32(fp8.MAX_FINITE)).astype(np.float32)
+                     amax.astype(np.float32) / np.float32(r)).astype(np.float32)
     y = (x / scale[..., None]).astype(np.float32)
-    return fp8.encode(y), scale
+    return enc(y), scale
+
+
+def code_values(codes: np.ndarray, dtype: str) -> np.ndarray:
+    """fp64 values of one-byte codes (before the scale)."""
+    return CODE_TYPES[dtype][2](codes)
 
 
 class PagedCacheModel:
@@ -55,7 +74,7 @@ class PagedCacheModel:
         self.num_blocks, self.num_kv_heads, self.head_dim = num_blocks, num_kv_heads, head_dim
         self.block_size, self.dtype = block_size, dtype
         shape = (num_blocks, num_kv_heads, block_size, head_dim)
-        if dtype == "fp8_e4m3":
+        if dtype in CODE_TYPES:
             self.k = np.full(shape, 0x7F, dtype=np.uint8)
             self.v = np.full(shape, 0x7F, dtype=np.uint8)
             self.k_scale = np.full(shape[:3], np.nan, dtype=np.float32)
@@ -80,9 +99,9 @@ class PagedCacheModel:
             blk, off = divmod(slot, bs)
             if blk >= self.num_blocks:
                 raise IndexError(f"slot {slot} outside the pool")
-            if self.dtype == "fp8_e4m3":
-                kc, ks = quantize_rows(k[t])
-                vc, vs = quantize_rows(v[t])
+            if self.dtype in CODE_TYPES:
+                kc, ks = quantize_rows(k[t], self.dtype)
+                vc, vs = quantize_rows(v[t], self.dtype)
                 self.k[blk, :, off, :] = kc
                 self.v[blk, :, off, :] = vc
                 self.k_scale[blk, :, off] = ks
@@ -102,8 +121,8 @@ class PagedCacheModel:
         self.filled[dst] = self.filled[src]
 
     def _dequant(self, codes_or_vals, scales):
-        if self.dtype == "fp8_e4m3":
-            return fp8.decode(codes_or_vals) * scales.astype(np.float64)[..., None]
+        if self.dtype in CODE_TYPES:
+            return code_values(codes_or_vals, self.dtype) * scales.astype(np.float64)[..., None]
         return codes_or_vals.astype(np.float64)
 
     def gather(self, table, length: int):
@@ -117,7 +136,7 @@ class PagedCacheModel:
         offs = pos % bs
         k = self.k[blocks, :, offs, :]          # [L, Hkv, D]
         v = self.v[blocks, :, offs, :]
-        if self.dtype == "fp8_e4m3":
+        if self.dtype in CODE_TYPES:
             ks = self.k_scale[blocks, :, offs]
             vs = self.v_scale[blocks, :, offs]
             return self._dequant(k, ks), self._dequant(v, vs)
@@ -131,7 +150,7 @@ def dequantize_rows(x: np.ndarray, dtype: str):
     as, without the paging.
     """
     x = np.asarray(x, dtype=np.float32)
-    if dtype == "fp8_e4m3":
-        codes, s = quantize_rows(x)
-        return fp8.decode(codes) * s.astype(np.float64)[..., None]
+    if dtype in CODE_TYPES:
+        codes, s = quantize_rows(x, dtype)
+        return code_values(codes, dtype) * s.astype(np.float64)[..., None]
     return x.astype(np.float64)

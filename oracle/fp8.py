@@ -70,3 +70,63 @@ def encode(y: np.ndarray) -> np.ndarray:
     mag = np.where(exact | pick_hi, _POS_CODES[hi], _POS_CODES[lo])
     sign = np.signbit(y).astype(np.int64) << 7
     return (mag | sign).astype(np.uint8)
+
+
+# ---------------------------------------------------------------------------
+# OCP FP8 E5M2, the other FP8 cache type the pages name
+# (``--kv-cache-dtype fp8_e5m2``, "KV Cache优化实战" §3.3):
+#
+# * bit 7: sign; bits 6..2: exponent with bias 15; bits 1..0: mantissa;
+# * exponent field 0 encodes subnormals m/4 * 2^-14 (smallest 2^-16);
+# * exponent field 31 is infinity (mantissa 0) or NaN, as in IEEE binary16,
+#   so the largest finite magnitude is 1.75 * 2^15 = 57344.
+#
+# Encoding mirrors E4M3: nearest finite code, ties to the even code,
+# saturating to +-57344, keeping the sign of zero.
+# ---------------------------------------------------------------------------
+E5M2_MAX_FINITE = 57344.0
+
+
+def e5m2_decode_value(code: int) -> float:
+    """Value of one E5M2 code as a Python float (inf / NaN for the special codes)."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    exp = (code >> 2) & 0x1F
+    man = code & 0x3
+    if exp == 0x1F:
+        return sign * float("inf") if man == 0 else float("nan")
+    if exp == 0:
+        return sign * (man / 4.0) * 2.0 ** (1 - 15)
+    return sign * (1.0 + man / 4.0) * 2.0 ** (exp - 15)
+
+
+def e5m2_decode_table() -> np.ndarray:
+    return np.array([e5m2_decode_value(c) for c in range(256)], dtype=np.float64)
+
+
+_E5M2_TABLE = e5m2_decode_table()
+# Non-negative finite codes 0x00..0x7B in increasing order of value.
+_E5M2_POS_CODES = np.arange(0x7C, dtype=np.int64)
+_E5M2_POS_VALUES = _E5M2_TABLE[:0x7C]
+
+
+def e5m2_decode(codes: np.ndarray) -> np.ndarray:
+    return _E5M2_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def e5m2_encode(y: np.ndarray) -> np.ndarray:
+    """Encode float32 values: nearest finite code, ties to the even code, saturate at 57344."""
+    y = np.asarray(y, dtype=np.float32)
+    if np.isnan(y).any():
+        raise ValueError("NaN has no place in the FP8 cache")
+    a = np.minimum(np.abs(y.astype(np.float64)), E5M2_MAX_FINITE)
+    hi = np.searchsorted(_E5M2_POS_VALUES, a, side="left")
+    hi = np.clip(hi, 0, 0x7B)
+    lo = np.clip(hi - 1, 0, 0x7B)
+    d_lo = a - _E5M2_POS_VALUES[lo]
+    d_hi = _E5M2_POS_VALUES[hi] - a
+    exact = d_hi == 0.0
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (_E5M2_POS_CODES[hi] % 2 == 0))
+    mag = np.where(exact | pick_hi, _E5M2_POS_CODES[hi], _E5M2_POS_CODES[lo])
+    sign = np.signbit(y).astype(np.int64) << 7
+    return (mag | sign).astype(np.uint8)

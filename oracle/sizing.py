@@ -19,7 +19,9 @@ preallocation holds max_len slots per request (§2.2).
 """
 from __future__ import annotations
 
-BYTES_PER_ELEMENT = {"f16": 2, "bf16": 2, "fp8_e4m3": 1, "int8": 1, "int4": 0.5}
+BYTES_PER_ELEMENT = {"f16": 2, "bf16": 2, "fp8_e4m3": 1, "fp8_e5m2": 1, "int8": 1, "int4": 0.5}
+# cache types stored as one-byte codes plus one fp32 scale per (token, KV head)
+SCALED_ONE_BYTE = ("fp8_e4m3", "fp8_e5m2", "int8")
 
 
 def kv_bytes(layers, kv_heads, head_dim, seq_len, batch, bytes_per_element):
@@ -68,8 +70,8 @@ def max_concurrency(budget_bytes, per_request_bytes):
 
 
 def pool_blocks(budget_bytes, layers, kv_heads, head_dim, dtype, block_size=16):
-    """Whole blocks a byte budget buys for every layer's K and V (plus FP8 scales)."""
-    if dtype == "fp8_e4m3":
+    """Whole blocks a byte budget buys for every layer's K and V (plus one-byte caches' scales)."""
+    if dtype in SCALED_ONE_BYTE:
         per_block = 2 * layers * kv_heads * block_size * (head_dim + 4)
     else:
         per_block = 2 * layers * kv_heads * block_size * head_dim * BYTES_PER_ELEMENT[dtype]
