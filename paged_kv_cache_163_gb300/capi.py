@@ -16,8 +16,11 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
-PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32 = 0, 1, 2, 3
-DTYPE_NAMES = {"f16": PKV_F16, "bf16": PKV_BF16, "fp8_e4m3": PKV_FP8_E4M3, "f32": PKV_F32}
+PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32, PKV_FP8_E5M2, PKV_INT8 = 0, 1, 2, 3, 4, 5
+DTYPE_NAMES = {"f16": PKV_F16, "bf16": PKV_BF16, "fp8_e4m3": PKV_FP8_E4M3, "f32": PKV_F32,
+               "fp8_e5m2": PKV_FP8_E5M2, "int8": PKV_INT8}
+# cache types stored as one-byte codes (uint8 tensors) plus fp32 scales
+ONE_BYTE_CACHES = ("fp8_e4m3", "fp8_e5m2", "int8")
 BLOCK_SIZE = 16
 MAX_SEQS_PER_CALL = 1024
 DEVERR_BAD_SLOT, DEVERR_BAD_BLOCK, DEVERR_BAD_CONTEXT_LEN, DEVERR_WAIT_TIMEOUT = 1, 2, 4, 8
@@ -251,10 +254,18 @@ def _dt(x) -> int:
     if isinstance(x, str):
         return DTYPE_NAMES[x]
     import torch
-    m = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.uint8: PKV_FP8_E4M3, torch.float32: PKV_F32}
+    m = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.uint8: PKV_FP8_E4M3, torch.float32: PKV_F32,
+         torch.int8: PKV_INT8}
     if hasattr(torch, "float8_e4m3fn"):
         m[torch.float8_e4m3fn] = PKV_FP8_E4M3
+    if hasattr(torch, "float8_e5m2"):
+        m[torch.float8_e5m2] = PKV_FP8_E5M2
     return m[x]
+
+
+def _cdt(k_cache, cache_dtype) -> int:
+    """Cache pkv_dtype: given by name, else read off the tensor (uint8 reads as FP8 E4M3)."""
+    return _dt(cache_dtype) if cache_dtype is not None else _dt(k_cache.dtype)
 
 
 def _dp(t):
@@ -276,20 +287,20 @@ def _stream(stream):
 
 
 def paged_kv_copy_blocks(k_cache, v_cache, k_scale, v_scale, src, dst, num_pairs=None,
-                         d_error=None, stream=None) -> None:
+                         d_error=None, stream=None, cache_dtype=None) -> None:
     nb, hkv, bs, d = k_cache.shape
     n = src.numel() if num_pairs is None else num_pairs
     _check(load().paged_kv_copy_blocks(_dp(k_cache), _dp(v_cache), _dp(k_scale), _dp(v_scale), _dp(src),
-                                       _dp(dst), n, hkv, d, _dt(k_cache.dtype), nb, _dp(d_error),
+                                       _dp(dst), n, hkv, d, _cdt(k_cache, cache_dtype), nb, _dp(d_error),
                                        _stream(stream)), "paged_kv_copy_blocks")
 
 
 def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None,
-                    d_error=None, stream=None) -> None:
+                    d_error=None, stream=None, cache_dtype=None) -> None:
     t, hkv, d = k.shape
     nb = k_cache.shape[0]
     _check(load().paged_kv_append(_dp(k), _dp(v), _dt(k.dtype), t, hkv, d, _dp(slot_mapping), _dp(k_cache),
-                                  _dp(v_cache), _dt(k_cache.dtype), _dp(k_scale), _dp(v_scale), nb,
+                                  _dp(v_cache), _cdt(k_cache, cache_dtype), _dp(k_scale), _dp(v_scale), nb,
                                   _dp(d_error), _stream(stream)), "paged_kv_append")
 
 
@@ -304,27 +315,29 @@ def paged_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_di
 
 def paged_attention_decode(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                            max_context_len, scale, workspace, d_error=None, stream=None,
-                           num_seqs=None) -> None:
+                           num_seqs=None, cache_dtype=None) -> None:
     b, hq, d = q.shape
     if num_seqs is not None:
         b = num_seqs
     nb, hkv = k_cache.shape[0], k_cache.shape[1]
     _check(load().paged_attention_decode(
-        _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_cache), _dp(v_cache), _dt(k_cache.dtype), _dp(k_scale),
+        _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_cache), _dp(v_cache), _cdt(k_cache, cache_dtype),
+        _dp(k_scale),
         _dp(v_scale), _dp(block_tables), block_tables.shape[-1], _dp(context_lens), int(max_context_len), b, hq,
         hkv, d, nb, float(scale), _dp(workspace), workspace.numel() * workspace.element_size(),
         _dp(d_error), _stream(stream)), "paged_attention_decode")
 
 
 def paged_attention_decode_static(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                                  max_context_len, scale, d_error=None, stream=None, num_seqs=None) -> None:
+                                  max_context_len, scale, d_error=None, stream=None, num_seqs=None,
+                                  cache_dtype=None) -> None:
     """paged_attention_decode with the library's static scratch (no workspace, no allocation)."""
     b, hq, d = q.shape
     if num_seqs is not None:
         b = num_seqs
     nb, hkv = k_cache.shape[0], k_cache.shape[1]
     _check(load().paged_attention_decode_static(
-        _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_cache), _dp(v_cache), _dt(k_cache.dtype),
+        _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_cache), _dp(v_cache), _cdt(k_cache, cache_dtype),
         _dp(k_scale), _dp(v_scale), _dp(block_tables), block_tables.shape[-1], _dp(context_lens),
         int(max_context_len), b, hq, hkv, d, nb, float(scale), _dp(d_error), _stream(stream)),
         "paged_attention_decode_static")

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
   const int64_t row = (blk * num_kv_heads + h) * kBS + off;  // index of the cache row
   const uint8_t *src = (kind ? v : k) + th * D * 2 + lane * EPL * 2;
 
-  if constexpr (CDT != PKV_FP8_E4M3) {
+  if constexpr (!is_code8(CDT)) {
     uint8_t *dst = (kind ? v_cache : k_cache) + row * D * 2 + lane * EPL * 2;
     if constexpr (EPL * 2 == 8) {
       *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(src);
@@ -71,12 +71,11 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
     for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, code8_range<CDT>());
     uint32_t packed = 0;
 #pragma unroll
     for (int e = 0; e < EPL; e += 2) {
-      float2 y = make_float2(__fdiv_rn(x[e], s), __fdiv_rn(x[e + 1], s));
-      uint32_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);  // y.x -> low byte
+      const uint32_t c2 = encode2<CDT>(__fdiv_rn(x[e], s), __fdiv_rn(x[e + 1], s));  // x[e] -> low byte
       packed |= c2 << (8 * e);
     }
     uint8_t *dst = (kind ? v_cache : k_cache) + row * D + lane * EPL;
@@ -132,14 +131,20 @@ static cudaError_t launch_append(const AppendArgs &a) {
   return cudaGetLastError();
 }
 
+template <int D, int CDT>
+static cudaError_t dispatch_code8(const AppendArgs &a) {
+  return a.in_dtype == PKV_BF16 ? launch_append<D, PKV_BF16, CDT>(a) : launch_append<D, PKV_F16, CDT>(a);
+}
+
 template <int D>
 static cudaError_t dispatch_append_d(const AppendArgs &a) {
-  if (a.cache_dtype == PKV_FP8_E4M3) {
-    return a.in_dtype == PKV_BF16 ? launch_append<D, PKV_BF16, PKV_FP8_E4M3>(a)
-                                  : launch_append<D, PKV_F16, PKV_FP8_E4M3>(a);
+  switch (a.cache_dtype) {
+    case PKV_FP8_E4M3: return dispatch_code8<D, PKV_FP8_E4M3>(a);
+    case PKV_FP8_E5M2: return dispatch_code8<D, PKV_FP8_E5M2>(a);
+    case PKV_INT8: return dispatch_code8<D, PKV_INT8>(a);
+    case PKV_BF16: return launch_append<D, PKV_BF16, PKV_BF16>(a);
+    default: return launch_append<D, PKV_F16, PKV_F16>(a);
   }
-  return a.cache_dtype == PKV_BF16 ? launch_append<D, PKV_BF16, PKV_BF16>(a)
-                                   : launch_append<D, PKV_F16, PKV_F16>(a);
 }
 
 cudaError_t run_append(const AppendArgs &a) {
@@ -149,14 +154,14 @@ cudaError_t run_append(const AppendArgs &a) {
 
 cudaError_t run_copy_blocks(const CopyArgs &a) {
   if (a.num_pairs == 0) return cudaSuccess;
-  const int esz = a.cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
+  const bool code8 = is_code8(a.cache_dtype);
+  const int esz = code8 ? 1 : 2;
   const int64_t block_bytes = static_cast<int64_t>(a.num_kv_heads) * kBS * a.head_dim * esz;
   const int32_t scale_elems = a.num_kv_heads * kBS;
   dim3 grid(a.num_pairs, 2);
   copy_blocks_kernel<<<grid, 256, 0, a.stream>>>(
       static_cast<uint8_t *>(a.k_cache), static_cast<uint8_t *>(a.v_cache),
-      a.cache_dtype == PKV_FP8_E4M3 ? a.k_scale : nullptr,
-      a.cache_dtype == PKV_FP8_E4M3 ? a.v_scale : nullptr, a.src, a.dst, block_bytes, scale_elems,
+      code8 ? a.k_scale : nullptr, code8 ? a.v_scale : nullptr, a.src, a.dst, block_bytes, scale_elems,
       a.num_blocks, a.d_error);
   return cudaGetLastError();
 }

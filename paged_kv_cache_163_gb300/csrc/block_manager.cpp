@@ -232,6 +232,8 @@ static int64_t elem_bytes_per_token_head(int32_t head_dim, pkv_dtype dt) {
     case PKV_BF16:
       return 2 * static_cast<int64_t>(head_dim);
     case PKV_FP8_E4M3:
+    case PKV_FP8_E5M2:
+    case PKV_INT8:
       return static_cast<int64_t>(head_dim) + 4;  // codes + one fp32 scale
     default:
       return -1;  // not a cache type

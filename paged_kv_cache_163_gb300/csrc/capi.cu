@@ -14,6 +14,7 @@
 
 #include "append.h"
 #include "decode.h"
+#include "dtypes.h"
 #include "pkv.h"
 #include "status.h"
 
@@ -70,6 +71,10 @@ MmaFn pick_mma(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
   if (cache_dtype == PKV_BF16 && q_dtype == PKV_BF16) return decode_mma_call_bf16;
   if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_F16) return decode_mma_call_fp8_f16;
   if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_BF16) return decode_mma_call_fp8_bf16;
+  if (cache_dtype == PKV_FP8_E5M2 && q_dtype == PKV_F16) return decode_mma_call_e5m2_f16;
+  if (cache_dtype == PKV_FP8_E5M2 && q_dtype == PKV_BF16) return decode_mma_call_e5m2_bf16;
+  if (cache_dtype == PKV_INT8 && q_dtype == PKV_F16) return decode_mma_call_int8_f16;
+  if (cache_dtype == PKV_INT8 && q_dtype == PKV_BF16) return decode_mma_call_int8_bf16;
   return nullptr;
 }
 
@@ -131,6 +136,10 @@ DecodeFn pick_decode(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
   if (cache_dtype == PKV_BF16 && q_dtype == PKV_BF16) return decode_call_bf16;
   if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_F16) return decode_call_fp8_f16;
   if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_BF16) return decode_call_fp8_bf16;
+  if (cache_dtype == PKV_FP8_E5M2 && q_dtype == PKV_F16) return decode_call_e5m2_f16;
+  if (cache_dtype == PKV_FP8_E5M2 && q_dtype == PKV_BF16) return decode_call_e5m2_bf16;
+  if (cache_dtype == PKV_INT8 && q_dtype == PKV_F16) return decode_call_int8_f16;
+  if (cache_dtype == PKV_INT8 && q_dtype == PKV_BF16) return decode_call_int8_bf16;
   return nullptr;
 }
 
@@ -206,14 +215,14 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
     return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: bad sizes");
   if (head_dim != 64 && head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "paged_kv_copy_blocks: head_dim must be 64 or 128");
-  if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3)
+  if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16 && !is_code8(cache_dtype))
     return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: bad cache dtype");
   if (num_pairs == 0) return PKV_OK;
   if (num_pairs > 65535) return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: at most 65535 pairs per call");
   if (!k_cache || !v_cache || !src || !dst || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: NULL or misaligned pointer");
-  if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale))
-    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: FP8 cache needs k_scale and v_scale");
+  if (is_code8(cache_dtype) && (!k_scale || !v_scale))
+    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: a one-byte cache needs k_scale and v_scale");
   CopyArgs a{k_cache, v_cache, k_scale, v_scale, src, dst, num_pairs, num_kv_heads,
              head_dim, cache_dtype, num_blocks, d_error, reinterpret_cast<cudaStream_t>(stream)};
   cudaError_t e = run_copy_blocks(a);
@@ -233,14 +242,14 @@ pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int
     return fail(PKV_ERR_UNSUPPORTED, "paged_kv_append: head_dim must be 64 or 128");
   if (in_dtype != PKV_F16 && in_dtype != PKV_BF16)
     return fail(PKV_ERR_INVALID, "paged_kv_append: input rows must be F16 or BF16");
-  if (cache_dtype != PKV_FP8_E4M3 && cache_dtype != in_dtype)
+  if (!is_code8(cache_dtype) && cache_dtype != in_dtype)
     return fail(PKV_ERR_UNSUPPORTED, "paged_kv_append: a 16-bit cache must match the input dtype");
   if (num_tokens == 0) return PKV_OK;
   if (!k || !v || !slot_mapping || !k_cache || !v_cache || !aligned16(k) || !aligned16(v) ||
       !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PKV_ERR_INVALID, "paged_kv_append: NULL or misaligned pointer");
-  if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale))
-    return fail(PKV_ERR_INVALID, "paged_kv_append: FP8 cache needs k_scale and v_scale");
+  if (is_code8(cache_dtype) && (!k_scale || !v_scale))
+    return fail(PKV_ERR_INVALID, "paged_kv_append: a one-byte cache needs k_scale and v_scale");
   AppendArgs a{k, v, in_dtype, num_tokens, num_kv_heads, head_dim, slot_mapping, k_cache, v_cache,
                cache_dtype, k_scale, v_scale, num_blocks, d_error,
                reinterpret_cast<cudaStream_t>(stream)};
@@ -305,9 +314,9 @@ pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, c
       !aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(workspace))
     return fail(PKV_ERR_INVALID, "paged_attention_decode: NULL or misaligned pointer");
-  if (cache_dtype == PKV_FP8_E4M3 &&
+  if (is_code8(cache_dtype) &&
       (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
-    return fail(PKV_ERR_INVALID, "paged_attention_decode: FP8 cache needs aligned k_scale and v_scale");
+    return fail(PKV_ERR_INVALID, "paged_attention_decode: a one-byte cache needs aligned k_scale and v_scale");
   DecodeLayout lay;
   s = decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, q_dtype, cache_dtype, &lay);
   if (s != PKV_OK) return s;
@@ -358,7 +367,7 @@ pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, c
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
     if (rows >= (int64_t(1) << 31))
       return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: pool larger than 2^31 token rows");
-    const int esz = cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
+    const int esz = is_code8(cache_dtype) ? 1 : 2;
     CUtensorMap tmk, tmv;
     s = cache_tensor_map(k_cache, rows, esz, &tmk);
     if (s != PKV_OK) return s;

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "dtypes.h"
 #include "pkv.h"
 
 namespace pkv {
@@ -37,28 +38,84 @@ __device__ __forceinline__ float2 unpack2<PKV_F16>(uint32_t w) {
   return __half22float2(h);
 }
 
-// Four E4M3 codes (byte 0 first) to four floats.  E4M3 values are exact in fp16.
-__device__ __forceinline__ void unpack_e4m3x4(uint32_t w, float *out) {
-  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
-  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
-  float2 a = __half22float2(*reinterpret_cast<__half2 *>(&lo));
-  float2 b = __half22float2(*reinterpret_cast<__half2 *>(&hi));
+// ---- one-byte cache codes ----------------------------------------------------
+// FP8 E4M3, FP8 E5M2 and INT8 caches store one byte per element and one
+// fp32 scale per (token, KV head); the value is code value x scale.
+
+// Largest code value R of a one-byte type: scale = amax / R.
+template <int DT>
+__device__ __forceinline__ float code8_range() {
+  static_assert(is_code8(DT), "one-byte cache type");
+  return DT == PKV_FP8_E4M3 ? 448.f : (DT == PKV_FP8_E5M2 ? 57344.f : 127.f);
+}
+
+// Four codes (byte 0 first) -> two f16x2 words (codes 0, 1 and codes 2, 3).
+// Exact for all three types: every E4M3 / E5M2 value and every integer in
+// [-128, 127] is a binary16 number.  INT8 goes through the biased-exponent
+// identity: the binary16 word 0x6400 | (x ^ 0x80) is 1152 + x, so one
+// f16x2 subtraction of 1152 recovers x exactly.
+template <int DT>
+__device__ __forceinline__ void code4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  static_assert(is_code8(DT), "one-byte cache type");
+  if constexpr (DT == PKV_FP8_E4M3) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  } else if constexpr (DT == PKV_FP8_E5M2) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, a;\n\tcvt.rn.f16x2.e5m2x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  } else {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+  }
+}
+
+// Four codes (byte 0 first) to four floats.
+template <int DT>
+__device__ __forceinline__ void unpack_code4(uint32_t w, float *out) {
+  uint32_t lo, hi;
+  code4_to_f16x2<DT>(w, lo, hi);
+  const float2 a = __half22float2(*reinterpret_cast<__half2 *>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<__half2 *>(&hi));
   out[0] = a.x;
   out[1] = a.y;
   out[2] = b.x;
   out[3] = b.y;
 }
 
-// Unpack n bytes of cache row (n = 4, 8 or 16) into floats.
+// Two float32 quotients -> two codes (a in the low byte): nearest code,
+// ties to even, saturating (FP8) or clamped to [-127, 127] (INT8).
+template <int DT>
+__device__ __forceinline__ uint32_t encode2(float a, float b) {
+  static_assert(is_code8(DT), "one-byte cache type");
+  if constexpr (DT == PKV_FP8_E4M3) {
+    return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  } else if constexpr (DT == PKV_FP8_E5M2) {
+    return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E5M2);
+  } else {
+    const int ia = min(max(__float2int_rn(a), -127), 127);
+    const int ib = min(max(__float2int_rn(b), -127), 127);
+    return (static_cast<uint32_t>(ia) & 0xffu) | ((static_cast<uint32_t>(ib) & 0xffu) << 8);
+  }
+}
+
+// Unpack n bytes of cache row (n = 2, 4, 8 or 16) into floats.
 template <int DT, int NBYTES>
 __device__ __forceinline__ void unpack_row(const uint8_t *src, float *out) {
   static_assert(NBYTES == 2 || NBYTES == 4 || NBYTES == 8 || NBYTES == 16, "vector width");
-  if constexpr (NBYTES == 2) {  // two E4M3 codes
-    static_assert(DT == PKV_FP8_E4M3, "2-byte rows are FP8 only");
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(*reinterpret_cast<const __nv_fp8x2_storage_t *>(src), __NV_E4M3);
-    float2 f = __half22float2(*reinterpret_cast<__half2 *>(&h));
-    out[0] = f.x;
-    out[1] = f.y;
+  if constexpr (NBYTES == 2) {  // two one-byte codes
+    static_assert(is_code8(DT), "2-byte rows hold one-byte codes only");
+    float f[4];
+    unpack_code4<DT>(*reinterpret_cast<const uint16_t *>(src), f);
+    out[0] = f[0];
+    out[1] = f[1];
     return;
   } else {
   uint32_t w[NBYTES / 4];
@@ -73,8 +130,8 @@ __device__ __forceinline__ void unpack_row(const uint8_t *src, float *out) {
   }
 #pragma unroll
   for (int i = 0; i < NBYTES / 4; ++i) {
-    if constexpr (DT == PKV_FP8_E4M3) {
-      unpack_e4m3x4(w[i], out + 4 * i);
+    if constexpr (is_code8(DT)) {
+      unpack_code4<DT>(w[i], out + 4 * i);
     } else {
       float2 f = unpack2<DT>(w[i]);
       out[2 * i] = f.x;

@@ -22,7 +22,7 @@
 //    scale * log2 e).  Scores: lanes split head_dim, partial dot products are
 //    reduced across lanes with a transposing butterfly (G heads reduce in
 //    G-1+log2(lanes/G) shuffles), online softmax in base 2.
-//  * FP8 tiles are dequantised in registers: the per-token K scale multiplies
+//  * One-byte tiles are dequantised in registers: the per-token K scale multiplies
 //    the score and the per-token V scale folds into the probability.
 #pragma once
 
@@ -42,7 +42,7 @@ template <int D, int G, int CDT, int QDT>
 struct DecodeCfg {
   static constexpr int kWarps = 8;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kEsz = CDT == PKV_FP8_E4M3 ? 1 : 2;
+  static constexpr int kEsz = is_code8(CDT) ? 1 : 2;
   static constexpr int kRow = D * kEsz;                     // bytes of one token's row
   static constexpr int kTile = kBS * kRow;                  // one (block, head) tile of K or V
   static constexpr int kLPT = (D == 128 && G == 8) ? 16 : 8;  // lanes per token in q.K
@@ -53,7 +53,7 @@ struct DecodeCfg {
   static constexpr int kEPC = kChunk / kEsz;                // elements per load
   static constexpr int kEPT = kEPC * kNChunk;               // q elements per lane
   static constexpr int kDPL = D / 32;                       // output elements per lane
-  static constexpr int kScale = CDT == PKV_FP8_E4M3 ? kBS * 4 : 0;
+  static constexpr int kScale = is_code8(CDT) ? kBS * 4 : 0;
   static constexpr int kQ = G * D * 2;
   static constexpr int kOffV = kTile;
   static constexpr int kOffKS = 2 * kTile;
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
             for (int e = 0; e < C::kEPC; ++e) part[g] = fmaf(qreg[g][c * C::kEPC + e], x[e], part[g]);
         }
         float r = reduce_heads<G, C::kLPT>(part, lane);
-        if constexpr (CDT == PKV_FP8_E4M3) r *= reinterpret_cast<const float *>(sb + C::kOffKS)[tok];
+        if constexpr (is_code8(CDT)) r *= reinterpret_cast<const float *>(sb + C::kOffKS)[tok];
         sc[ps] = tok < ntok ? r : -INFINITY;
       }
       // -- online softmax over this tile (per head) --
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
         for (int ps = 0; ps < C::kPasses; ++ps) {
           const int tok = ps * C::kTPP + tg;
           float pv = pr[ps];
-          if constexpr (CDT == PKV_FP8_E4M3) pv *= reinterpret_cast<const float *>(sb + C::kOffVS)[tok];
+          if constexpr (is_code8(CDT)) pv *= reinterpret_cast<const float *>(sb + C::kOffVS)[tok];
           pbuf[tok * G + hd] = pv;
         }
         if (tg == 0) {

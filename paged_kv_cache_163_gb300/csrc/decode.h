@@ -72,6 +72,14 @@ cudaError_t decode_call_fp8_f16(int head_dim, int group, int op, const DecodePar
                                 int64_t *launches, DecodeShape *shape);
 cudaError_t decode_call_fp8_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
                                  int64_t *launches, DecodeShape *shape);
+cudaError_t decode_call_e5m2_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                                 int64_t *launches, DecodeShape *shape);
+cudaError_t decode_call_e5m2_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                                 int64_t *launches, DecodeShape *shape);
+cudaError_t decode_call_int8_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                                 int64_t *launches, DecodeShape *shape);
+cudaError_t decode_call_int8_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                                 int64_t *launches, DecodeShape *shape);
 
 // Tensor-core variant (head_dim 128 only); tmk / tmv map the K and V pools as
 // 2D [rows = num_blocks * num_kv_heads * 16][128 elements] with 128-byte swizzle.
@@ -82,6 +90,14 @@ cudaError_t decode_mma_call_bf16(int group, int op, const DecodeParams *p, const
 cudaError_t decode_mma_call_fp8_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                     const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 cudaError_t decode_mma_call_fp8_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                     const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
+cudaError_t decode_mma_call_e5m2_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                     const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
+cudaError_t decode_mma_call_e5m2_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                     const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
+cudaError_t decode_mma_call_int8_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                     const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
+cudaError_t decode_mma_call_int8_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                      const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 
 // paged_attention_decode with a choice of launch: programmatic == true lets

@@ -10,8 +10,9 @@
 // are conflict-free because the head_dim order inside the MMAs is permuted
 // (a dot product and the output rows do not depend on the order, only on
 // using the same order for K and Q, and writing O with the matching d).
-// FP8 codes become fp16 in registers (exact); a bf16 P is split into a
-// high and a low bf16 half so the probabilities keep fp16-class precision.
+// One-byte codes (FP8 E4M3 / E5M2, INT8) become fp16 in registers (exact);
+// a bf16 P is split into a high and a low bf16 half so the probabilities
+// keep fp16-class precision.
 #pragma once
 
 #include <cuda.h>
@@ -44,14 +45,6 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return y;
 }
 
-// Four E4M3 codes (byte 0 first) -> two f16x2 (codes 0,1 and 2,3); exact.
-__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
@@ -75,18 +68,18 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 template <int G, int CDT, int QDT>
 struct MmaCfg {
   static constexpr int kD = 128;
-  static constexpr bool kFp8 = CDT == PKV_FP8_E4M3;
-  // FP8 tiles are half the bytes, so an SM holds twice the warps (with at
-  // most 128 registers a thread).  They form one 16-warp CTA: two 8-warp CTAs
-  // on an SM were measured to run unevenly (the CTA launched first streamed
-  // ~13% faster), leaving the SM half idle at the end of a call.
-  static constexpr int kWarps = kFp8 ? 16 : 8;
+  static constexpr bool kCode8 = is_code8(CDT);  // one-byte codes (FP8 E4M3 / E5M2, INT8) with scales
+  // One-byte tiles are half the bytes, so an SM holds twice the warps (with
+  // at most 128 registers a thread).  They form one 16-warp CTA: two 8-warp
+  // CTAs on an SM were measured to run unevenly (the CTA launched first
+  // streamed ~13% faster), leaving the SM half idle at the end of a call.
+  static constexpr int kWarps = kCode8 ? 16 : 8;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr bool kBf16 = !kFp8 && CDT == PKV_BF16;  // MMA operand type: bf16, else f16
-  static constexpr int kEsz = kFp8 ? 1 : 2;
+  static constexpr bool kBf16 = !kCode8 && CDT == PKV_BF16;  // MMA operand type: bf16, else f16
+  static constexpr int kEsz = kCode8 ? 1 : 2;
   static constexpr int kTile = kBS * kD * kEsz;  // K or V tile bytes (1024-aligned in shared memory)
   static constexpr int kKV = 2 * kTile;
-  static constexpr int kScale = kFp8 ? kBS * 4 : 0;
+  static constexpr int kScale = kCode8 ? kBS * 4 : 0;
   static constexpr int kQ = G * kD * 2;
   static constexpr int kAux = round_up_c(2 * kScale + kQ, 128);  // [k scales][v scales][q rows]
   // Two stages per warp: measured faster than deeper rings on GB300 (more
@@ -105,9 +98,9 @@ struct MmaCfg {
 };
 
 // head_dim index of output row m (0..15) of m-tile i for lane group g (see kernel comment).
-template <bool FP8>
+template <bool CODE8>
 __device__ __forceinline__ int out_d(int g, int i, int hrow) {
-  return FP8 ? 16 * g + 2 * i + hrow : 64 * (i >> 2) + 8 * g + 2 * (i & 3) + hrow;
+  return CODE8 ? 16 * g + 2 * i + hrow : 64 * (i >> 2) + 8 * g + 2 * (i & 3) + hrow;
 }
 
 template <int G, int CDT, int QDT>
@@ -171,7 +164,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
           const int kvh = item % p.num_kv_heads;
           const int64_t tile = static_cast<int64_t>(d.x) * p.num_kv_heads + kvh;
           const int row = static_cast<int>(tile * kBS);
-          if constexpr (C::kFp8) {
+          if constexpr (C::kCode8) {
             tma_load_2d(tb, &tmk, 0, row, bars + st, pol);
             tma_load_2d(tb + C::kTile, &tmv, 0, row, bars + st, pol);
             bulk_g2s(ab, p.k_scale + tile * kBS, C::kScale, bars + st, pol);
@@ -205,6 +198,10 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
   uint32_t qb[8][2];   // Q^T B fragments (8 k-steps)
   float oacc[8][4];    // O^T accumulators (8 m-tiles of 16 head_dim rows x 8 heads)
   float m_run[2], l_run[2];  // heads 2 q4 and 2 q4 + 1 (running max: base-2 domain)
+  // One-byte caches: oacc holds O / vunit, where vunit is the largest V scale
+  // of the latest tile (P carries the tile's scales relative to it, so the
+  // fp16 B operand stays in [0, 1] whatever the scales' magnitude).
+  float vunit = 1.f;
   int cur_item = -1;
   bool whole_start = false, saw_last = false;
 
@@ -223,11 +220,11 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       const int n = 2 * q4 + j;
       if (n >= G) continue;
       if (whole) {
-        const float inv = lt[j] > 0.f ? 1.f / lt[j] : 0.f;
+        const float inv = (lt[j] > 0.f ? 1.f / lt[j] : 0.f) * vunit;
         const size_t row = (static_cast<size_t>(item) * G + n) * D;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int d0 = out_d<C::kFp8>(g, i, 0);
+          const int d0 = out_d<C::kCode8>(g, i, 0);
           const float r0 = oacc[i][j] * inv, r1 = oacc[i][2 + j] * inv;
           if (p.out_f32) {
             *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.out) + row + d0) = make_float2(r0, r1);
@@ -240,15 +237,16 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
         float *op = p.ws_o + (slot * G + n) * D;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float2 *>(op + out_d<C::kFp8>(g, i, 0)) = make_float2(oacc[i][j], oacc[i][2 + j]);
+          *reinterpret_cast<float2 *>(op + out_d<C::kCode8>(g, i, 0)) =
+              make_float2(oacc[i][j] * vunit, oacc[i][2 + j] * vunit);
         if (g == 0) {
           p.ws_ml[(slot * G + n) * 2] = m_run[j];
           p.ws_ml[(slot * G + n) * 2 + 1] = lt[j];
         }
       }
     }
-    // merge batches sized to the register budget (FP8 instances: 128 a thread)
-    if (!whole) finish_partial<D, G, QDT, C::kFp8 ? 8 : 32>(p, cum, item, total, nwarps);
+    // merge batches sized to the register budget (one-byte instances: 128 a thread)
+    if (!whole) finish_partial<D, G, QDT, C::kCode8 ? 8 : 32>(p, cum, item, total, nwarps);
   };
 
   // tokens whose V rows this lane reads (B-fragment k rows of P^T)
@@ -282,10 +280,10 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       const uint8_t *qs = ab + 2 * C::kScale;  // [G][128] rows in the query dtype
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const int d0 = C::kFp8 ? 32 * q4 + 4 * s : 64 * (s >> 2) + 16 * q4 + 4 * (s & 3);
+        const int d0 = C::kCode8 ? 32 * q4 + 4 * s : 64 * (s >> 2) + 16 * q4 + 4 * (s & 3);
         uint2 raw = make_uint2(0u, 0u);
         if (g < G) raw = *reinterpret_cast<const uint2 *>(qs + (g * D + d0) * 2);
-        if constexpr (C::kFp8 && QDT == PKV_BF16) {  // f16 MMA operands
+        if constexpr (C::kCode8 && QDT == PKV_BF16) {  // f16 MMA operands
           const float2 a = unpack2<QDT>(raw.x), b = unpack2<QDT>(raw.y);
           qb[s][0] = pack2<PKV_F16>(a.x, a.y);
           qb[s][1] = pack2<PKV_F16>(b.x, b.y);
@@ -299,6 +297,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
 #pragma unroll
         for (int c = 0; c < 4; ++c) oacc[i][c] = 0.f;
       m_run[0] = m_run[1] = -INFINITY;
+      vunit = 1.f;
       l_run[0] = l_run[1] = 0.f;
     }
     saw_last = (d.y >> 5) & 1;
@@ -306,7 +305,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
     if (d.x >= 0) {
       // ---- S^T = K Q^T: lane rows g and g + 8, head columns 2 q4, 2 q4 + 1 ----
       float sacc4[4][4] = {};  // four independent accumulation chains over the 8 k-steps
-      if constexpr (C::kFp8) {
+      if constexpr (C::kCode8) {
         uint4 kr[2][2];  // [row g, g + 8][chunk 2 q4 + j]
 #pragma unroll
         for (int r = 0; r < 2; ++r)
@@ -318,8 +317,8 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           uint32_t a[4];
-          e4m3x4_to_f16(word(kr[0][s >> 2], s & 3), a[0], a[2]);
-          e4m3x4_to_f16(word(kr[1][s >> 2], s & 3), a[1], a[3]);
+          code4_to_f16x2<CDT>(word(kr[0][s >> 2], s & 3), a[0], a[2]);
+          code4_to_f16x2<CDT>(word(kr[1][s >> 2], s & 3), a[1], a[3]);
           mma_16816(sacc4[s & 3], a, qb[s][0], qb[s][1], false);
         }
       } else {
@@ -346,7 +345,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       for (int c = 0; c < 4; ++c) sacc[c] = (sacc4[0][c] + sacc4[1][c]) + (sacc4[2][c] + sacc4[3][c]);
       // ---- scale, mask, online softmax (base 2) ----
       float sc0 = p.scale_log2, sc1 = p.scale_log2;
-      if constexpr (C::kFp8) {
+      if constexpr (C::kCode8) {
         const float *ksc = reinterpret_cast<const float *>(ab);
         sc0 *= ksc[g];
         sc1 *= ksc[g + 8];
@@ -363,26 +362,37 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
         mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
       }
       const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-      const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
+      float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
       m_run[0] = mn0;
       m_run[1] = mn1;
       float p00 = exp2f(s00 - mn0), p01 = exp2f(s01 - mn1), p10 = exp2f(s10 - mn0), p11 = exp2f(s11 - mn1);
       l_run[0] = l_run[0] * al0 + (p00 + p10);
       l_run[1] = l_run[1] * al1 + (p01 + p11);
+      if constexpr (C::kCode8) {  // per-token V scales, relative to the tile's largest, go into P
+        const float *vsc = reinterpret_cast<const float *>(ab + C::kScale);
+        const float vs0 = v0 ? vsc[g] : 0.f, vs1 = v1 ? vsc[g + 8] : 0.f;
+        float vmax = fmaxf(vs0, vs1);  // over the tile's 16 tokens (lane groups g hold tokens g, g + 8)
+        vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 4));
+        vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 8));
+        vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 16));
+        if (!(vmax > 0.f)) vmax = 1.f;  // all scales zero: the tile adds nothing either way
+        const float rv = 1.f / vmax;
+        const float w0 = vs0 * rv, w1 = vs1 * rv;
+        p00 *= w0;
+        p01 *= w0;
+        p10 *= w1;
+        p11 *= w1;
+        const float ru = vunit * rv;  // oacc changes units from the old vunit to vmax
+        al0 *= ru;
+        al1 *= ru;
+        vunit = vmax;
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         oacc[i][0] *= al0;
         oacc[i][1] *= al1;
         oacc[i][2] *= al0;
         oacc[i][3] *= al1;
-      }
-      if constexpr (C::kFp8) {  // fold the per-token V scale into P
-        const float *vsc = reinterpret_cast<const float *>(ab + C::kScale);
-        const float w0 = v0 ? vsc[g] : 0.f, w1 = v1 ? vsc[g + 8] : 0.f;
-        p00 *= w0;
-        p01 *= w0;
-        p10 *= w1;
-        p11 *= w1;
       }
       // ---- P^T B fragments (k rows = tokens, n columns = heads) ----
       uint32_t pb[2][2];  // [hi / lo][b0, b1]
@@ -400,7 +410,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       }
       // ---- O^T += V^T P^T ----
       const bool tail = ntok < kBS;
-      if constexpr (C::kFp8) {
+      if constexpr (C::kCode8) {
         uint4 vr[4];  // tokens tk0..tk3, chunk g (head_dim 16 g .. 16 g + 15)
         const int tks[4] = {tk0, tk1, tk2, tk3};
 #pragma unroll
@@ -412,10 +422,10 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
         for (int w = 0; w < 4; ++w) {
           const uint32_t x0 = word(vr[0], w), y0 = word(vr[1], w), x1 = word(vr[2], w), y1 = word(vr[3], w);
           uint32_t a[4], b[4];
-          e4m3x4_to_f16(prmt(x0, y0, 0x5140), a[0], a[1]);
-          e4m3x4_to_f16(prmt(x1, y1, 0x5140), a[2], a[3]);
-          e4m3x4_to_f16(prmt(x0, y0, 0x7362), b[0], b[1]);
-          e4m3x4_to_f16(prmt(x1, y1, 0x7362), b[2], b[3]);
+          code4_to_f16x2<CDT>(prmt(x0, y0, 0x5140), a[0], a[1]);
+          code4_to_f16x2<CDT>(prmt(x1, y1, 0x5140), a[2], a[3]);
+          code4_to_f16x2<CDT>(prmt(x0, y0, 0x7362), b[0], b[1]);
+          code4_to_f16x2<CDT>(prmt(x1, y1, 0x7362), b[2], b[3]);
           mma_16816(oacc[2 * w], a, pb[0][0], pb[0][1], false);
           mma_16816(oacc[2 * w + 1], b, pb[0][0], pb[0][1], false);
         }

@@ -16,6 +16,7 @@
 
 #include "append.h"
 #include "decode.h"
+#include "dtypes.h"
 #include "pkv.h"
 #include "status.h"
 
@@ -71,7 +72,7 @@ pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32
   if (!pool || !out || max_seqs <= 0 || max_seqs > PKV_MAX_SEQS_PER_CALL || max_blocks_per_seq <= 0)
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: bad argument");
   if (pool->num_layers <= 0 || pool->num_blocks <= 0 || pool->num_kv_heads <= 0 || !pool->k_cache ||
-      !pool->v_cache || (pool->cache_dtype == PKV_FP8_E4M3 && (!pool->k_scale || !pool->v_scale)))
+      !pool->v_cache || (pkv::is_code8(pool->cache_dtype) && (!pool->k_scale || !pool->v_scale)))
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: bad pool descriptor");
   if (!host_staging || host_staging_bytes < pkv_stepper_host_bytes(max_seqs, max_blocks_per_seq) ||
       !dev_meta || dev_meta_bytes < pkv_stepper_device_bytes(max_seqs, max_blocks_per_seq))

@@ -26,7 +26,9 @@ def torch_dtype(name: str):
     global _TORCH_DTYPES
     import torch
     if _TORCH_DTYPES is None:
-        _TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}
+        # one-byte caches hold their codes as bytes; the type is passed by name
+        _TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8,
+                         "fp8_e5m2": torch.uint8, "int8": torch.uint8}
     return _TORCH_DTYPES[name]
 
 
@@ -67,7 +69,7 @@ class PagedKVCache:
         tdt = torch_dtype(cache_dtype)
         self.k = torch.empty(shape, dtype=tdt, device=self.device)
         self.v = torch.empty(shape, dtype=tdt, device=self.device)
-        if cache_dtype == "fp8_e4m3":
+        if cache_dtype in capi.ONE_BYTE_CACHES:
             self.k_scale = torch.empty(shape[:4], dtype=torch.float32, device=self.device)
             self.v_scale = torch.empty(shape[:4], dtype=torch.float32, device=self.device)
         else:
@@ -163,12 +165,12 @@ class PagedKVCache:
             vs = self.v_scale[li] if self.v_scale is not None else None
             if len(cs):
                 capi.paged_kv_copy_blocks(self.k[li], self.v[li], ks, vs, d_src, d_dst, len(cs),
-                                          d_error=self.err, stream=stream)
+                                          d_error=self.err, stream=stream, cache_dtype=self.cache_dtype)
             kr = k_rows[li] if k_rows.dim() == 4 else k_rows
             vr = v_rows[li] if v_rows.dim() == 4 else v_rows
             if len(slots):
                 capi.paged_kv_append(kr, vr, d_slots, self.k[li], self.v[li], ks, vs,
-                                     d_error=self.err, stream=stream)
+                                     d_error=self.err, stream=stream, cache_dtype=self.cache_dtype)
 
     # -- decode ------------------------------------------------------------------
     def tables(self, seq_ids):
@@ -213,7 +215,7 @@ class PagedKVCache:
             vs = self.v_scale[li] if self.v_scale is not None else None
             capi.paged_attention_decode(out if one else out[li], q if one else q[li], self.k[li], self.v[li],
                                         ks, vs, d_tables, d_ctx, max_len, scale, ws, d_error=self.err,
-                                        stream=stream)
+                                        stream=stream, cache_dtype=self.cache_dtype)
         if marks is not None:
             marks[1].record(stream)
         return out

@@ -53,6 +53,10 @@ def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(f"no rounding for {dtype}")
 
 
+# cache types stored as one-byte codes plus an fp32 scale per (token, KV head)
+ONE_BYTE_CACHES = ("fp8_e4m3", "fp8_e5m2", "int8")
+
+
 @dataclass
 class Workload:
     name: str
@@ -62,7 +66,7 @@ class Workload:
     num_kv_heads: int
     head_dim: int
     q_dtype: str              # 'f16' | 'bf16'  (also the dtype of appended K/V rows)
-    cache_dtype: str          # 'f16' | 'bf16' | 'fp8_e4m3'
+    cache_dtype: str          # 'f16' | 'bf16' | 'fp8_e4m3' | 'fp8_e5m2' | 'int8'
     num_layers: int
     context_lens: np.ndarray  # int64 [B], post-append
     num_blocks: int
@@ -155,7 +159,7 @@ class Workload:
     def kv_bytes(self, step: int = 0) -> int:
         """Bytes of K and V (codes + fp32 scales for FP8) the decode step reads per layer."""
         tokens = int(self.context_lens.sum()) + step * self.num_seqs
-        per = self.num_kv_heads * (self.head_dim + 4 if self.cache_dtype == "fp8_e4m3"
+        per = self.num_kv_heads * (self.head_dim + 4 if self.cache_dtype in ONE_BYTE_CACHES
                                    else self.head_dim * 2)
         return 2 * tokens * per
 

@@ -1,15 +1,16 @@
 """GPU parity of reshape-and-cache (append) and copy-on-write block copies.
 
-Bit-exact against the oracle: 16-bit caches hold the input bits; the FP8
-cache holds the oracle's E4M3 codes and fp32 scales, including an
-exhaustive sweep over every E4M3 value and every midpoint between two
-neighbours (round-to-nearest-even ties), subnormals, +-0 and saturation.
+Bit-exact against the oracle: 16-bit caches hold the input bits; one-byte
+caches (FP8 E4M3, FP8 E5M2, INT8) hold the oracle's codes and fp32 scales,
+including exhaustive sweeps over every code value and every midpoint
+between two neighbours (round-to-nearest-even ties), subnormals, +-0 and
+saturation.
 """
 import numpy as np
 import pytest
 
 from oracle import fp8
-from oracle.cache import PagedCacheModel
+from oracle.cache import CODE_TYPES, PagedCacheModel
 from paged_kv_cache_163_gb300 import workloads as wl
 
 from helpers import cache_bits, oracle_bits
@@ -33,21 +34,21 @@ def run_append(capi, rows_k, rows_v, slots, num_blocks, hkv, d, in_dtype, cache_
     kc.view(torch.uint8).fill_(0xFF)
     vc.view(torch.uint8).fill_(0xFF)
     ks = vs = None
-    if cache_dtype == "fp8_e4m3":
+    if cache_dtype in CODE_TYPES:
         ks = torch.full((num_blocks, hkv, 16), float("nan"), device=dev)
         vs = torch.full_like(ks, float("nan"))
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     k = torch.from_numpy(rows_k).to(dev).to(torch_dtype(in_dtype))
     v = torch.from_numpy(rows_v).to(dev).to(torch_dtype(in_dtype))
     s = torch.from_numpy(np.asarray(slots, dtype=np.int32)).to(dev)
-    capi.paged_kv_append(k, v, s, kc, vc, ks, vs, d_error=err)
+    capi.paged_kv_append(k, v, s, kc, vc, ks, vs, d_error=err, cache_dtype=cache_dtype)
     flag = capi.pkv_read_device_error(err)
     return kc, vc, ks, vs, flag
 
 
 def compare_with_oracle(kc, vc, ks, vs, model: PagedCacheModel, cache_dtype):
     filled = model.filled            # [blocks, 16]
-    if cache_dtype == "fp8_e4m3":
+    if cache_dtype in CODE_TYPES:
         for got, want in ((cache_bits(kc), model.k), (cache_bits(vc), model.v)):
             g = got.transpose(0, 2, 1, 3)[filled]      # [n, hkv, d]
             w = want.transpose(0, 2, 1, 3)[filled]
@@ -65,7 +66,9 @@ def compare_with_oracle(kc, vc, ks, vs, model: PagedCacheModel, cache_dtype):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("in_dtype,cache_dtype", [("f16", "f16"), ("bf16", "bf16"),
-                                                  ("bf16", "fp8_e4m3"), ("f16", "fp8_e4m3")])
+                                                  ("bf16", "fp8_e4m3"), ("f16", "fp8_e4m3"),
+                                                  ("bf16", "fp8_e5m2"), ("f16", "fp8_e5m2"),
+                                                  ("bf16", "int8"), ("f16", "int8")])
 def test_append_random_rows_bit_exact(capi, d, in_dtype, cache_dtype):
     rng = np.random.default_rng(d + len(cache_dtype))
     nb, hkv, t = 37, 4, 300
@@ -113,6 +116,69 @@ def test_fp8_grid_and_midpoint_sweep(capi, in_dtype):
     model.write(slots, x, -x)
     assert np.all(model.k_scale.reshape(-1)[:n] == 1.0)
     compare_with_oracle(kc, vc, ks, vs, model, "fp8_e4m3")
+
+
+def _grid_rows(vals, top, d=128):
+    """Rows of d values whose first element is `top` (so amax = top and the scale is exactly 1)."""
+    per = d - 1
+    n = -(-len(vals) // per)
+    rows = np.zeros((n, per), dtype=np.float64)
+    rows.flat[:len(vals)] = vals
+    return np.concatenate([np.full((n, 1), top), rows], axis=1).astype(np.float32)
+
+
+@pytest.mark.parametrize("in_dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("cache_dtype", ["fp8_e5m2", "int8"])
+def test_onebyte_grid_and_midpoint_sweep(capi, in_dtype, cache_dtype):
+    """Rows whose amax is the format's largest value R (scale exactly 1): every value and every tie."""
+    if cache_dtype == "fp8_e5m2":
+        grid = fp8.e5m2_decode_table()[:0x7C]             # 0 .. 57344
+        extra = [2.0 ** -17, 3 * 2.0 ** -17]
+    else:
+        grid = np.arange(128, dtype=np.float64)            # 0 .. 127
+        extra = [0.49, 0.51]
+    top = CODE_TYPES[cache_dtype][0]
+    mids = (grid[:-1] + grid[1:]) / 2
+    vals = np.concatenate([grid, mids, -grid, -mids, extra, [-0.0]])
+    vals = vals[np.abs(vals) <= top]
+    rows = _grid_rows(vals, top)
+    keep = np.array_equal(wl.round_to(rows, in_dtype), rows)
+    if not keep:                                          # drop what the input type cannot hold
+        ok = wl.round_to(vals.astype(np.float32), in_dtype) == vals
+        rows = _grid_rows(vals[ok], top)
+    assert np.array_equal(wl.round_to(rows, in_dtype), rows)
+    x = rows[:, None, :]
+    n = x.shape[0]
+    slots = np.arange(n, dtype=np.int32)
+    nb = -(-n // 16)
+    kc, vc, ks, vs, flag = run_append(capi, x, -x, slots, nb, 1, 128, in_dtype, cache_dtype)
+    assert flag == 0
+    model = PagedCacheModel(nb, 1, 128, cache_dtype)
+    model.write(slots, x, -x)
+    assert np.all(model.k_scale.reshape(-1)[:n] == 1.0)
+    compare_with_oracle(kc, vc, ks, vs, model, cache_dtype)
+
+
+@pytest.mark.parametrize("cache_dtype", ["fp8_e5m2", "int8"])
+def test_onebyte_scale_ties(capi, cache_dtype):
+    """Rows of code values times amax / R: quotients land on or next to code values after a real division."""
+    rng = np.random.default_rng(7)
+    d, hkv, t = 128, 2, 512
+    r, _, dec = CODE_TYPES[cache_dtype]
+    amax = wl.round_to(rng.uniform(1e-6, 1e4, (t, hkv)).astype(np.float32), "bf16")
+    if cache_dtype == "fp8_e5m2":
+        codes = rng.integers(0, 0x7C, (t, hkv, d))
+        base = fp8.e5m2_decode_table()[codes] / r
+    else:
+        base = (rng.integers(-127, 128, (t, hkv, d)) + rng.choice([0.0, 0.5], (t, hkv, d))) / r
+    x = wl.round_to((base * amax[..., None]).astype(np.float32), "bf16")
+    x[..., 0] = amax
+    slots = rng.permutation(64 * 16)[:t].astype(np.int32)
+    kc, vc, ks, vs, flag = run_append(capi, x, x[::-1].copy(), slots, 64, hkv, d, "bf16", cache_dtype)
+    assert flag == 0
+    model = PagedCacheModel(64, hkv, d, cache_dtype)
+    model.write(slots, x, x[::-1].copy())
+    compare_with_oracle(kc, vc, ks, vs, model, cache_dtype)
 
 
 def test_fp8_scale_ties_and_tiny_rows(capi):
