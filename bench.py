@@ -46,15 +46,18 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu capture), keyed by workload and by the hash of the decode kernel source it
 # was taken on; reported only while the source is unchanged.
 NCU_TRAFFIC = {
-    # decode kernel source 0e9e55bcdd3685bb (tensor-core kernel, two-stage rings), default "auto" variant
-    ("long-fp8", "0e9e55bcdd3685bb"): 814_920_960,    # 810.41 MB read + 4.51 MB written
-    ("llama3-8b", "0e9e55bcdd3685bb"): 145_818_880,   # 142.71 MB read + 3.11 MB written
+    # decode kernel source 15857f1aad5937c5: tensor-core kernel, 16-warp CTAs for one-byte caches,
+    # one-pass merge, per-tile V-scale normalisation; default "auto" variant
+    ("llama3-8b", "15857f1aad5937c5"): 146_192_128,            # 142.69 MB read + 3.51 MB written
+    ("long-fp8", "15857f1aad5937c5"): 813_521_920,             # 810.14 MB read + 3.38 MB written
+    ("long-fp8:fp8_e5m2", "15857f1aad5937c5"): 813_516_544,    # 810.21 MB read + 3.31 MB written
+    ("long-fp8:int8", "15857f1aad5937c5"): 813_247_744,        # 810.08 MB read + 3.17 MB written
 }
 
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cuh", "decode_mma.cuh", "common.cuh"):
+    for f in ("decode.cuh", "decode_mma.cuh", "common.cuh", "dtypes.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_163_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -67,6 +70,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cache-dtype", choices=["fp8_e4m3", "fp8_e5m2", "int8"], default=None,
+                    help="swap the workload's cache for this one-byte type (same shapes and values)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
@@ -227,7 +232,7 @@ def run_ours(args, world, rank, local):
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
     attn_steps = max(3, min(args.steps, 30))
     total_steps = args.warmup + args.steps + attn_steps + e2e_steps
-    w = wl.make(wid, extra_steps=max(total_steps, CPU_MAX_STEPS) + 1)
+    w = wl.make(wid, extra_steps=max(total_steps, CPU_MAX_STEPS) + 1, cache_dtype=args.cache_dtype)
     cache = play.new_cache(w, device=dev)
     play.prefill(w, cache, device=dev)
     torch.cuda.synchronize()
@@ -299,7 +304,8 @@ def run_ours(args, world, rank, local):
     per_launch_bytes = statistics.mean(a["roofline_bytes"] for a in attn_acc)
     per_launch_s = t_attn / (attn_steps * w.num_layers)
     achieved = per_launch_bytes / per_launch_s / 1e9
-    traffic = NCU_TRAFFIC.get((args.workload, kernel_hash())) if args.kernel == "auto" else None
+    traffic_key = args.workload if args.cache_dtype is None else f"{args.workload}:{args.cache_dtype}"
+    traffic = NCU_TRAFFIC.get((traffic_key, kernel_hash())) if args.kernel == "auto" else None
     value = whole_job_rate(world, kv_total, t_total) / 1e9
     result = {
         "metric": METRIC,
@@ -312,7 +318,8 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.cache_dtype if w.cache_dtype != "fp8_e4m3" else "fp8_e4m3 (bf16 q, fp32 accumulate)",
+        "dtype": w.cache_dtype if w.cache_dtype not in wl.ONE_BYTE_CACHES else
+        f"{w.cache_dtype} ({w.q_dtype} q, fp32 accumulate)",
         "data": "synthetic (seeded N(0,1); no dataset or weights)",
         "config": workload_config(w, args.workload, {"parallelism": f"replicas x{world} (sequences sharded)",
                                                      "decode_kernel": args.kernel}),
@@ -452,7 +459,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     wid = WORKLOADS[args.workload]
-    w = wl.make(wid, extra_steps=max(args.warmup + args.steps + 1, CPU_MAX_STEPS + 1))
+    w = wl.make(wid, extra_steps=max(args.warmup + args.steps + 1, CPU_MAX_STEPS + 1), cache_dtype=args.cache_dtype)
     seqs = sample_seqs(w, 3000 if w.cache_dtype != "fp8_e4m3" else 17000)
     o = oracle_sample_state(w, seqs, max_steps=args.warmup + args.steps + 1)
     oracle_steps(w, o, seqs, 0, 0.0, max_steps=args.warmup)

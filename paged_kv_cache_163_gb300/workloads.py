@@ -27,7 +27,7 @@ tokens, then the decode step appends one token and attends over all L.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 import numpy as np
 
@@ -172,8 +172,28 @@ def _blocks(lengths) -> int:
     return int(sum(-(-int(L) // BLOCK_SIZE) for L in lengths))
 
 
-def make(wid: int, *, extra_steps: int = 0, num_seqs: int | None = None) -> Workload:
-    """Workload 1..5.  ``extra_steps`` reserves pool room for that many more decode steps."""
+def make(wid: int, *, extra_steps: int = 0, num_seqs: int | None = None,
+         cache_dtype: str | None = None) -> Workload:
+    """Workload 1..5.  ``extra_steps`` reserves pool room for that many more decode steps.
+
+    ``cache_dtype`` swaps the cache for a one-byte type (same shapes, seeds
+    and values; the rows are quantised on append).
+    """
+    w = _make(wid, extra_steps=extra_steps, num_seqs=num_seqs)
+    if cache_dtype is None or cache_dtype == w.cache_dtype:
+        return w
+    if cache_dtype not in ONE_BYTE_CACHES:
+        raise ValueError(f"a workload's cache can only be swapped for a one-byte type, not {cache_dtype}")
+    if w.cache_dtype in ONE_BYTE_CACHES:
+        name = w.name.rsplit("-", 1)[0]
+        desc = w.description.replace(w.cache_dtype.replace("_", " "), cache_dtype.replace("_", " "))
+    else:
+        name = w.name
+        desc = f"{w.description}; cache swapped to {cache_dtype} + fp32 scales"
+    return replace(w, name=f"{name}-{cache_dtype}", cache_dtype=cache_dtype, description=desc)
+
+
+def _make(wid: int, *, extra_steps: int = 0, num_seqs: int | None = None) -> Workload:
     seed = SEED_BASE + wid
     rlen = _rng(seed, 0)
     scale = lambda d: float(np.float32(1.0) / np.sqrt(np.float32(d)))
