@@ -235,6 +235,25 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
                                   float scale, void *workspace, size_t workspace_bytes,
                                   int32_t *d_error, pkv_stream_t stream);
 
+/* Append and decode in one launch ("KV Cache 与 vLLM" §1.3: every step
+ * appends the new token's K/V, then the query attends over the whole
+ * cache).  Same arguments and result as paged_attention_decode, plus the new
+ * rows: k_new, v_new [num_seqs][num_kv_heads][head_dim] in q_dtype, row b
+ * written at position context_lens[b] - 1 of sequence b (the last token
+ * the table covers) exactly as paged_kv_append would write it (16-bit copy,
+ * or one-byte codes with the scale to k_scale / v_scale), before the
+ * attention reads that block.  The caller has already grown the tables
+ * (pkv_seq_append_slots) and copied any shared block it writes into
+ * (paged_kv_copy_blocks).  The cache pointers are written. */
+pkv_status paged_attention_decode_append(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                         const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                         pkv_dtype cache_dtype, float *k_scale, float *v_scale,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                         int32_t *d_error, pkv_stream_t stream);
+
 /* Decode without a workspace argument, for callers that cannot allocate
  * device memory: a plugin whose host framework owns every device
  * allocation, or a latency-critical loop where an allocation could

@@ -82,6 +82,11 @@ _PROTOS = {
     "paged_attention_decode": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, C.c_int, _vp, _vp, _vp, C.c_int32,
                                          _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                          C.c_int32, C.c_float, _vp, C.c_size_t, _vp, _vp]),
+    # out, out_dtype, q, q_dtype, k_new, v_new, k_cache, v_cache, cache_dtype, k_scale, v_scale, tables,
+    # max_blocks, lens, max_len, num_seqs, hq, hkv, d, num_blocks, scale, workspace, bytes, d_error, stream
+    "paged_attention_decode_append": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, _vp, _vp, C.c_int, _vp, _vp,
+                                                _vp, C.c_int32, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                                C.c_int32, C.c_int32, C.c_float, _vp, C.c_size_t, _vp, _vp]),
     "paged_attention_decode_static": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, C.c_int, _vp, _vp, _vp,
                                                 C.c_int32, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                                 C.c_int32, C.c_int32, C.c_float, _vp, _vp]),
@@ -326,6 +331,21 @@ def paged_attention_decode(out, q, k_cache, v_cache, k_scale, v_scale, block_tab
         _dp(v_scale), _dp(block_tables), block_tables.shape[-1], _dp(context_lens), int(max_context_len), b, hq,
         hkv, d, nb, float(scale), _dp(workspace), workspace.numel() * workspace.element_size(),
         _dp(d_error), _stream(stream)), "paged_attention_decode")
+
+
+def paged_attention_decode_append(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                  context_lens, max_context_len, scale, workspace, d_error=None, stream=None,
+                                  num_seqs=None, cache_dtype=None) -> None:
+    """Append row b of k_new / v_new at position context_lens[b] - 1, then decode (one launch)."""
+    b, hq, d = q.shape
+    if num_seqs is not None:
+        b = num_seqs
+    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    _check(load().paged_attention_decode_append(
+        _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_new), _dp(v_new), _dp(k_cache), _dp(v_cache),
+        _cdt(k_cache, cache_dtype), _dp(k_scale), _dp(v_scale), _dp(block_tables), block_tables.shape[-1],
+        _dp(context_lens), int(max_context_len), b, hq, hkv, d, nb, float(scale), _dp(workspace),
+        workspace.numel() * workspace.element_size(), _dp(d_error), _stream(stream)), "paged_attention_decode_append")
 
 
 def paged_attention_decode_static(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,

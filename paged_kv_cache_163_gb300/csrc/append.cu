@@ -2,12 +2,15 @@
 //
 // Append ("KV Cache 与 vLLM" (zwxr.cn) §1.3, "企业官网建设流程全解析" §3.2):
 // every decode step writes the new token's K and V rows into the slot the
-// block manager gave it.  With an FP8 E4M3 cache ("KV Cache优化实战"
-// §3.2-§3.3) each (token, KV head) row is quantised with its own scale,
-// amax / 448, using IEEE fp32 divisions so the codes are reproducible.
+// block manager gave it.  With a one-byte cache ("KV Cache优化实战"
+// §3.2-§3.3: FP8 E4M3 / E5M2, INT8) each (token, KV head) row is quantised
+// with its own scale, amax / R, using IEEE fp32 divisions so the codes are
+// reproducible (common.cuh: append_row).
 //
 // Copy ("KV Cache 与 vLLM" §3.3): a shared block that must change is
 // copied whole to a fresh block before the new token lands in it.
+#include <algorithm>
+
 #include "append.h"
 #include "common.cuh"
 
@@ -27,7 +30,6 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
                                                      int32_t num_blocks, int32_t *err,
                                                      const int4 *__restrict__ meta_src,
                                                      int4 *__restrict__ meta_dst, int64_t meta_vecs) {
-  constexpr int EPL = D / 32;  // elements per lane
   // A decode launched after this kernel as a programmatic dependent may start
   // its prologue now; it waits for this grid to finish before reading K / V.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -54,42 +56,23 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
   const int64_t blk = slot / kBS;
   const int off = slot % kBS;
   const int64_t row = (blk * num_kv_heads + h) * kBS + off;  // index of the cache row
-  const uint8_t *src = (kind ? v : k) + th * D * 2 + lane * EPL * 2;
+  append_row<D, IDT, CDT>((kind ? v : k) + th * D * 2, kind ? v_cache : k_cache, kind ? v_scale : k_scale, row,
+                          lane);
+}
 
-  if constexpr (!is_code8(CDT)) {
-    uint8_t *dst = (kind ? v_cache : k_cache) + row * D * 2 + lane * EPL * 2;
-    if constexpr (EPL * 2 == 8) {
-      *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(src);
-    } else {
-      *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(src);
-    }
-  } else {
-    float x[EPL];
-    unpack_row<IDT, EPL * 2>(src, x);
-    float amax = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, code8_range<CDT>());
-    uint32_t packed = 0;
-#pragma unroll
-    for (int e = 0; e < EPL; e += 2) {
-      const uint32_t c2 = encode2<CDT>(__fdiv_rn(x[e], s), __fdiv_rn(x[e + 1], s));  // x[e] -> low byte
-      packed |= c2 << (8 * e);
-    }
-    uint8_t *dst = (kind ? v_cache : k_cache) + row * D + lane * EPL;
-    if constexpr (EPL == 4) {
-      *reinterpret_cast<uint32_t *>(dst) = packed;
-    } else {
-      *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
-    }
-    if (lane == 0) (kind ? v_scale : k_scale)[row] = s;
-  }
+// Step metadata: page-locked host staging -> device, 16-byte vectors.  A
+// decode launched after it as a programmatic dependent may start at once: it
+// reads the staging itself and waits for this grid before anything else.
+__global__ void __launch_bounds__(256) copy_meta_kernel(const int4 *__restrict__ src, int4 *__restrict__ dst,
+                                                        int64_t vecs) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+#pragma unroll 4
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < vecs; i += nth) dst[i] = src[i];
 }
 
 // One CTA per (pair, K-or-V): copies a whole physical block (all heads, all
-// 16 slots) and, for FP8, its scales.
+// 16 slots) and, for one-byte caches, its scales.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t *k_cache, uint8_t *v_cache,
                                                           float *k_scale, float *v_scale,
                                                           const int32_t *__restrict__ src,
@@ -150,6 +133,15 @@ static cudaError_t dispatch_append_d(const AppendArgs &a) {
 cudaError_t run_append(const AppendArgs &a) {
   if (a.num_tokens == 0) return cudaSuccess;
   return a.head_dim == 128 ? dispatch_append_d<128>(a) : dispatch_append_d<64>(a);
+}
+
+cudaError_t run_copy_meta(const int32_t *src, int32_t *dst, int64_t ints, cudaStream_t stream) {
+  const int64_t vecs = (ints + 3) / 4;
+  if (vecs <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((vecs + 255) / 256, 1024);
+  copy_meta_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(reinterpret_cast<const int4 *>(src),
+                                                                      reinterpret_cast<int4 *>(dst), vecs);
+  return cudaGetLastError();
 }
 
 cudaError_t run_copy_blocks(const CopyArgs &a) {

@@ -39,9 +39,13 @@ struct CopyArgs {
 
 cudaError_t run_append(const AppendArgs &a);
 cudaError_t run_copy_blocks(const CopyArgs &a);
+// Copy `ints` int32 (rounded up to whole 16-byte vectors) from page-locked host
+// memory (device address) to device memory; both 16-byte aligned.
+cudaError_t run_copy_meta(const int32_t *src, int32_t *dst, int64_t ints, cudaStream_t stream);
 
 // Launch with the caller's validation (the step executor's); count the launch.
 pkv_status append_unchecked(const AppendArgs &a);
 pkv_status copy_blocks_unchecked(const CopyArgs &a);
+pkv_status copy_meta_unchecked(const int32_t *src, int32_t *dst, int64_t ints, cudaStream_t stream);
 
 }  // namespace pkv

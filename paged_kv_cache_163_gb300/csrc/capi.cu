@@ -285,6 +285,13 @@ pkv_status append_unchecked(const AppendArgs &a) {
   return PKV_OK;
 }
 
+pkv_status copy_meta_unchecked(const int32_t *src, int32_t *dst, int64_t ints, cudaStream_t stream) {
+  cudaError_t e = run_copy_meta(src, dst, ints, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "step metadata copy");
+  ++t_launches;
+  return PKV_OK;
+}
+
 pkv_status copy_blocks_unchecked(const CopyArgs &a) {
   cudaError_t e = run_copy_blocks(a);
   if (e != cudaSuccess) return cuda_fail(e, "paged_kv_copy_blocks");
@@ -292,7 +299,8 @@ pkv_status copy_blocks_unchecked(const CopyArgs &a) {
   return PKV_OK;
 }
 
-pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_new, void *out, pkv_dtype out_dtype,
+                            const void *q, pkv_dtype q_dtype,
                             const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
                             const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,
                             const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
@@ -317,6 +325,8 @@ pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, c
   if (is_code8(cache_dtype) &&
       (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
     return fail(PKV_ERR_INVALID, "paged_attention_decode: a one-byte cache needs aligned k_scale and v_scale");
+  if ((k_new != nullptr) != (v_new != nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+    return fail(PKV_ERR_INVALID, "paged_attention_decode_append: k_new and v_new must both be given, 16-byte aligned");
   DecodeLayout lay;
   s = decode_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, q_dtype, cache_dtype, &lay);
   if (s != PKV_OK) return s;
@@ -347,6 +357,8 @@ pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, c
   p.d_error = d_error;
   p.stream = reinterpret_cast<cudaStream_t>(stream);
   p.programmatic = programmatic ? 1 : 0;
+  p.k_new = static_cast<const uint8_t *>(k_new);
+  p.v_new = static_cast<const uint8_t *>(v_new);
   s = prepare_counters(workspace, num_seqs, num_kv_heads, p.ws_ctr, static_cast<size_t>(lay.ctr_bytes), p.stream);
   if (s != PKV_OK) return s;
 
@@ -396,9 +408,25 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
                                   int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                                   float scale, void *workspace, size_t workspace_bytes,
                                   int32_t *d_error, pkv_stream_t stream) {
-  return pkv::attention_decode(false, out, out_dtype, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
-                               block_tables, max_blocks_per_seq, context_lens, max_context_len, num_seqs,
-                               num_q_heads, num_kv_heads, head_dim, num_blocks, scale, workspace,
+  return pkv::attention_decode(false, nullptr, nullptr, out, out_dtype, q, q_dtype, k_cache, v_cache, cache_dtype,
+                               k_scale, v_scale, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                               num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale, workspace,
+                               workspace_bytes, d_error, stream);
+}
+
+pkv_status paged_attention_decode_append(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                         const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                         pkv_dtype cache_dtype, float *k_scale, float *v_scale,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                         int32_t *d_error, pkv_stream_t stream) {
+  if (num_seqs > 0 && (!k_new || !v_new))
+    return fail(PKV_ERR_INVALID, "paged_attention_decode_append: NULL k_new or v_new");
+  return pkv::attention_decode(false, k_new, v_new, out, out_dtype, q, q_dtype, k_cache, v_cache, cache_dtype,
+                               k_scale, v_scale, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                               num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale, workspace,
                                workspace_bytes, d_error, stream);
 }
 

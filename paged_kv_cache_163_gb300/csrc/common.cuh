@@ -154,6 +154,73 @@ __device__ __forceinline__ uint32_t pack2<PKV_F16>(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// ---- reshape-and-cache of one row --------------------------------------------
+// One warp encodes one (token, KV head) row of K or V: head_dim elements of
+// 16-bit input into the cache's representation.  16-bit caches keep the
+// bits.  One-byte caches store per-row absmax codes: scale = amax / R in
+// IEEE fp32 (1 for an all-zero row), code = Q(x / scale) with an IEEE fp32
+// division.  Lane i holds elements [i * D/32, (i + 1) * D/32): its slice of
+// the cache row is kSliceBytes bytes, returned in the low bytes of a uint2.
+template <int D, int CDT>
+__host__ __device__ constexpr int slice_bytes() { return is_code8(CDT) ? D / 32 : D / 16; }
+
+template <int D, int IDT, int CDT>
+__device__ __forceinline__ uint2 encode_slice(const uint8_t *src_row, int lane, float &scale) {
+  constexpr int EPL = D / 32;  // elements per lane
+  const uint8_t *src = src_row + lane * EPL * 2;
+  uint2 r = make_uint2(0u, 0u);
+  if constexpr (!is_code8(CDT)) {
+    if constexpr (EPL == 4) {
+      r = *reinterpret_cast<const uint2 *>(src);
+    } else {
+      r.x = *reinterpret_cast<const uint32_t *>(src);
+    }
+    scale = 1.f;
+  } else {
+    float x[EPL];
+    unpack_row<IDT, EPL * 2>(src, x);
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, code8_range<CDT>());
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2) {
+      const uint32_t c2 = encode2<CDT>(__fdiv_rn(x[e], s), __fdiv_rn(x[e + 1], s));  // x[e] -> low byte
+      r.x |= c2 << (8 * e);
+    }
+    scale = s;
+  }
+  return r;
+}
+
+template <int D, int CDT>
+__device__ __forceinline__ void store_slice(uint8_t *dst, uint2 r) {
+  constexpr int B = slice_bytes<D, CDT>();
+  if constexpr (B == 8) {
+    *reinterpret_cast<uint2 *>(dst) = r;
+  } else if constexpr (B == 4) {
+    *reinterpret_cast<uint32_t *>(dst) = r.x;
+  } else {
+    *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(r.x);
+  }
+}
+
+// Encode `src_row` and store it as cache row `row` (index into
+// [blocks][heads][16]); lane 0 stores the scale of a one-byte cache.
+template <int D, int IDT, int CDT>
+__device__ __forceinline__ void append_row(const uint8_t *src_row, uint8_t *cache, float *scales, int64_t row,
+                                           int lane) {
+  float s;
+  const uint2 r = encode_slice<D, IDT, CDT>(src_row, lane, s);
+  constexpr int B = slice_bytes<D, CDT>();
+  store_slice<D, CDT>(cache + row * (B * 32) + lane * B, r);
+  if constexpr (is_code8(CDT)) {
+    if (lane == 0) scales[row] = s;
+  }
+}
+
 // ---- shared-memory barriers and bulk copies (sm_90+ PTX) -------------------
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -59,7 +59,9 @@ struct DecodeCfg {
   static constexpr int kOffKS = 2 * kTile;
   static constexpr int kOffVS = 2 * kTile + kScale;
   static constexpr int kOffQ = 2 * kTile + 2 * kScale;
-  static constexpr int kStage = round_up_c(kOffQ + kQ, 128);
+  static constexpr int kNew = 2 * D * 2;                    // fused append: the new token's K and V rows
+  static constexpr int kOffNew = kOffQ + kQ;
+  static constexpr int kStage = round_up_c(kOffNew + kNew, 128);
   static constexpr int kStages = clamp_c(27900 / kStage, 2, 6);
   static constexpr int kCumBytes = round_up_c((PKV_MAX_SEQS_PER_CALL + 1) * 4, 128);
   static constexpr int kMiscBytes = 128;                    // scan scratch
@@ -410,7 +412,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
       uint8_t *sb = stages + st * C::kStage;
       const int item = d.y >> 7;
       const bool need_q = (m == 0) || ((d.y >> 6) & 1);
-      const uint32_t bytes = (d.x >= 0 ? 2 * C::kTile + 2 * C::kScale : 0) + (need_q ? C::kQ : 0);
+      const bool need_new = p.k_new && d.x >= 0 && ((d.y >> 5) & 1);  // the item's last tile: its new token
+      const uint32_t bytes =
+          (d.x >= 0 ? 2 * C::kTile + 2 * C::kScale : 0) + (need_q ? C::kQ : 0) + (need_new ? C::kNew : 0);
       fence_proxy_async_smem();
       if (bytes == 0) {
         mbar_arrive(bars + st);
@@ -427,6 +431,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
           }
         }
         if (need_q) bulk_g2s(sb + C::kOffQ, p.q + static_cast<size_t>(item) * C::kQ, C::kQ, bars + st);
+        if (need_new) {
+          bulk_g2s(sb + C::kOffNew, p.k_new + static_cast<size_t>(item) * D * 2, D * 2, bars + st);
+          bulk_g2s(sb + C::kOffNew + D * 2, p.v_new + static_cast<size_t>(item) * D * 2, D * 2, bars + st);
+        }
       }
     }
   };
@@ -547,6 +555,33 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
       m_mine = -INFINITY;
     }
     saw_last = (d.y >> 5) & 1;
+
+    if (p.k_new && d.x >= 0 && saw_last) {
+      // Fused append: the item's new token is row r of this tile.  Encode the
+      // staged K / V rows as the cache holds them, put them into the staged
+      // tile and into the cache for later steps.  No other warp reads this
+      // tile, and its copy has landed, so nothing races.
+      const int r = (d.y & 31) - 1;
+      const int64_t grow = (static_cast<int64_t>(d.x) * p.num_kv_heads + item % p.num_kv_heads) * kBS + r;
+      float kscl, vscl;
+      const uint2 kb = encode_slice<D, QDT, CDT>(sb + C::kOffNew, lane, kscl);
+      const uint2 vb = encode_slice<D, QDT, CDT>(sb + C::kOffNew + D * 2, lane, vscl);
+      constexpr int B = slice_bytes<D, CDT>();
+      store_slice<D, CDT>(sb + r * C::kRow + lane * B, kb);
+      store_slice<D, CDT>(sb + C::kOffV + r * C::kRow + lane * B, vb);
+      // the caches are read-only everywhere else in the kernel
+      store_slice<D, CDT>(const_cast<uint8_t *>(p.k_cache) + grow * C::kRow + lane * B, kb);
+      store_slice<D, CDT>(const_cast<uint8_t *>(p.v_cache) + grow * C::kRow + lane * B, vb);
+      if constexpr (C::kScale > 0) {
+        if (lane == 0) {
+          reinterpret_cast<float *>(sb + C::kOffKS)[r] = kscl;
+          reinterpret_cast<float *>(sb + C::kOffVS)[r] = vscl;
+          const_cast<float *>(p.k_scale)[grow] = kscl;
+          const_cast<float *>(p.v_scale)[grow] = vscl;
+        }
+      }
+      __syncwarp();
+    }
 
     if (d.x >= 0) {
       const uint8_t *ks = sb;

@@ -38,6 +38,10 @@ struct DecodeParams {
   int32_t *d_error;
   cudaStream_t stream;
   int32_t programmatic;  // 1: launch as a programmatic dependent of the stream's previous kernel
+  // Optional fused append: row (b, kvh) of k_new / v_new ([num_seqs][num_kv_heads][head_dim] in the
+  // query dtype) is written at position context_lens[b] - 1 before that tile is read.  NULL: none.
+  const uint8_t *k_new;
+  const uint8_t *v_new;
 };
 
 // Launch `kernel` on `stream`; with programmatic != 0 the launch may begin
@@ -100,11 +104,13 @@ cudaError_t decode_mma_call_int8_f16(int group, int op, const DecodeParams *p, c
 cudaError_t decode_mma_call_int8_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                      const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 
-// paged_attention_decode with a choice of launch: programmatic == true lets
-// the kernel start while the stream's previous kernel finishes.  Only for
-// callers that know that kernel writes neither the block tables nor the
-// context lengths (the decode kernel reads those before it waits).
-pkv_status attention_decode(bool programmatic, void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+// paged_attention_decode (k_new == v_new == NULL) or
+// paged_attention_decode_append, with a choice of launch: programmatic ==
+// true lets the kernel start while the stream's previous kernel finishes.
+// Only for callers that know that kernel writes neither the block tables nor
+// the context lengths (the decode kernel reads those before it waits).
+pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_new, void *out, pkv_dtype out_dtype,
+                            const void *q, pkv_dtype q_dtype,
                             const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
                             const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,
                             const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,

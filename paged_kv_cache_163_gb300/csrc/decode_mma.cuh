@@ -81,7 +81,9 @@ struct MmaCfg {
   static constexpr int kKV = 2 * kTile;
   static constexpr int kScale = kCode8 ? kBS * 4 : 0;
   static constexpr int kQ = G * kD * 2;
-  static constexpr int kAux = round_up_c(2 * kScale + kQ, 128);  // [k scales][v scales][q rows]
+  static constexpr int kNew = 2 * kD * 2;  // fused append: the new token's K and V rows (query dtype)
+  static constexpr int kOffNew = 2 * kScale + kQ;
+  static constexpr int kAux = round_up_c(2 * kScale + kQ + kNew, 128);  // [k scales][v scales][q rows][new rows]
   // Two stages per warp: measured faster than deeper rings on GB300 (more
   // copies in flight than HBM needs only lengthen the queues).
   static constexpr int kStages = 2;
@@ -154,7 +156,9 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       uint8_t *ab = aux + st * C::kAux;
       const int item = d.y >> 7;
       const bool need_q = (m == 0) || ((d.y >> 6) & 1);
-      const uint32_t bytes = (d.x >= 0 ? C::kKV + 2 * C::kScale : 0) + (need_q ? C::kQ : 0);
+      const bool need_new = p.k_new && d.x >= 0 && ((d.y >> 5) & 1);  // the item's last tile: its new token
+      const uint32_t bytes =
+          (d.x >= 0 ? C::kKV + 2 * C::kScale : 0) + (need_q ? C::kQ : 0) + (need_new ? C::kNew : 0);
       fence_proxy_async_smem();
       if (bytes == 0) {
         mbar_arrive(bars + st);
@@ -177,6 +181,10 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
           }
         }
         if (need_q) bulk_g2s(ab + 2 * C::kScale, p.q + static_cast<size_t>(item) * C::kQ, C::kQ, bars + st);
+        if (need_new) {
+          bulk_g2s(ab + C::kOffNew, p.k_new + static_cast<size_t>(item) * D * 2, D * 2, bars + st);
+          bulk_g2s(ab + C::kOffNew + D * 2, p.v_new + static_cast<size_t>(item) * D * 2, D * 2, bars + st);
+        }
       }
     }
   };
@@ -301,6 +309,36 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       l_run[0] = l_run[1] = 0.f;
     }
     saw_last = (d.y >> 5) & 1;
+
+    if (p.k_new && d.x >= 0 && saw_last) {
+      // Fused append: the item's new token is row r of this tile.  Encode the
+      // staged K / V rows as the cache holds them, put them into the staged
+      // tile (swizzled layout) and into the cache for later steps.  No other
+      // warp reads this tile, and its copy has landed, so nothing races.
+      const int r = (d.y & 31) - 1;
+      const int64_t grow = (static_cast<int64_t>(d.x) * p.num_kv_heads + item % p.num_kv_heads) * kBS + r;
+      float ks, vs;
+      const uint2 kb = encode_slice<D, QDT, CDT>(ab + C::kOffNew, lane, ks);
+      const uint2 vb = encode_slice<D, QDT, CDT>(ab + C::kOffNew + D * 2, lane, vs);
+      const int off = C::kCode8 ? r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4
+                                : (lane >> 4) * 2048 + r * 128 + ((((lane & 15) >> 1) ^ (r & 7)) << 4) + (lane & 1) * 8;
+      store_slice<D, CDT>(tiles + st * C::kKV + off, kb);
+      store_slice<D, CDT>(tiles + st * C::kKV + C::kTile + off, vb);
+      constexpr int B = slice_bytes<D, CDT>();
+      // the caches are read-only everywhere else in the kernel
+      store_slice<D, CDT>(const_cast<uint8_t *>(p.k_cache) + grow * (B * 32) + lane * B, kb);
+      store_slice<D, CDT>(const_cast<uint8_t *>(p.v_cache) + grow * (B * 32) + lane * B, vb);
+      if constexpr (C::kCode8) {
+        if (lane == 0) {
+          float *sab = reinterpret_cast<float *>(aux + st * C::kAux);
+          sab[r] = ks;
+          sab[kBS + r] = vs;
+          const_cast<float *>(p.k_scale)[grow] = ks;
+          const_cast<float *>(p.v_scale)[grow] = vs;
+        }
+      }
+      __syncwarp();
+    }
 
     if (d.x >= 0) {
       // ---- S^T = K Q^T: lane rows g and g + 8, head columns 2 q4, 2 q4 + 1 ----

@@ -1,11 +1,12 @@
-// Decode step executor: host block manager and every layer's copy / append /
-// decode launches in a single native call, with no separate metadata transfer.
+// Decode step executor: host block manager and every layer's launches in a
+// single native call, with no separate metadata transfer.
 //
 // The step's metadata (slot mapping, copy pairs, lengths, block tables) is
-// written to page-locked host staging, which kernels read in place: layer 0's
-// block copies and append read it directly, and layer 0's append also copies
-// it to device memory for the later layers and the decode kernels.  Staging
-// and device metadata are double-buffered; half h is rewritten only after the
+// written to page-locked host staging, which kernels read in place: the
+// block copies and layer 0's decode read it directly, and with more layers
+// one small kernel copies it to device memory for layers 1...  Each layer is
+// one launch of the decode kernel with the append fused in.  Staging and
+// device metadata are double-buffered; half h is rewritten only after the
 // kernels of the step that last used it are done (one event per half).
 #include <cuda_runtime.h>
 
@@ -190,38 +191,37 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   auto scale_ptr = [&](float *base, int32_t l) {
     return base ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(base) + l * P.scale_layer_stride) : nullptr;
   };
-  for (int32_t l = 0; l < P.num_layers; ++l) {
-    // layer 0 reads the staging in place; its append copies it to Dh for the rest
-    const int32_t *meta = l == 0 ? Hd : Dh;
-    uint8_t *kc = layer_ptr(P.k_cache, P.cache_layer_stride, l);
-    uint8_t *vc = layer_ptr(P.v_cache, P.cache_layer_stride, l);
-    float *ks = scale_ptr(P.k_scale, l), *vs = scale_ptr(P.v_scale, l);
-    if (ncow) {
-      pkv::CopyArgs c{kc, vc, ks, vs, meta + n, meta + 2 * n, ncow, P.num_kv_heads, P.head_dim, P.cache_dtype,
-                      P.num_blocks, d_error, cs};
+  // Layer 0 reads the staging in place; with more layers one small kernel
+  // copies it to Dh for the others.
+  if (P.num_layers > 1) {
+    s = pkv::copy_meta_unchecked(Hd, Dh, ints, cs);
+    if (s != PKV_OK) return s;
+  }
+  if (ncow) {  // copy-on-write: every layer's shared blocks, before any append writes into the copies
+    for (int32_t l = 0; l < P.num_layers; ++l) {
+      pkv::CopyArgs c{layer_ptr(P.k_cache, P.cache_layer_stride, l), layer_ptr(P.v_cache, P.cache_layer_stride, l),
+                      scale_ptr(P.k_scale, l), scale_ptr(P.v_scale, l), Hd + n, Hd + 2 * n, ncow,
+                      P.num_kv_heads, P.head_dim, P.cache_dtype, P.num_blocks, d_error, cs};
       s = pkv::copy_blocks_unchecked(c);
       if (s != PKV_OK) return s;
     }
-    pkv::AppendArgs a{layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l), P.q_dtype, n,
-                      P.num_kv_heads, P.head_dim, meta, kc, vc, P.cache_dtype, ks, vs, P.num_blocks, d_error, cs,
-                      l == 0 ? Hd : nullptr, l == 0 ? Dh : nullptr, l == 0 ? ints : 0};
-    s = pkv::append_unchecked(a);
-    if (s != PKV_OK) return s;
   }
   if (attn_begin) {
     e = cudaEventRecord(static_cast<cudaEvent_t>(attn_begin), cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");
   }
   for (int32_t l = 0; l < P.num_layers; ++l) {
-    // A decode reads the lengths and tables before it waits for the kernel
-    // launched just before it, so it may start early (programmatic launch).
-    // With one layer that kernel is the append that copies them to Dh, so
-    // that decode reads them from the staging instead.
-    const bool from_staging = l == 0 && P.num_layers == 1;
-    const int32_t *t_lens = from_staging ? Hd + 3 * n : d_lens;
-    const int32_t *t_tables = from_staging ? Hd + 4 * n : d_tables;
-    s = pkv::attention_decode(true, layer_ptr(out, out_layer_stride, l), out_dtype,
-                              layer_ptr(q, q_layer_stride, l), P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
+    // Each layer is one launch: the new token's K/V rows are written by the
+    // warp that owns each sequence's last tile, then the query attends.  A
+    // decode reads the lengths and tables before it waits for the kernel
+    // launched just before it, so it may start early (programmatic launch):
+    // layer 0 reads them from the staging, later layers from Dh, which the
+    // copy kernel finished before layer 0 got past its wait.
+    const int32_t *t_lens = l == 0 ? Hd + 3 * n : d_lens;
+    const int32_t *t_tables = l == 0 ? Hd + 4 * n : d_tables;
+    s = pkv::attention_decode(true, layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l),
+                              layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l),
+                              P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
                               layer_ptr(P.v_cache, P.cache_layer_stride, l), P.cache_dtype, scale_ptr(P.k_scale, l),
                               scale_ptr(P.v_scale, l), t_tables, mb, t_lens, max_len, n, P.num_q_heads,
                               P.num_kv_heads, P.head_dim, P.num_blocks, scale, st->workspace, st->workspace_bytes,
