@@ -95,9 +95,11 @@ pkv_status pkv_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *
                          pkv_bm **out);
 void pkv_bm_destroy(pkv_bm *bm);
 
-/* Take one block from the free list (its count becomes 1). */
+/* Take one block from the free list (its count becomes 1); with the prefix
+ * cache on and the free list empty, evict a cached block (see below). */
 pkv_status kv_block_alloc(pkv_bm *bm, int32_t *block_id);
-/* Drop one reference; at 0 the block joins the tail of the free list. */
+/* Drop one reference; at 0 the block joins the tail of the free list (or,
+ * if it is registered in the prefix cache, stays cached). */
 pkv_status kv_block_free(pkv_bm *bm, int32_t block_id);
 
 /* New empty sequence; seq_id must not exist. */
@@ -131,12 +133,66 @@ pkv_status pkv_seq_append_slots(pkv_bm *bm, const int64_t *seq_ids, int32_t n,
 pkv_status pkv_build_block_tables(const pkv_bm *bm, const int64_t *seq_ids, int32_t n,
                                   int32_t max_blocks, int32_t *tables, int32_t *context_lens);
 
+/* Blocks a request can take: the free list plus cached, unreferenced blocks. */
 int32_t pkv_bm_num_free(const pkv_bm *bm);
 int32_t pkv_bm_num_blocks(const pkv_bm *bm);
 /* The free list in FIFO order: writes min(cap, free) ids to out, *n = free. */
 pkv_status pkv_bm_free_list(const pkv_bm *bm, int32_t *out, int32_t cap, int32_t *n);
 pkv_status pkv_bm_refcount(const pkv_bm *bm, int32_t block_id, int32_t *count);
 pkv_status pkv_seq_len(const pkv_bm *bm, int64_t seq_id, int32_t *len);
+
+/* ------------------------------------------------------------------------ */
+/* Automatic prefix caching ("KV Cache优化实战" §5.2: cached blocks keyed by */
+/* a content hash, reused block by block when a new request's prefix        */
+/* matches token for token; "企业官网建设流程全解析" §6.2: the key covers    */
+/* the model, the token ids and the configuration; §6.3: eviction follows   */
+/* the hash chain, since a block's later tokens depend on earlier ones).    */
+/*                                                                          */
+/* Only full blocks are cached.  Block j of a prompt is keyed by the chain  */
+/* h_j = pkv_block_hash(h_{j-1}, tokens[16j .. 16j+16), config_key),        */
+/* h_{-1} = 0; a hit also compares the stored token ids.  A registered      */
+/* block whose references drop to 0 stays cached and counts as free         */
+/* capacity; the free list is used first, then the cached unreferenced      */
+/* block with no cached child is evicted (least recently used -- by the     */
+/* admit, commit or release call that last touched it --, then the deepest, */
+/* then the lowest id), so no cached block loses a block it depends on.     */
+/* ------------------------------------------------------------------------ */
+
+/* FNV-1a 64 (offset basis 0xcbf29ce484222325, prime 0x100000001b3) over
+ * parent_hash (8 bytes little-endian), tokens[0..16) (4 bytes each,
+ * little-endian two's complement) and config_key (8 bytes little-endian). */
+uint64_t pkv_block_hash(uint64_t parent_hash, const int32_t *tokens, uint64_t config_key);
+
+/* Turn the prefix cache on (once per block manager); config_key stands for
+ * the model and the settings that change the cached K/V. */
+pkv_status pkv_bm_enable_prefix_cache(pkv_bm *bm, uint64_t config_key);
+
+/* Create seq_id for a prompt of num_tokens token ids (host int32) and map
+ * the longest chain of cached blocks that matches it, at most
+ * (num_tokens - 1) / 16 blocks so that at least one prompt token is
+ * computed.  Each mapped block gains a reference.  *num_cached = tokens
+ * mapped (the sequence's length, a multiple of 16); the caller appends and
+ * writes the rest of the prompt. */
+pkv_status pkv_seq_admit(pkv_bm *bm, int64_t seq_id, const int32_t *tokens, int32_t num_tokens,
+                         int32_t *num_cached);
+
+/* Register the full blocks among the first num_tokens tokens of seq_id
+ * (num_tokens <= its length; tokens are its token ids, host int32) once
+ * their K/V are written.  Registration follows the chain from block 0 and
+ * stops at the first block whose key is already held by another block (that
+ * block and the rest stay private).  *num_registered (may be NULL) = blocks
+ * newly registered. */
+pkv_status pkv_seq_commit_prefix(pkv_bm *bm, int64_t seq_id, const int32_t *tokens, int32_t num_tokens,
+                                 int32_t *num_registered);
+
+typedef struct {
+  int64_t lookups;    /* full prompt blocks looked up by pkv_seq_admit */
+  int64_t hits;       /* of those, reused */
+  int64_t evictions;  /* cached blocks evicted to serve allocations */
+  int64_t registered; /* blocks in the cache now */
+  int64_t evictable;  /* of those, unreferenced */
+} pkv_prefix_stats;
+pkv_status pkv_prefix_cache_stats(const pkv_bm *bm, pkv_prefix_stats *out);
 
 /* ------------------------------------------------------------------------ */
 /* Sizing ("KV Cache优化实战" §2.1: bytes = 2 x layers x kv_heads x head_dim */

@@ -90,6 +90,11 @@ _PROTOS = {
     "paged_attention_decode_static": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, C.c_int, _vp, _vp, _vp,
                                                 C.c_int32, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                                 C.c_int32, C.c_int32, C.c_float, _vp, _vp]),
+    "pkv_block_hash": (C.c_uint64, [C.c_uint64, _i32p, C.c_uint64]),
+    "pkv_bm_enable_prefix_cache": (C.c_int, [_vp, C.c_uint64]),
+    "pkv_seq_admit": (C.c_int, [_vp, C.c_int64, _i32p, C.c_int32, _i32p]),
+    "pkv_seq_commit_prefix": (C.c_int, [_vp, C.c_int64, _i32p, C.c_int32, _i32p]),
+    "pkv_prefix_cache_stats": (C.c_int, [_vp, C.c_void_p]),
     "pkv_stepper_host_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
     "pkv_stepper_device_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
     "pkv_stepper_create": (C.c_int, [C.POINTER(PoolDesc), C.c_int32, C.c_int32, _vp, C.c_size_t, _vp, C.c_size_t,
@@ -249,6 +254,45 @@ def pkv_kv_bytes(layers, kv_heads, head_dim, tokens, cache_dtype) -> int:
 
 def pkv_pool_blocks(budget_bytes, layers, kv_heads, head_dim, cache_dtype) -> int:
     return int(load().pkv_pool_blocks(budget_bytes, layers, kv_heads, head_dim, _dt(cache_dtype)))
+
+
+# ---- prefix cache --------------------------------------------------------------
+class PrefixStats(C.Structure):
+    _fields_ = [("lookups", C.c_int64), ("hits", C.c_int64), ("evictions", C.c_int64),
+                ("registered", C.c_int64), ("evictable", C.c_int64)]
+
+
+def pkv_block_hash(parent_hash: int, tokens, config_key: int) -> int:
+    t = _i32(tokens)
+    if t.size != BLOCK_SIZE:
+        raise ValueError("a block hash takes exactly 16 token ids")
+    return int(load().pkv_block_hash(parent_hash & 0xFFFFFFFFFFFFFFFF, _ptr(t, C.c_int32),
+                                     config_key & 0xFFFFFFFFFFFFFFFF))
+
+
+def pkv_bm_enable_prefix_cache(bm, config_key: int = 0) -> None:
+    _check(load().pkv_bm_enable_prefix_cache(bm, config_key & 0xFFFFFFFFFFFFFFFF), "pkv_bm_enable_prefix_cache")
+
+
+def pkv_seq_admit(bm, seq_id, tokens) -> int:
+    t = _i32(tokens)
+    out = C.c_int32()
+    _check(load().pkv_seq_admit(bm, int(seq_id), _ptr(t, C.c_int32), t.size, C.byref(out)), "pkv_seq_admit")
+    return out.value
+
+
+def pkv_seq_commit_prefix(bm, seq_id, tokens) -> int:
+    t = _i32(tokens)
+    out = C.c_int32()
+    _check(load().pkv_seq_commit_prefix(bm, int(seq_id), _ptr(t, C.c_int32), t.size, C.byref(out)),
+           "pkv_seq_commit_prefix")
+    return out.value
+
+
+def pkv_prefix_cache_stats(bm) -> dict:
+    st = PrefixStats()
+    _check(load().pkv_prefix_cache_stats(bm, C.byref(st)), "pkv_prefix_cache_stats")
+    return {k: int(getattr(st, k)) for k, _ in PrefixStats._fields_}
 
 
 # ---- device calls --------------------------------------------------------------

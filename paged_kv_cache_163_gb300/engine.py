@@ -117,6 +117,25 @@ class PagedKVCache:
     def seq_len(self, seq: int) -> int:
         return capi.pkv_seq_len(self.bm, seq)
 
+    # -- prefix cache --------------------------------------------------------------
+    def enable_prefix_cache(self, config_key: int = 0):
+        """Key full blocks by their token ids so later requests can reuse them."""
+        capi.pkv_bm_enable_prefix_cache(self.bm, config_key)
+
+    def admit(self, seq: int, tokens) -> int:
+        """Create `seq` for a prompt and map its longest cached prefix; returns the tokens mapped.
+
+        The caller appends the K/V rows of the remaining prompt tokens, then commits.
+        """
+        return capi.pkv_seq_admit(self.bm, seq, tokens)
+
+    def commit(self, seq: int, tokens) -> int:
+        """Register the full blocks of `seq`'s first len(tokens) tokens; returns how many."""
+        return capi.pkv_seq_commit_prefix(self.bm, seq, tokens)
+
+    def prefix_stats(self) -> dict:
+        return capi.pkv_prefix_cache_stats(self.bm)
+
     # -- metadata upload ---------------------------------------------------------
     def _upload(self, parts, stream):
         """Copy int32 host arrays to the device in one transfer; returns device views."""

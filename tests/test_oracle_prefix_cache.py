@@ -165,6 +165,19 @@ def test_duplicate_content_stays_private():
     assert list(a.free)[-2:] == t1           # never registered: back to the FIFO
 
 
+def test_commit_stops_at_a_duplicate_block():
+    base = _prompt(48, 12)
+    a = PrefixCachingAllocator(10)
+    for s in (0, 1):
+        a.create(s)
+        a.append_slots([s] * 48)
+    assert a.commit(0, base[:16]) == 1       # seq 0 registers only its first block
+    assert a.commit(1, base) == 0            # seq 1's first block duplicates it: nothing registered
+    first = a.tables[0][0]
+    a.free_seq(0)                            # seq 0's blocks: the registered one stays cached, a leaf
+    assert a.reg.keys() == {first} and a._victim() == first
+
+
 def test_random_trace_invariants():
     rng = random.Random(11)
     prompts = [_prompt(rng.randrange(1, 120), 100 + i) for i in range(6)]
@@ -193,11 +206,16 @@ def test_random_trace_invariants():
         held = sum(a.refcount)
         assert held == sum(len(t) for t in a.tables.values())
         assert len(a.free) + len(a._evictable()) + sum(1 for r in a.refcount if r > 0) == a.num_blocks
-        # a registered block's parent is registered too (no orphaned chain)
+        # a registered block's parent is registered too (no orphaned chain), and
+        # whoever holds a block holds its parent
         for b, (h, parent, depth, _) in a.reg.items():
             assert a.by_hash[h] == b
             assert (parent == -1) == (depth == 0)
             if parent >= 0:
                 assert parent in a.reg
+                assert a.refcount[parent] >= a.refcount[b]
+                assert all(t[depth - 1] == parent for t in a.tables.values() if len(t) > depth and t[depth] == b)
+        if a._evictable():
+            assert any(a.children[b] == 0 for b in a._evictable())
         for b in range(a.num_blocks):
             assert a.children[b] == sum(1 for r in a.reg.values() if r[1] == b)
