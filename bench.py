@@ -72,6 +72,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cache-dtype", choices=["fp8_e4m3", "fp8_e5m2", "int8"], default=None,
                     help="swap the workload's cache for this one-byte type (same shapes and values)")
+    ap.add_argument("--block-size", type=int, choices=[16, 32], default=16,
+                    help="tokens per physical block (the pool is sized for it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
@@ -134,6 +136,14 @@ def step_accounting(w: wl.Workload, step: int):
             "roofline_bytes": kv_unique + q_bytes + table_bytes + lens_bytes}
 
 
+def kv_utilisation(w: wl.Workload) -> dict:
+    """Token slots held that hold a token, for the workload's lengths (paged blocks vs max-length reservation)."""
+    from paged_kv_cache_163_gb300 import utilisation as ut
+    lens = [int(x) for x in w.context_lens]
+    return {"paged_bs16": round(ut.paged(lens, 16), 4), "paged_bs32": round(ut.paged(lens, 32), 4),
+            "prealloc_max_len": round(ut.prealloc(lens, w.max_context_len), 4), "max_len": w.max_context_len}
+
+
 def decode_kernel_name(w: wl.Workload, kind: str) -> str:
     """The decode kernel a call runs: tensor cores for head_dim 128 unless 'simt' is forced."""
     return "paged_decode_mma_kernel" if w.head_dim == 128 and kind != "simt" else "paged_decode_kernel"
@@ -161,9 +171,10 @@ class L2Flush:
 def workload_config(w: wl.Workload, name: str, extra=None):
     cfg = {"workload": name, "description": w.description, "num_seqs": w.num_seqs,
            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-           "layers": w.num_layers, "q_dtype": w.q_dtype, "cache_dtype": w.cache_dtype, "block_size": 16,
+           "layers": w.num_layers, "q_dtype": w.q_dtype, "cache_dtype": w.cache_dtype,
            "context_tokens": int(w.context_lens.sum()), "max_context_len": w.max_context_len,
-           "seed": w.seed, "l2": "flushed between timed steps: 256 MiB write, then 256 MiB read of another buffer"}
+           "seed": w.seed, "block_size": w.block_size,
+           "l2": "flushed between timed steps: 256 MiB write, then 256 MiB read of another buffer"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -251,7 +262,8 @@ def run_ours(args, world, rank, local):
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
     attn_steps = max(3, min(args.steps, 30))
     total_steps = args.warmup + args.steps + attn_steps + e2e_steps
-    w = wl.make(wid, extra_steps=max(total_steps, CPU_MAX_STEPS) + 1, cache_dtype=args.cache_dtype)
+    w = wl.make(wid, extra_steps=max(total_steps, CPU_MAX_STEPS) + 1, cache_dtype=args.cache_dtype,
+                block_size=args.block_size)
     cache = play.new_cache(w, device=dev)
     play.prefill(w, cache, device=dev)
     torch.cuda.synchronize()
@@ -324,6 +336,8 @@ def run_ours(args, world, rank, local):
     per_launch_s = t_attn / (attn_steps * w.num_layers)
     achieved = per_launch_bytes / per_launch_s / 1e9
     traffic_key = args.workload if args.cache_dtype is None else f"{args.workload}:{args.cache_dtype}"
+    if args.block_size != 16:
+        traffic_key += f":bs{args.block_size}"
     traffic = NCU_TRAFFIC.get((traffic_key, kernel_hash())) if args.kernel == "auto" else None
     value = whole_job_rate(world, kv_total, t_total) / 1e9
     result = {
@@ -355,6 +369,7 @@ def run_ours(args, world, rank, local):
                      "launch_us": round(per_launch_s * 1e6, 3)},
         "gpu_launches": int(launches),
         "clocks": clk,
+        "kv_utilisation": kv_utilisation(w),
     }
     if e2e is not None:
         result["e2e"] = e2e
@@ -478,7 +493,8 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     wid = WORKLOADS[args.workload]
-    w = wl.make(wid, extra_steps=max(args.warmup + args.steps + 1, CPU_MAX_STEPS + 1), cache_dtype=args.cache_dtype)
+    w = wl.make(wid, extra_steps=max(args.warmup + args.steps + 1, CPU_MAX_STEPS + 1), cache_dtype=args.cache_dtype,
+                block_size=args.block_size)
     seqs = sample_seqs(w, 3000 if w.cache_dtype != "fp8_e4m3" else 17000)
     o = oracle_sample_state(w, seqs, max_steps=args.warmup + args.steps + 1)
     oracle_steps(w, o, seqs, 0, 0.0, max_steps=args.warmup)

@@ -26,10 +26,12 @@
  *    offending access; it never traps.
  *  - Device arrays are dense and row-major in the shapes stated, and every
  *    device pointer must be 16-byte aligned.
- *  - Cache layout, per layer: k_cache, v_cache [num_blocks][num_kv_heads][16][head_dim];
- *    one-byte caches (FP8_E4M3, FP8_E5M2, INT8) also have scales k_scale,
- *    v_scale float32 [num_blocks][num_kv_heads][16].
- *    Token n of a sequence lives at slot table[n / 16] * 16 + n % 16.
+ *  - Cache layout, per layer: k_cache, v_cache
+ *    [num_blocks][num_kv_heads][block_size][head_dim]; one-byte caches
+ *    (FP8_E4M3, FP8_E5M2, INT8) also have scales k_scale, v_scale float32
+ *    [num_blocks][num_kv_heads][block_size].  block_size is 16 or 32.
+ *    Token n of a sequence lives at slot
+ *    table[n / block_size] * block_size + n % block_size.
  *  - Several layers are several calls with per-layer cache pointers.
  *  - Not thread-safe per block manager handle.
  */
@@ -71,12 +73,17 @@ typedef enum {
 } pkv_dtype;
 
 /* Bits a kernel ORs into *d_error. */
-#define PKV_DEVERR_BAD_SLOT 1        /* append: slot >= num_blocks * 16 */
+#define PKV_DEVERR_BAD_SLOT 1        /* append: slot >= num_blocks * block_size */
 #define PKV_DEVERR_BAD_BLOCK 2       /* copy / decode: block id outside [0, num_blocks) */
-#define PKV_DEVERR_BAD_CONTEXT_LEN 4 /* decode: context_len < 0 or > max_blocks_per_seq * 16 */
+#define PKV_DEVERR_BAD_CONTEXT_LEN 4 /* decode: context_len < 0 or > max_blocks_per_seq * block_size */
 #define PKV_DEVERR_WAIT_TIMEOUT 8    /* decode: a staging wait ran out its iteration limit */
 
+/* Tokens per physical block ("KV Cache 与 vLLM" §3.1: 16 by default; §4.2
+ * and "KV Cache优化实战" §7.5 treat it as a tuning knob).  Pools, tables and
+ * the device calls take a block_size of 16 (PKV_BLOCK_SIZE) or 32; the
+ * kernels work on 16-token tiles, two per 32-token block. */
 #define PKV_BLOCK_SIZE 16
+#define PKV_BLOCK_SIZE_32 32
 #define PKV_MAX_SEQS_PER_CALL 1024   /* paged_attention_decode batch limit */
 
 /* ------------------------------------------------------------------------ */
@@ -88,7 +95,7 @@ typedef enum {
 /* ------------------------------------------------------------------------ */
 typedef struct pkv_bm pkv_bm;
 
-/* num_blocks > 0; block_size must be 16; alloc_order (may be NULL) is a
+/* num_blocks > 0; block_size 16 or 32; alloc_order (may be NULL) is a
  * permutation of 0..num_blocks-1 copied by the call.  *out owns host memory
  * released by pkv_bm_destroy. */
 pkv_status pkv_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *alloc_order,
@@ -136,6 +143,7 @@ pkv_status pkv_build_block_tables(const pkv_bm *bm, const int64_t *seq_ids, int3
 /* Blocks a request can take: the free list plus cached, unreferenced blocks. */
 int32_t pkv_bm_num_free(const pkv_bm *bm);
 int32_t pkv_bm_num_blocks(const pkv_bm *bm);
+int32_t pkv_bm_block_size(const pkv_bm *bm);
 /* The free list in FIFO order: writes min(cap, free) ids to out, *n = free. */
 pkv_status pkv_bm_free_list(const pkv_bm *bm, int32_t *out, int32_t cap, int32_t *n);
 pkv_status pkv_bm_refcount(const pkv_bm *bm, int32_t block_id, int32_t *count);
@@ -148,6 +156,7 @@ pkv_status pkv_seq_len(const pkv_bm *bm, int64_t seq_id, int32_t *len);
 /* the model, the token ids and the configuration; §6.3: eviction follows   */
 /* the hash chain, since a block's later tokens depend on earlier ones).    */
 /*                                                                          */
+/* Needs a block manager with 16-token blocks.                              */
 /* Only full blocks are cached.  Block j of a prompt is keyed by the chain  */
 /* h_j = pkv_block_hash(h_{j-1}, tokens[16j .. 16j+16), config_key),        */
 /* h_{-1} = 0; a hit also compares the stored token ids.  A registered      */
@@ -201,9 +210,10 @@ pkv_status pkv_prefix_cache_stats(const pkv_bm *bm, pkv_prefix_stats *out);
 /* ------------------------------------------------------------------------ */
 int64_t pkv_kv_bytes(int32_t layers, int32_t kv_heads, int32_t head_dim, int64_t tokens,
                      pkv_dtype cache_dtype);
-/* Whole blocks a byte budget buys for all layers' K, V (and scales). */
+/* Whole blocks of block_size (16 or 32) tokens a byte budget buys for all
+ * layers' K, V (and scales). */
 int64_t pkv_pool_blocks(int64_t budget_bytes, int32_t layers, int32_t kv_heads, int32_t head_dim,
-                        pkv_dtype cache_dtype);
+                        pkv_dtype cache_dtype, int32_t block_size);
 
 /* ------------------------------------------------------------------------ */
 /* Device calls                                                              */
@@ -217,7 +227,8 @@ int64_t pkv_pool_blocks(int64_t budget_bytes, int32_t layers, int32_t kv_heads, 
 pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                                 const int32_t *src, const int32_t *dst, int32_t num_pairs,
                                 int32_t num_kv_heads, int32_t head_dim, pkv_dtype cache_dtype,
-                                int32_t num_blocks, int32_t *d_error, pkv_stream_t stream);
+                                int32_t num_blocks, int32_t block_size, int32_t *d_error,
+                                pkv_stream_t stream);
 
 /* Reshape-and-cache ("KV Cache 与 vLLM" §1.3 append; "企业官网建设流程全解析"
  * §3.2): token t's rows k[t], v[t] ([num_kv_heads][head_dim], in_dtype
@@ -237,7 +248,7 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
 pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int32_t num_tokens,
                            int32_t num_kv_heads, int32_t head_dim, const int32_t *slot_mapping,
                            void *k_cache, void *v_cache, pkv_dtype cache_dtype, float *k_scale,
-                           float *v_scale, int32_t num_blocks, int32_t *d_error,
+                           float *v_scale, int32_t num_blocks, int32_t block_size, int32_t *d_error,
                            pkv_stream_t stream);
 
 /* Which decode kernel runs.  SIMT: CUDA-core dot products (any head_dim).
@@ -288,7 +299,7 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
                                   int32_t max_blocks_per_seq, const int32_t *context_lens,
                                   int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
                                   int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
-                                  float scale, void *workspace, size_t workspace_bytes,
+                                  int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
                                   int32_t *d_error, pkv_stream_t stream);
 
 /* Append and decode in one launch ("KV Cache 与 vLLM" §1.3: every step
@@ -307,7 +318,8 @@ pkv_status paged_attention_decode_append(void *out, pkv_dtype out_dtype, const v
                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
                                          const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                         int32_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                         int32_t num_blocks, int32_t block_size, float scale, void *workspace,
+                                         size_t workspace_bytes,
                                          int32_t *d_error, pkv_stream_t stream);
 
 /* Decode without a workspace argument, for callers that cannot allocate
@@ -334,7 +346,7 @@ pkv_status paged_attention_decode_static(void *out, pkv_dtype out_dtype, const v
                                          int32_t max_blocks_per_seq, const int32_t *context_lens,
                                          int32_t max_context_len, int32_t num_seqs,
                                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                         int32_t num_blocks, float scale, int32_t *d_error,
+                                         int32_t num_blocks, int32_t block_size, float scale, int32_t *d_error,
                                          pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
@@ -355,6 +367,7 @@ typedef struct {
   int64_t cache_layer_stride;
   float *k_scale, *v_scale;         /* one-byte caches only (else NULL); layer l at + l * scale_layer_stride bytes */
   int64_t scale_layer_stride;
+  int32_t block_size;               /* 16 or 32: must match the block manager's */
 } pkv_pool_desc;
 
 typedef struct pkv_stepper pkv_stepper;

@@ -48,7 +48,7 @@ class PoolDesc(C.Structure):
                 ("num_q_heads", C.c_int32), ("head_dim", C.c_int32), ("q_dtype", C.c_int),
                 ("cache_dtype", C.c_int), ("k_cache", C.c_void_p), ("v_cache", C.c_void_p),
                 ("cache_layer_stride", C.c_int64), ("k_scale", C.c_void_p), ("v_scale", C.c_void_p),
-                ("scale_layer_stride", C.c_int64)]
+                ("scale_layer_stride", C.c_int64), ("block_size", C.c_int32)]
 
 
 _i32p = C.POINTER(C.c_int32)
@@ -68,28 +68,31 @@ _PROTOS = {
     "pkv_build_block_tables": (C.c_int, [_vp, _i64p, C.c_int32, C.c_int32, _i32p, _i32p]),
     "pkv_bm_num_free": (C.c_int32, [_vp]),
     "pkv_bm_num_blocks": (C.c_int32, [_vp]),
+    "pkv_bm_block_size": (C.c_int32, [_vp]),
     "pkv_bm_free_list": (C.c_int, [_vp, _i32p, C.c_int32, _i32p]),
     "pkv_bm_refcount": (C.c_int, [_vp, C.c_int32, _i32p]),
     "pkv_seq_len": (C.c_int, [_vp, C.c_int64, _i32p]),
     "pkv_kv_bytes": (C.c_int64, [C.c_int32, C.c_int32, C.c_int32, C.c_int64, C.c_int]),
-    "pkv_pool_blocks": (C.c_int64, [C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int]),
+    "pkv_pool_blocks": (C.c_int64, [C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int, C.c_int32]),
     "paged_kv_copy_blocks": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32,
-                                       C.c_int, C.c_int32, _vp, _vp]),
+                                       C.c_int, C.c_int32, C.c_int32, _vp, _vp]),
     "paged_kv_append": (C.c_int, [_vp, _vp, C.c_int, C.c_int32, C.c_int32, C.c_int32, _vp, _vp, _vp,
-                                  C.c_int, _vp, _vp, C.c_int32, _vp, _vp]),
+                                  C.c_int, _vp, _vp, C.c_int32, C.c_int32, _vp, _vp]),
     "paged_attention_workspace_bytes": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int,
                                                   C.c_int, C.POINTER(C.c_size_t)]),
     "paged_attention_decode": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, C.c_int, _vp, _vp, _vp, C.c_int32,
                                          _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
-                                         C.c_int32, C.c_float, _vp, C.c_size_t, _vp, _vp]),
+                                         C.c_int32, C.c_int32, C.c_float, _vp, C.c_size_t, _vp, _vp]),
     # out, out_dtype, q, q_dtype, k_new, v_new, k_cache, v_cache, cache_dtype, k_scale, v_scale, tables,
-    # max_blocks, lens, max_len, num_seqs, hq, hkv, d, num_blocks, scale, workspace, bytes, d_error, stream
+    # max_blocks, lens, max_len, num_seqs, hq, hkv, d, num_blocks, block_size, scale, workspace, bytes,
+    # d_error, stream
     "paged_attention_decode_append": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, _vp, _vp, C.c_int, _vp, _vp,
                                                 _vp, C.c_int32, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
-                                                C.c_int32, C.c_int32, C.c_float, _vp, C.c_size_t, _vp, _vp]),
+                                                C.c_int32, C.c_int32, C.c_int32, C.c_float, _vp, C.c_size_t, _vp,
+                                                _vp]),
     "paged_attention_decode_static": (C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, C.c_int, _vp, _vp, _vp,
                                                 C.c_int32, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
-                                                C.c_int32, C.c_int32, C.c_float, _vp, _vp]),
+                                                C.c_int32, C.c_int32, C.c_int32, C.c_float, _vp, _vp]),
     "pkv_block_hash": (C.c_uint64, [C.c_uint64, _i32p, C.c_uint64]),
     "pkv_bm_enable_prefix_cache": (C.c_int, [_vp, C.c_uint64]),
     "pkv_seq_admit": (C.c_int, [_vp, C.c_int64, _i32p, C.c_int32, _i32p]),
@@ -252,8 +255,12 @@ def pkv_kv_bytes(layers, kv_heads, head_dim, tokens, cache_dtype) -> int:
     return int(load().pkv_kv_bytes(layers, kv_heads, head_dim, tokens, _dt(cache_dtype)))
 
 
-def pkv_pool_blocks(budget_bytes, layers, kv_heads, head_dim, cache_dtype) -> int:
-    return int(load().pkv_pool_blocks(budget_bytes, layers, kv_heads, head_dim, _dt(cache_dtype)))
+def pkv_pool_blocks(budget_bytes, layers, kv_heads, head_dim, cache_dtype, block_size=BLOCK_SIZE) -> int:
+    return int(load().pkv_pool_blocks(budget_bytes, layers, kv_heads, head_dim, _dt(cache_dtype), block_size))
+
+
+def pkv_bm_block_size(bm) -> int:
+    return int(load().pkv_bm_block_size(bm))
 
 
 # ---- prefix cache --------------------------------------------------------------
@@ -340,16 +347,16 @@ def paged_kv_copy_blocks(k_cache, v_cache, k_scale, v_scale, src, dst, num_pairs
     nb, hkv, bs, d = k_cache.shape
     n = src.numel() if num_pairs is None else num_pairs
     _check(load().paged_kv_copy_blocks(_dp(k_cache), _dp(v_cache), _dp(k_scale), _dp(v_scale), _dp(src),
-                                       _dp(dst), n, hkv, d, _cdt(k_cache, cache_dtype), nb, _dp(d_error),
+                                       _dp(dst), n, hkv, d, _cdt(k_cache, cache_dtype), nb, bs, _dp(d_error),
                                        _stream(stream)), "paged_kv_copy_blocks")
 
 
 def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None,
                     d_error=None, stream=None, cache_dtype=None) -> None:
     t, hkv, d = k.shape
-    nb = k_cache.shape[0]
+    nb, bs = k_cache.shape[0], k_cache.shape[2]
     _check(load().paged_kv_append(_dp(k), _dp(v), _dt(k.dtype), t, hkv, d, _dp(slot_mapping), _dp(k_cache),
-                                  _dp(v_cache), _cdt(k_cache, cache_dtype), _dp(k_scale), _dp(v_scale), nb,
+                                  _dp(v_cache), _cdt(k_cache, cache_dtype), _dp(k_scale), _dp(v_scale), nb, bs,
                                   _dp(d_error), _stream(stream)), "paged_kv_append")
 
 
@@ -368,12 +375,12 @@ def paged_attention_decode(out, q, k_cache, v_cache, k_scale, v_scale, block_tab
     b, hq, d = q.shape
     if num_seqs is not None:
         b = num_seqs
-    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    nb, hkv, bs = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     _check(load().paged_attention_decode(
         _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_cache), _dp(v_cache), _cdt(k_cache, cache_dtype),
         _dp(k_scale),
         _dp(v_scale), _dp(block_tables), block_tables.shape[-1], _dp(context_lens), int(max_context_len), b, hq,
-        hkv, d, nb, float(scale), _dp(workspace), workspace.numel() * workspace.element_size(),
+        hkv, d, nb, bs, float(scale), _dp(workspace), workspace.numel() * workspace.element_size(),
         _dp(d_error), _stream(stream)), "paged_attention_decode")
 
 
@@ -384,11 +391,11 @@ def paged_attention_decode_append(out, q, k_new, v_new, k_cache, v_cache, k_scal
     b, hq, d = q.shape
     if num_seqs is not None:
         b = num_seqs
-    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    nb, hkv, bs = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     _check(load().paged_attention_decode_append(
         _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_new), _dp(v_new), _dp(k_cache), _dp(v_cache),
         _cdt(k_cache, cache_dtype), _dp(k_scale), _dp(v_scale), _dp(block_tables), block_tables.shape[-1],
-        _dp(context_lens), int(max_context_len), b, hq, hkv, d, nb, float(scale), _dp(workspace),
+        _dp(context_lens), int(max_context_len), b, hq, hkv, d, nb, bs, float(scale), _dp(workspace),
         workspace.numel() * workspace.element_size(), _dp(d_error), _stream(stream)), "paged_attention_decode_append")
 
 
@@ -399,11 +406,11 @@ def paged_attention_decode_static(out, q, k_cache, v_cache, k_scale, v_scale, bl
     b, hq, d = q.shape
     if num_seqs is not None:
         b = num_seqs
-    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    nb, hkv, bs = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     _check(load().paged_attention_decode_static(
         _dp(out), _dt(out.dtype), _dp(q), _dt(q.dtype), _dp(k_cache), _dp(v_cache), _cdt(k_cache, cache_dtype),
         _dp(k_scale), _dp(v_scale), _dp(block_tables), block_tables.shape[-1], _dp(context_lens),
-        int(max_context_len), b, hq, hkv, d, nb, float(scale), _dp(d_error), _stream(stream)),
+        int(max_context_len), b, hq, hkv, d, nb, bs, float(scale), _dp(d_error), _stream(stream)),
         "paged_attention_decode_static")
 
 

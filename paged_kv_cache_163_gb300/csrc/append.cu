@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
                                                      uint8_t *__restrict__ v_cache,
                                                      float *__restrict__ k_scale,
                                                      float *__restrict__ v_scale,
-                                                     int32_t num_blocks, int32_t *err,
+                                                     int32_t num_blocks, int32_t bs, int32_t *err,
                                                      const int4 *__restrict__ meta_src,
                                                      int4 *__restrict__ meta_dst, int64_t meta_vecs) {
   // A decode launched after this kernel as a programmatic dependent may start
@@ -49,13 +49,13 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
   const int h = static_cast<int>(th - t * num_kv_heads);
   const int32_t slot = slot_mapping[t];
   if (slot < 0) return;
-  if (slot >= static_cast<int64_t>(num_blocks) * kBS) {
+  if (slot >= static_cast<int64_t>(num_blocks) * bs) {
     if (lane == 0) report(err, PKV_DEVERR_BAD_SLOT);
     return;
   }
-  const int64_t blk = slot / kBS;
-  const int off = slot % kBS;
-  const int64_t row = (blk * num_kv_heads + h) * kBS + off;  // index of the cache row
+  const int64_t blk = slot / bs;
+  const int off = slot % bs;
+  const int64_t row = (blk * num_kv_heads + h) * bs + off;  // index of the cache row
   append_row<D, IDT, CDT>((kind ? v : k) + th * D * 2, kind ? v_cache : k_cache, kind ? v_scale : k_scale, row,
                           lane);
 }
@@ -108,7 +108,7 @@ static cudaError_t launch_append(const AppendArgs &a) {
   append_kernel<D, IDT, CDT><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
       static_cast<const uint8_t *>(a.k), static_cast<const uint8_t *>(a.v), a.slot_mapping,
       a.num_tokens, a.num_kv_heads, static_cast<uint8_t *>(a.k_cache),
-      static_cast<uint8_t *>(a.v_cache), a.k_scale, a.v_scale, a.num_blocks, a.d_error,
+      static_cast<uint8_t *>(a.v_cache), a.k_scale, a.v_scale, a.num_blocks, a.block_size, a.d_error,
       reinterpret_cast<const int4 *>(a.meta_src), reinterpret_cast<int4 *>(a.meta_dst),
       a.meta_src ? (a.meta_ints + 3) / 4 : 0);
   return cudaGetLastError();
@@ -148,8 +148,8 @@ cudaError_t run_copy_blocks(const CopyArgs &a) {
   if (a.num_pairs == 0) return cudaSuccess;
   const bool code8 = is_code8(a.cache_dtype);
   const int esz = code8 ? 1 : 2;
-  const int64_t block_bytes = static_cast<int64_t>(a.num_kv_heads) * kBS * a.head_dim * esz;
-  const int32_t scale_elems = a.num_kv_heads * kBS;
+  const int64_t block_bytes = static_cast<int64_t>(a.num_kv_heads) * a.block_size * a.head_dim * esz;
+  const int32_t scale_elems = a.num_kv_heads * a.block_size;
   dim3 grid(a.num_pairs, 2);
   copy_blocks_kernel<<<grid, 256, 0, a.stream>>>(
       static_cast<uint8_t *>(a.k_cache), static_cast<uint8_t *>(a.v_cache),

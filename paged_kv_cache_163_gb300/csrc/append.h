@@ -18,6 +18,7 @@ struct AppendArgs {
   int32_t num_blocks;
   int32_t *d_error;
   cudaStream_t stream;
+  int32_t block_size;  // 16 or 32 tokens per physical block
   // Optional: the kernel also copies meta_ints int32 from meta_src (page-locked
   // host memory, read in place) to meta_dst (device), 16-byte vectors, with
   // both pointers 16-byte aligned and room for meta_ints rounded up to 4.
@@ -35,6 +36,7 @@ struct CopyArgs {
   int32_t num_blocks;
   int32_t *d_error;
   cudaStream_t stream;
+  int32_t block_size;  // 16 or 32 tokens per physical block
 };
 
 cudaError_t run_append(const AppendArgs &a);

@@ -127,8 +127,8 @@ pkv_status pkv_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *
                          pkv_bm **out) {
   if (!out) return fail(PKV_ERR_INVALID, "pkv_bm_create: out is NULL");
   if (num_blocks <= 0) return fail(PKV_ERR_INVALID, "pkv_bm_create: num_blocks must be > 0");
-  if (block_size != PKV_BLOCK_SIZE)
-    return fail(PKV_ERR_UNSUPPORTED, "pkv_bm_create: block_size must be 16");
+  if (block_size != PKV_BLOCK_SIZE && block_size != PKV_BLOCK_SIZE_32)
+    return fail(PKV_ERR_UNSUPPORTED, "pkv_bm_create: block_size must be 16 or 32");
   std::vector<char> seen(num_blocks, 0);
   if (alloc_order) {
     for (int32_t i = 0; i < num_blocks; ++i) {
@@ -282,6 +282,8 @@ int32_t pkv_bm_num_free(const pkv_bm *bm) {
 
 int32_t pkv_bm_num_blocks(const pkv_bm *bm) { return bm ? bm->num_blocks : -1; }
 
+int32_t pkv_bm_block_size(const pkv_bm *bm) { return bm ? bm->block_size : -1; }
+
 pkv_status pkv_bm_free_list(const pkv_bm *bm, int32_t *out, int32_t cap, int32_t *n) {
   if (!bm || !n || cap < 0 || (cap > 0 && !out))
     return fail(PKV_ERR_INVALID, "pkv_bm_free_list: bad argument");
@@ -331,8 +333,9 @@ int64_t pkv_kv_bytes(int32_t layers, int32_t kv_heads, int32_t head_dim, int64_t
 }
 
 int64_t pkv_pool_blocks(int64_t budget_bytes, int32_t layers, int32_t kv_heads, int32_t head_dim,
-                        pkv_dtype cache_dtype) {
-  int64_t per_block = pkv_kv_bytes(layers, kv_heads, head_dim, PKV_BLOCK_SIZE, cache_dtype);
+                        pkv_dtype cache_dtype, int32_t block_size) {
+  if (block_size != PKV_BLOCK_SIZE && block_size != PKV_BLOCK_SIZE_32) return -1;
+  int64_t per_block = pkv_kv_bytes(layers, kv_heads, head_dim, block_size, cache_dtype);
   if (budget_bytes < 0 || per_block <= 0) return -1;
   return budget_bytes / per_block;
 }
@@ -350,6 +353,8 @@ uint64_t pkv_block_hash(uint64_t parent_hash, const int32_t *tokens, uint64_t co
 pkv_status pkv_bm_enable_prefix_cache(pkv_bm *bm, uint64_t config_key) {
   if (!bm) return fail(PKV_ERR_INVALID, "pkv_bm_enable_prefix_cache: NULL handle");
   if (bm->cache_on) return fail(PKV_ERR_INVALID, "pkv_bm_enable_prefix_cache: already enabled");
+  if (bm->block_size != PKV_BLOCK_SIZE)
+    return fail(PKV_ERR_UNSUPPORTED, "pkv_bm_enable_prefix_cache: needs 16-token blocks");
   const size_t n = static_cast<size_t>(bm->num_blocks);
   bm->cache_on = true;
   bm->config_key = config_key;

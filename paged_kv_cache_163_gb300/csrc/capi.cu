@@ -210,9 +210,11 @@ pkv_decode_kernel pkv_get_decode_kernel(void) { return static_cast<pkv_decode_ke
 pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                                 const int32_t *src, const int32_t *dst, int32_t num_pairs,
                                 int32_t num_kv_heads, int32_t head_dim, pkv_dtype cache_dtype,
-                                int32_t num_blocks, int32_t *d_error, pkv_stream_t stream) {
+                                int32_t num_blocks, int32_t block_size, int32_t *d_error, pkv_stream_t stream) {
   if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0)
     return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: bad sizes");
+  if (block_size != PKV_BLOCK_SIZE && block_size != PKV_BLOCK_SIZE_32)
+    return fail(PKV_ERR_UNSUPPORTED, "paged_kv_copy_blocks: block_size must be 16 or 32");
   if (head_dim != 64 && head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "paged_kv_copy_blocks: head_dim must be 64 or 128");
   if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16 && !is_code8(cache_dtype))
@@ -224,7 +226,7 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
   if (is_code8(cache_dtype) && (!k_scale || !v_scale))
     return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: a one-byte cache needs k_scale and v_scale");
   CopyArgs a{k_cache, v_cache, k_scale, v_scale, src, dst, num_pairs, num_kv_heads,
-             head_dim, cache_dtype, num_blocks, d_error, reinterpret_cast<cudaStream_t>(stream)};
+             head_dim, cache_dtype, num_blocks, d_error, reinterpret_cast<cudaStream_t>(stream), block_size};
   cudaError_t e = run_copy_blocks(a);
   if (e != cudaSuccess) return cuda_fail(e, "paged_kv_copy_blocks");
   ++t_launches;
@@ -234,10 +236,12 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
 pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int32_t num_tokens,
                            int32_t num_kv_heads, int32_t head_dim, const int32_t *slot_mapping,
                            void *k_cache, void *v_cache, pkv_dtype cache_dtype, float *k_scale,
-                           float *v_scale, int32_t num_blocks, int32_t *d_error,
+                           float *v_scale, int32_t num_blocks, int32_t block_size, int32_t *d_error,
                            pkv_stream_t stream) {
   if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0)
     return fail(PKV_ERR_INVALID, "paged_kv_append: bad sizes");
+  if (block_size != PKV_BLOCK_SIZE && block_size != PKV_BLOCK_SIZE_32)
+    return fail(PKV_ERR_UNSUPPORTED, "paged_kv_append: block_size must be 16 or 32");
   if (head_dim != 64 && head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "paged_kv_append: head_dim must be 64 or 128");
   if (in_dtype != PKV_F16 && in_dtype != PKV_BF16)
@@ -252,7 +256,7 @@ pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int
     return fail(PKV_ERR_INVALID, "paged_kv_append: a one-byte cache needs k_scale and v_scale");
   AppendArgs a{k, v, in_dtype, num_tokens, num_kv_heads, head_dim, slot_mapping, k_cache, v_cache,
                cache_dtype, k_scale, v_scale, num_blocks, d_error,
-               reinterpret_cast<cudaStream_t>(stream)};
+               reinterpret_cast<cudaStream_t>(stream), block_size};
   cudaError_t e = run_append(a);
   if (e != cudaSuccess) return cuda_fail(e, "paged_kv_append");
   ++t_launches;
@@ -305,14 +309,18 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
                             const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,
                             const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
-                            float scale, void *workspace, size_t workspace_bytes, int32_t *d_error,
-                            pkv_stream_t stream) {
+                            int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
+                            int32_t *d_error, pkv_stream_t stream) {
   if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS_PER_CALL)
     return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: num_seqs must be in [0, 1024]");
   pkv_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
   if (s != PKV_OK) return s;
   if (max_blocks_per_seq < 0 || max_context_len < 0 || num_blocks <= 0)
     return fail(PKV_ERR_INVALID, "paged_attention_decode: bad sizes");
+  if (block_size != PKV_BLOCK_SIZE && block_size != PKV_BLOCK_SIZE_32)
+    return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: block_size must be 16 or 32");
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size >= (int64_t(1) << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: pool larger than 2^31 token rows");
   if (static_cast<int64_t>(num_seqs) * num_kv_heads > (1 << 24))
     return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: too many (sequence, KV head) pairs");
   if (out_dtype != PKV_F32 && out_dtype != q_dtype)
@@ -349,6 +357,8 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
   p.num_seqs = num_seqs;
   p.num_kv_heads = num_kv_heads;
   p.num_blocks = num_blocks;
+  p.block_size = block_size;
+  p.tiles_per_block = block_size / PKV_BLOCK_SIZE;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.ws_ctr = reinterpret_cast<uint32_t *>(ws);
   p.ws_ml = reinterpret_cast<float *>(ws + lay.ctr_bytes);
@@ -376,9 +386,7 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
 
   cudaError_t e;
   if (mma) {
-    const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
-    if (rows >= (int64_t(1) << 31))
-      return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: pool larger than 2^31 token rows");
+    const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
     const int esz = is_code8(cache_dtype) ? 1 : 2;
     CUtensorMap tmk, tmv;
     s = cache_tensor_map(k_cache, rows, esz, &tmk);
@@ -406,12 +414,12 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
                                   int32_t max_blocks_per_seq, const int32_t *context_lens,
                                   int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
                                   int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
-                                  float scale, void *workspace, size_t workspace_bytes,
+                                  int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
                                   int32_t *d_error, pkv_stream_t stream) {
   return pkv::attention_decode(false, nullptr, nullptr, out, out_dtype, q, q_dtype, k_cache, v_cache, cache_dtype,
                                k_scale, v_scale, block_tables, max_blocks_per_seq, context_lens, max_context_len,
-                               num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale, workspace,
-                               workspace_bytes, d_error, stream);
+                               num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
+                               workspace, workspace_bytes, d_error, stream);
 }
 
 pkv_status paged_attention_decode_append(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
@@ -420,14 +428,14 @@ pkv_status paged_attention_decode_append(void *out, pkv_dtype out_dtype, const v
                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
                                          const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                         int32_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
-                                         int32_t *d_error, pkv_stream_t stream) {
+                                         int32_t num_blocks, int32_t block_size, float scale, void *workspace,
+                                         size_t workspace_bytes, int32_t *d_error, pkv_stream_t stream) {
   if (num_seqs > 0 && (!k_new || !v_new))
     return fail(PKV_ERR_INVALID, "paged_attention_decode_append: NULL k_new or v_new");
   return pkv::attention_decode(false, k_new, v_new, out, out_dtype, q, q_dtype, k_cache, v_cache, cache_dtype,
                                k_scale, v_scale, block_tables, max_blocks_per_seq, context_lens, max_context_len,
-                               num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale, workspace,
-                               workspace_bytes, d_error, stream);
+                               num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
+                               workspace, workspace_bytes, d_error, stream);
 }
 
 pkv_status pkv_read_device_error(int32_t *d_error, int32_t *h_error, int32_t clear,

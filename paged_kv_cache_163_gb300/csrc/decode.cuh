@@ -110,7 +110,10 @@ __device__ __forceinline__ int find_seq(const int32_t *cum, int num_seqs, int hk
   return lo;
 }
 
-// Descriptor of one tile: x = physical block (-1 if invalid),
+// Descriptor of one 16-token tile: x = its row index in the pool divided by
+// 16, i.e. ((physical block * Hkv + KV head) * tiles per block + tile within
+// the block) (-1 if the block id is invalid); the tile's K rows start at
+// k_cache + x * 16 rows, its scales at scale + x * 16.
 // y = item << 7 | first << 6 | last << 5 | valid tokens.
 __device__ __forceinline__ int2 tile_desc(const DecodeParams &p, const int32_t *cum, int64_t t) {
   const int b = find_seq(cum, p.num_seqs, p.num_kv_heads, t);
@@ -120,13 +123,16 @@ __device__ __forceinline__ int2 tile_desc(const DecodeParams &p, const int32_t *
   const int lb = static_cast<int>(r - static_cast<int64_t>(kvh) * nb);
   const int L = __ldg(p.context_lens + b);
   const int ntok = min(kBS, L - lb * kBS);
-  int32_t blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + lb);
+  const int tpb = p.tiles_per_block;
+  const int32_t blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + lb / tpb);
+  int32_t x = -1;
   if (blk < 0 || blk >= p.num_blocks) {
     report(p.d_error, PKV_DEVERR_BAD_BLOCK);
-    blk = -1;
+  } else {
+    x = (blk * p.num_kv_heads + kvh) * tpb + lb % tpb;
   }
   const int item = b * p.num_kv_heads + kvh;
-  return make_int2(blk, (item << 7) | ((lb == 0) << 6) | ((lb == nb - 1) << 5) | ntok);
+  return make_int2(x, (item << 7) | ((lb == 0) << 6) | ((lb == nb - 1) << 5) | ntok);
 }
 
 // CTA prologue shared by the decode kernels, reading only the context lengths:
@@ -146,7 +152,7 @@ __device__ __forceinline__ void scan_blocks(const DecodeParams &p, int32_t *cum,
     if (s < p.num_seqs) {
       const int L = p.context_lens[s];
       if (L < 0 || L > p.max_context_len ||
-          static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBS) {
+          static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size) {
         report(p.d_error, PKV_DEVERR_BAD_CONTEXT_LEN);
       } else {
         nb = (L + kBS - 1) / kBS;
@@ -421,8 +427,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
       } else {
         mbar_arrive_expect_tx(bars + st, bytes);
         if (d.x >= 0) {
-          const int kvh = item % p.num_kv_heads;
-          const size_t tile = static_cast<size_t>(d.x) * p.num_kv_heads + kvh;
+          const size_t tile = static_cast<size_t>(d.x);
           bulk_g2s(sb, p.k_cache + tile * head_tile, C::kTile, bars + st, pol);
           bulk_g2s(sb + C::kOffV, p.v_cache + tile * head_tile, C::kTile, bars + st, pol);
           if constexpr (C::kScale > 0) {
@@ -562,7 +567,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
       // tile and into the cache for later steps.  No other warp reads this
       // tile, and its copy has landed, so nothing races.
       const int r = (d.y & 31) - 1;
-      const int64_t grow = (static_cast<int64_t>(d.x) * p.num_kv_heads + item % p.num_kv_heads) * kBS + r;
+      const int64_t grow = static_cast<int64_t>(d.x) * kBS + r;
       float kscl, vscl;
       const uint2 kb = encode_slice<D, QDT, CDT>(sb + C::kOffNew, lane, kscl);
       const uint2 vb = encode_slice<D, QDT, CDT>(sb + C::kOffNew + D * 2, lane, vscl);

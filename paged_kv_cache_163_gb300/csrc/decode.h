@@ -30,6 +30,8 @@ struct DecodeParams {
   int32_t num_seqs;
   int32_t num_kv_heads;
   int32_t num_blocks;
+  int32_t block_size;       // tokens per physical block: 16 or 32
+  int32_t tiles_per_block;  // 16-token tiles per physical block: 1 or 2
   float scale_log2;  // scale * log2(e)
   uint32_t *ws_ctr;  // [2][num_seqs * num_kv_heads] partials stored per item; bank epoch & 1
   uint32_t epoch;    // one value per decode call; consecutive calls alternate banks
@@ -115,7 +117,7 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
                             const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,
                             const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
-                            float scale, void *workspace, size_t workspace_bytes, int32_t *d_error,
-                            pkv_stream_t stream);
+                            int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
+                            int32_t *d_error, pkv_stream_t stream);
 
 }  // namespace pkv

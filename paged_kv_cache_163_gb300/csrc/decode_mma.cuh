@@ -165,8 +165,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       } else {
         mbar_arrive_expect_tx(bars + st, bytes);
         if (d.x >= 0) {
-          const int kvh = item % p.num_kv_heads;
-          const int64_t tile = static_cast<int64_t>(d.x) * p.num_kv_heads + kvh;
+          const int64_t tile = d.x;
           const int row = static_cast<int>(tile * kBS);
           if constexpr (C::kCode8) {
             tma_load_2d(tb, &tmk, 0, row, bars + st, pol);
@@ -316,7 +315,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       // tile (swizzled layout) and into the cache for later steps.  No other
       // warp reads this tile, and its copy has landed, so nothing races.
       const int r = (d.y & 31) - 1;
-      const int64_t grow = (static_cast<int64_t>(d.x) * p.num_kv_heads + item % p.num_kv_heads) * kBS + r;
+      const int64_t grow = static_cast<int64_t>(d.x) * kBS + r;
       float ks, vs;
       const uint2 kb = encode_slice<D, QDT, CDT>(ab + C::kOffNew, lane, ks);
       const uint2 vb = encode_slice<D, QDT, CDT>(ab + C::kOffNew + D * 2, lane, vs);

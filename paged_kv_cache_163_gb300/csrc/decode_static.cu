@@ -78,7 +78,8 @@ extern "C" pkv_status paged_attention_decode_static(
     const void *v_cache, pkv_dtype cache_dtype, const float *k_scale, const float *v_scale,
     const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
     int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-    int32_t head_dim, int32_t num_blocks, float scale, int32_t *d_error, pkv_stream_t stream) {
+    int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, int32_t *d_error,
+    pkv_stream_t stream) {
   size_t need = 0;
   pkv_status s = paged_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, q_dtype,
                                                  cache_dtype, &need);
@@ -94,6 +95,6 @@ extern "C" pkv_status paged_attention_decode_static(
   if (s != PKV_OK) return s;
   return paged_attention_decode(out, out_dtype, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
                                 block_tables, max_blocks_per_seq, context_lens, max_context_len, num_seqs,
-                                num_q_heads, num_kv_heads, head_dim, num_blocks, scale, ws,
+                                num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, ws,
                                 pkv::kStaticScratchBytes, d_error, stream);
 }

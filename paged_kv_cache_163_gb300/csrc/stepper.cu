@@ -72,6 +72,8 @@ pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32
                               pkv_stepper **out) {
   if (!pool || !out || max_seqs <= 0 || max_seqs > PKV_MAX_SEQS_PER_CALL || max_blocks_per_seq <= 0)
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: bad argument");
+  if (pool->block_size != PKV_BLOCK_SIZE && pool->block_size != PKV_BLOCK_SIZE_32)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_stepper_create: block_size must be 16 or 32");
   if (pool->num_layers <= 0 || pool->num_blocks <= 0 || pool->num_kv_heads <= 0 || !pool->k_cache ||
       !pool->v_cache || (pkv::is_code8(pool->cache_dtype) && (!pool->k_scale || !pool->v_scale)))
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: bad pool descriptor");
@@ -133,6 +135,8 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
                             pkv_stream_t stream) {
   if (!st || !bm || n < 0 || n > st->max_seqs || (n > 0 && (!seq_ids || !k_new || !v_new || !q || !out)))
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: bad argument");
+  if (pkv_bm_block_size(bm) != st->pool.block_size)
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: the block manager's block size differs from the pool's");
   if (num_cow) *num_cow = 0;
   if (n == 0) return PKV_OK;
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
@@ -152,7 +156,7 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     pkv_status s = pkv_seq_len(bm, seq_ids[i], &len);
     if (s != PKV_OK) return s;
     const int32_t after = len + 1;
-    const int32_t blocks = (after + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+    const int32_t blocks = (after + P.block_size - 1) / P.block_size;
     if (blocks > st->max_blocks)
       return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: a table would exceed max_blocks_per_seq");
     mb = std::max(mb, blocks);
@@ -201,7 +205,7 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     for (int32_t l = 0; l < P.num_layers; ++l) {
       pkv::CopyArgs c{layer_ptr(P.k_cache, P.cache_layer_stride, l), layer_ptr(P.v_cache, P.cache_layer_stride, l),
                       scale_ptr(P.k_scale, l), scale_ptr(P.v_scale, l), Hd + n, Hd + 2 * n, ncow,
-                      P.num_kv_heads, P.head_dim, P.cache_dtype, P.num_blocks, d_error, cs};
+                      P.num_kv_heads, P.head_dim, P.cache_dtype, P.num_blocks, d_error, cs, P.block_size};
       s = pkv::copy_blocks_unchecked(c);
       if (s != PKV_OK) return s;
     }
@@ -224,8 +228,8 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
                               P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
                               layer_ptr(P.v_cache, P.cache_layer_stride, l), P.cache_dtype, scale_ptr(P.k_scale, l),
                               scale_ptr(P.v_scale, l), t_tables, mb, t_lens, max_len, n, P.num_q_heads,
-                              P.num_kv_heads, P.head_dim, P.num_blocks, scale, st->workspace, st->workspace_bytes,
-                              d_error, stream);
+                              P.num_kv_heads, P.head_dim, P.num_blocks, P.block_size, scale, st->workspace,
+                              st->workspace_bytes, d_error, stream);
     if (s != PKV_OK) return s;
   }
   if (attn_end) {

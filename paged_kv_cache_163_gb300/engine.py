@@ -59,13 +59,14 @@ class _PinnedRing:
 
 class PagedKVCache:
     def __init__(self, *, num_layers: int, num_blocks: int, num_kv_heads: int, head_dim: int,
-                 cache_dtype: str, alloc_order=None, device="cuda", poison: bool = False):
+                 cache_dtype: str, alloc_order=None, device="cuda", poison: bool = False,
+                 block_size: int = capi.BLOCK_SIZE):
         import torch
-        self.num_layers, self.num_blocks = num_layers, num_blocks
+        self.num_layers, self.num_blocks, self.block_size = num_layers, num_blocks, block_size
         self.num_kv_heads, self.head_dim, self.cache_dtype = num_kv_heads, head_dim, cache_dtype
         self.device = torch.device(device)
-        self.bm = capi.pkv_bm_create(num_blocks, capi.BLOCK_SIZE, alloc_order)
-        shape = (num_layers, num_blocks, num_kv_heads, capi.BLOCK_SIZE, head_dim)
+        self.bm = capi.pkv_bm_create(num_blocks, block_size, alloc_order)
+        shape = (num_layers, num_blocks, num_kv_heads, block_size, head_dim)
         tdt = torch_dtype(cache_dtype)
         self.k = torch.empty(shape, dtype=tdt, device=self.device)
         self.v = torch.empty(shape, dtype=tdt, device=self.device)
@@ -194,7 +195,7 @@ class PagedKVCache:
     # -- decode ------------------------------------------------------------------
     def tables(self, seq_ids):
         lens = [self.seq_len(s) for s in seq_ids]
-        max_blocks = max(1, max((-(-L // capi.BLOCK_SIZE) for L in lens), default=1))
+        max_blocks = max(1, max((-(-L // self.block_size) for L in lens), default=1))
         tables, ctx = capi.pkv_build_block_tables(self.bm, seq_ids, max_blocks)
         return tables, ctx
 
@@ -262,7 +263,8 @@ class PagedKVCache:
             cache_layer_stride=self.k.stride(0) * kb,
             k_scale=self.k_scale.data_ptr() if self.k_scale is not None else None,
             v_scale=self.v_scale.data_ptr() if self.v_scale is not None else None,
-            scale_layer_stride=self.k_scale.stride(0) * 4 if self.k_scale is not None else 0)
+            scale_layer_stride=self.k_scale.stride(0) * 4 if self.k_scale is not None else 0,
+            block_size=self.block_size)
         self._stepper = capi.pkv_stepper_create(pool, n, max_blocks, host, dev, ws)
         self._stepper_bufs = (host, dev, ws)
         self._stepper_key = key
@@ -300,5 +302,5 @@ class PagedKVCache:
         return capi.pkv_read_device_error(self.err, clear=True, stream=self._stream(stream))
 
 
-def blocks_for(length: int) -> int:
-    return int(math.ceil(length / capi.BLOCK_SIZE))
+def blocks_for(length: int, block_size: int = capi.BLOCK_SIZE) -> int:
+    return int(math.ceil(length / block_size))

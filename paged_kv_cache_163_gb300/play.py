@@ -22,7 +22,7 @@ def new_cache(w: Workload, device="cuda", poison=False, alloc_order=None) -> Pag
     return PagedKVCache(num_layers=w.num_layers, num_blocks=w.num_blocks, num_kv_heads=w.num_kv_heads,
                         head_dim=w.head_dim, cache_dtype=w.cache_dtype,
                         alloc_order=w.alloc_order if alloc_order is None else alloc_order,
-                        device=device, poison=poison)
+                        device=device, poison=poison, block_size=w.block_size)
 
 
 def prefill(w: Workload, cache: PagedKVCache, device="cuda") -> None:

@@ -78,6 +78,7 @@ class Workload:
     seed: int = 0
     description: str = ""
     extra: dict = field(default_factory=dict)
+    block_size: int = BLOCK_SIZE  # tokens per physical block: 16 or 32
 
     @property
     def seq_ids(self):
@@ -173,13 +174,16 @@ def _blocks(lengths) -> int:
 
 
 def make(wid: int, *, extra_steps: int = 0, num_seqs: int | None = None,
-         cache_dtype: str | None = None) -> Workload:
+         cache_dtype: str | None = None, block_size: int = BLOCK_SIZE) -> Workload:
     """Workload 1..5.  ``extra_steps`` reserves pool room for that many more decode steps.
 
     ``cache_dtype`` swaps the cache for a one-byte type (same shapes, seeds
-    and values; the rows are quantised on append).
+    and values; the rows are quantised on append).  ``block_size`` 32 sizes
+    the pool in 32-token blocks (same lengths and values).
     """
     w = _make(wid, extra_steps=extra_steps, num_seqs=num_seqs)
+    if block_size != BLOCK_SIZE:
+        w = _resize_blocks(w, block_size, extra_steps)
     if cache_dtype is None or cache_dtype == w.cache_dtype:
         return w
     if cache_dtype not in ONE_BYTE_CACHES:
@@ -191,6 +195,25 @@ def make(wid: int, *, extra_steps: int = 0, num_seqs: int | None = None,
         name = w.name
         desc = f"{w.description}; cache swapped to {cache_dtype} + fp32 scales"
     return replace(w, name=f"{name}-{cache_dtype}", cache_dtype=cache_dtype, description=desc)
+
+
+def _resize_blocks(w: Workload, bs: int, extra_steps: int) -> Workload:
+    """The same workload on a pool of `bs`-token blocks (shuffled ids, or the interleave of workload 3)."""
+    g = _rng(w.seed, 3)
+    if w.prefix_len:
+        p = w.prefix_len
+        need = -(-p // bs) + int(sum(-(-(p % bs + int(L) - p + extra_steps) // bs) for L in w.context_lens))
+    else:
+        need = int(sum(-(-(int(L) + extra_steps) // bs) for L in w.context_lens))
+    if w.wid == 3:
+        per = -(-(int(w.context_lens.max()) + extra_steps) // bs)
+        order = np.array([j * w.num_seqs + s for s in range(w.num_seqs) for j in range(per)], dtype=np.int32)
+        nb = w.num_seqs * per
+    else:
+        nb = _pool(need)
+        order = g.permutation(nb).astype(np.int32)
+    return replace(w, block_size=bs, num_blocks=nb, alloc_order=order,
+                   name=f"{w.name}-bs{bs}", description=f"{w.description}; {bs}-token blocks")
 
 
 def _make(wid: int, *, extra_steps: int = 0, num_seqs: int | None = None) -> Workload:
@@ -245,17 +268,17 @@ def _make(wid: int, *, extra_steps: int = 0, num_seqs: int | None = None) -> Wor
 
 def custom(name, *, lens, num_q_heads, num_kv_heads, head_dim, q_dtype, cache_dtype,
            num_blocks=None, seed=7, prefix_len=0, outlier_p=0.0, num_layers=1,
-           shuffle=True, slack=0.10) -> Workload:
+           shuffle=True, slack=0.10, block_size=BLOCK_SIZE) -> Workload:
     """A small ad-hoc workload (edge cases in tests)."""
     lens = np.asarray(lens, dtype=np.int64)
     g = _rng(seed, 0)
+    bs = block_size
     if num_blocks is None:
-        need = _blocks(lens) if not prefix_len else (
-            -(-prefix_len // BLOCK_SIZE) + int(sum(-(-(prefix_len % BLOCK_SIZE + int(L) - prefix_len) // BLOCK_SIZE)
-                                                   for L in lens)))
+        need = int(sum(-(-int(L) // bs) for L in lens)) if not prefix_len else (
+            -(-prefix_len // bs) + int(sum(-(-(prefix_len % bs + int(L) - prefix_len) // bs) for L in lens)))
         num_blocks = max(1, _pool(need, slack))
     order = (g.permutation(num_blocks) if shuffle else np.arange(num_blocks)).astype(np.int32)
     return Workload(name, 0, len(lens), num_q_heads, num_kv_heads, head_dim, q_dtype, cache_dtype,
                     num_layers, lens, num_blocks, order,
                     float(np.float32(1.0) / np.sqrt(np.float32(head_dim))),
-                    prefix_len=prefix_len, outlier_p=outlier_p, seed=seed)
+                    prefix_len=prefix_len, outlier_p=outlier_p, seed=seed, block_size=block_size)

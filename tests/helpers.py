@@ -18,6 +18,7 @@ REL_L2 = 2e-3
 def oracle_play(w, alloc_order=None, layers=1, with_step=True):
     """Pre-fill (and the decode step's append) on the oracle; returns the oracle state."""
     o = PagedKVOracle(layers, w.num_blocks, w.num_kv_heads, w.head_dim, w.cache_dtype,
+                      block_size=w.block_size,
                       alloc_order=w.alloc_order if alloc_order is None else alloc_order)
     for op in w.prefill_ops():
         if op[0] == "create":

@@ -46,9 +46,9 @@ def test_status_strings(lib):
 class Mirror:
     """Drive the C++ block manager and the oracle allocator with the same calls."""
 
-    def __init__(self, n, order=None):
-        self.bm = capi.pkv_bm_create(n, 16, order)
-        self.model = AllocatorModel(n, 16, order)
+    def __init__(self, n, order=None, bs=16):
+        self.bm = capi.pkv_bm_create(n, bs, order)
+        self.model = AllocatorModel(n, bs, order)
 
     def same_state(self):
         assert list(capi.pkv_bm_free_list(self.bm)) == list(self.model.free)
@@ -78,12 +78,14 @@ def test_fork_cow_example_matches_oracle():
     m.same_state()
 
 
-def test_random_traces_match_oracle_bit_exact():
-    rng = np.random.default_rng(11)
+@pytest.mark.parametrize("bs", [16, 32])
+def test_random_traces_match_oracle_bit_exact(bs):
+    rng = np.random.default_rng(11 + bs)
     for trial in range(25):
         n = int(rng.integers(4, 80))
         order = rng.permutation(n)
-        m = Mirror(n, order)
+        m = Mirror(n, order, bs)
+        assert capi.pkv_bm_block_size(m.bm) == bs
         live, nid = [], 0
         for _ in range(150):
             op = int(rng.integers(0, 10))
@@ -140,7 +142,7 @@ def test_invalid_arguments_raise():
     with pytest.raises(capi.PkvError):
         capi.pkv_bm_create(4, 16, [0, 1, 1, 2])
     with pytest.raises(capi.PkvError):
-        capi.pkv_bm_create(4, 32)
+        capi.pkv_bm_create(4, 24)
     capi.pkv_seq_append_slots(bm, [1] * 40)
     with pytest.raises(capi.PkvError):
         capi.pkv_build_block_tables(bm, [1], 2)

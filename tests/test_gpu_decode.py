@@ -292,3 +292,24 @@ def test_repeated_calls_reuse_the_workspace(play, kernel_kind):
     assert torch.equal(first, out[0])
     assert cache.check() == 0
     cache.close()
+
+
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
+@pytest.mark.parametrize("q_dtype,cache_dtype,d", [("bf16", "bf16", 128), ("f16", "f16", 64),
+                                                   ("bf16", "fp8_e4m3", 128), ("f16", "int8", 128)])
+def test_block_size_32(play, kernel_kind, q_dtype, cache_dtype, d):
+    """32-token blocks: two 16-token tiles per block; a shared prefix with copy-on-write in the step."""
+    prefix = 70                              # two full 32-token blocks + 6 tokens: the partial block is shared
+    lens = [prefix + s for s in (1, 2, 31, 32, 33, 100, 500)]
+    w = wl.custom(f"bs32-{cache_dtype}-{d}", lens=lens, num_q_heads=4 * 2, num_kv_heads=2, head_dim=d,
+                  q_dtype=q_dtype, cache_dtype=cache_dtype, prefix_len=prefix, outlier_p=0.003, seed=55,
+                  block_size=32)
+    full_oracle_check(play, w)
+
+
+@pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
+def test_block_size_32_ragged_no_sharing(play, kernel_kind):
+    lens = [1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 1000, 2]
+    w = wl.custom("bs32-ragged", lens=lens, num_q_heads=32, num_kv_heads=8, head_dim=128, q_dtype="bf16",
+                  cache_dtype="bf16", seed=56, block_size=32)
+    full_oracle_check(play, w)
