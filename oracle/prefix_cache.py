@@ -29,8 +29,12 @@ counts and eviction order are unique and can be compared bit for bit:
   stops at the first miss; at most (n - 1) // 16 blocks are reused for an n
   token prompt, so at least one prompt token is always computed;
 * a sequence's blocks are registered by an explicit commit once their K/V
-  are written (the block manager never sees token ids otherwise); a block
-  whose hash is already registered (to another block) stays private;
+  are written (the block manager never sees token ids otherwise), in chain
+  order; at the first block whose hash is already registered to another
+  block the sequence's chain stops, and that block and the ones after it
+  stay private.  So whoever holds a registered block also holds its parent,
+  and an unreferenced registered block has only unreferenced descendants:
+  there is always a leaf to evict;
 * a registered block whose reference count drops to 0 stays cached and
   counts as free capacity; plain free blocks (never registered) are taken
   first, in FIFO order;
@@ -182,17 +186,20 @@ class PrefixCachingAllocator(AllocatorModel):
             blk_tokens = tuple(tokens[j * bs:(j + 1) * bs])
             h = block_hash(h, blk_tokens, self.config_key)
             b = self.tables[seq][j]
-            if h not in self.by_hash and b not in self.reg:
+            holder = self.by_hash.get(h)
+            if holder is not None:
+                if holder != b:      # a duplicate of another block: the chain stops here
+                    break
+            elif b in self.reg:      # registered under another chain: the chain stops here
+                break
+            else:
                 self.by_hash[h] = b
                 self.reg[b] = (h, parent, j, blk_tokens)
                 if parent >= 0:
                     self.children[parent] += 1
                 self.last_use[b] = self.tick
                 added += 1
-            holder = self.by_hash.get(h)
-            if holder is None:   # b was registered under another chain: the chain stops here
-                break
-            parent = holder
+            parent = b
         return added
 
     def stats(self):
