@@ -223,7 +223,11 @@ def _make(wid: int, *, extra_steps: int = 0, num_seqs: int | None = None) -> Wor
     if wid == 1:
         lens = np.array([1, 17, 33, 100], dtype=np.int64)
         order = rlen.permutation(32).astype(np.int32)
-        return Workload("tiny-gqa-fp16", 1, 4, 8, 2, 64, "f16", "f16", 1, lens, 32, order,
+        nb = 32
+        if extra_steps:  # room for more steps: further blocks after the 32, in order
+            nb = max(32, _blocks(lens + extra_steps))
+            order = np.concatenate([order, np.arange(32, nb, dtype=np.int32)])
+        return Workload("tiny-gqa-fp16", 1, 4, 8, 2, 64, "f16", "f16", 1, lens, nb, order,
                         scale(64), seed=seed,
                         description="4 seqs L={1,17,33,100}, Hq8/Hkv2/d64 fp16, 32-block pool")
     if wid == 2:
