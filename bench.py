@@ -46,12 +46,17 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu capture), keyed by workload and by the hash of the decode kernel source it
 # was taken on; reported only while the source is unchanged.
 NCU_TRAFFIC = {
-    # decode kernel source 15857f1aad5937c5: tensor-core kernel, 16-warp CTAs for one-byte caches,
-    # one-pass merge, per-tile V-scale normalisation; default "auto" variant
-    ("llama3-8b", "15857f1aad5937c5"): 146_192_128,            # 142.69 MB read + 3.51 MB written
-    ("long-fp8", "15857f1aad5937c5"): 813_521_920,             # 810.14 MB read + 3.38 MB written
-    ("long-fp8:fp8_e5m2", "15857f1aad5937c5"): 813_516_544,    # 810.21 MB read + 3.31 MB written
-    ("long-fp8:int8", "15857f1aad5937c5"): 813_247_744,        # 810.08 MB read + 3.17 MB written
+    # decode kernel source f5d4af69c6427c89: tensor-core kernel with the step's append fused in,
+    # 16-warp CTAs for one-byte caches, one-pass merge; default "auto" variant.  dram__bytes_read.sum
+    # + dram__bytes_write.sum of one launch (the fifth decode call of a --steps 4 --warmup 3 run)
+    ("llama3-8b", "f5d4af69c6427c89"): 146_437_888,              # full capture: 142.76 MB read + 3.68 MB written
+    ("llama3-8b:bs32", "f5d4af69c6427c89"): 145_819_904,
+    ("mha7b-40layer", "f5d4af69c6427c89"): 271_355_392,
+    ("prefix-share", "f5d4af69c6427c89"): 47_947_008,
+    ("long-fp8", "f5d4af69c6427c89"): 813_543_680,               # full capture: 810.19 MB read + 3.35 MB written
+    ("long-fp8:fp8_e5m2", "f5d4af69c6427c89"): 813_330_688,
+    ("long-fp8:int8", "f5d4af69c6427c89"): 813_372_416,
+    ("long-fp8:bs32", "f5d4af69c6427c89"): 797_106_688,
 }
 
 
@@ -415,7 +420,7 @@ def run_e2e(w, cache, steps, first_step, dev, scrub):
     t = sum(a.elapsed_time(b) for a, b in ev) / 1e3
     kv = sum(step_accounting(w, first_step + i)["kv_bytes"] for i in range(steps)) * w.num_layers
     lens = w.context_lens + first_step
-    max_blocks = int(max(-(-int(L) // 16) for L in lens))
+    max_blocks = int(max(-(-int(L) // w.block_size) for L in lens))
     meta_bytes = 4 * (w.num_seqs + w.num_seqs * max_blocks + w.num_seqs)
     h2d = sum(x.numel() * x.element_size() for x in hosts[0]) + meta_bytes
     return {"value": round(kv / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
