@@ -24,6 +24,11 @@ Storage types:
   - ``int8``: R = 127, Q = nearest integer in [-127, 127] (``int8.encode``).
 
   The dequantised value is ``value(code) * s`` in fp64.
+* ``fp8_e4m3_int4``: the mixed scheme of "KV Cache优化实战" §3.2 (8-bit
+  keys, 4-bit values): K as ``fp8_e4m3`` above, V as ``int4`` -- R = 7,
+  Q = nearest integer in [-7, 7], two codes a byte (``int4``), so one
+  token's V row is head_dim / 2 bytes and the V pool is
+  ``[num_blocks, num_kv_heads, block_size, head_dim / 2]``.
 
 Slots never written hold NaN in this model (fp32 storage, and an fp32 NaN
 scale for one-byte codes), so that a gather that strays onto one shows up
@@ -33,22 +38,35 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import fp8, int8
+from . import fp8, int4, int8
 
-DTYPES = ("f16", "bf16", "fp8_e4m3", "fp8_e5m2", "int8")
-# one-byte cache types: (R, encode float32 quotients -> codes, decode codes -> fp64)
+DTYPES = ("f16", "bf16", "fp8_e4m3", "fp8_e5m2", "int8", "fp8_e4m3_int4")
+# coded storage types: (R, encode float32 quotients -> stored bytes, decode stored bytes -> fp64)
 CODE_TYPES = {
     "fp8_e4m3": (fp8.MAX_FINITE, fp8.encode, fp8.decode),
     "fp8_e5m2": (fp8.E5M2_MAX_FINITE, fp8.e5m2_encode, fp8.e5m2_decode),
     "int8": (int8.MAX_CODE, lambda y: int8.encode(y).view(np.uint8), int8.decode),
+    "int4": (int4.MAX_CODE, lambda y: int4.pack(int4.encode(y)), int4.decode),
 }
+# cache types whose K and V halves are stored differently: (K type, V type)
+MIXED = {"fp8_e4m3_int4": ("fp8_e4m3", "int4")}
+
+
+def part_types(dtype: str):
+    """(K storage type, V storage type) of a cache type."""
+    return MIXED.get(dtype, (dtype, dtype))
+
+
+def row_bytes(part: str, head_dim: int) -> int:
+    """Stored bytes of one token's row of one K or V storage type."""
+    return {"f16": 2, "bf16": 2, "int4": 0.5}.get(part, 1) * head_dim
 
 
 def quantize_rows(x: np.ndarray, dtype: str = "fp8_e4m3"):
-    """Per-row quantisation of float32 rows ``[..., head_dim]`` to one-byte codes.
+    """Per-row quantisation of float32 rows ``[..., head_dim]`` to codes.
 
-    Returns (codes uint8 [..., head_dim] -- an int8 code as its byte --,
-    scale float32 [...]).
+    Returns (stored bytes uint8 [..., head_dim] -- an int8 code as its byte;
+    [..., head_dim / 2] for int4 --, scale float32 [...]).
     """
     r, enc, _ = CODE_TYPES[dtype]
     x = np.asarray(x, dtype=np.float32)
@@ -60,7 +78,7 @@ def quantize_rows(x: np.ndarray, dtype: str = "fp8_e4m3"):
 
 
 def code_values(codes: np.ndarray, dtype: str) -> np.ndarray:
-    """fp64 values of one-byte codes (before the scale)."""
+    """fp64 values of stored codes (before the scale)."""
     return CODE_TYPES[dtype][2](codes)
 
 
@@ -73,18 +91,19 @@ class PagedCacheModel:
             raise ValueError(f"unknown cache dtype {dtype}")
         self.num_blocks, self.num_kv_heads, self.head_dim = num_blocks, num_kv_heads, head_dim
         self.block_size, self.dtype = block_size, dtype
-        shape = (num_blocks, num_kv_heads, block_size, head_dim)
-        if dtype in CODE_TYPES:
-            self.k = np.full(shape, 0x7F, dtype=np.uint8)
-            self.v = np.full(shape, 0x7F, dtype=np.uint8)
-            self.k_scale = np.full(shape[:3], np.nan, dtype=np.float32)
-            self.v_scale = np.full(shape[:3], np.nan, dtype=np.float32)
-        else:
-            self.k = np.full(shape, np.nan, dtype=np.float32)
-            self.v = np.full(shape, np.nan, dtype=np.float32)
-            self.k_scale = self.v_scale = None
+        self.k_type, self.v_type = part_types(dtype)
+        self.k, self.k_scale = self._pool(self.k_type)
+        self.v, self.v_scale = self._pool(self.v_type)
         # which slots have been written (parity compares filled slots only)
         self.filled = np.zeros((num_blocks, block_size), dtype=bool)
+
+    def _pool(self, part):
+        shape = (self.num_blocks, self.num_kv_heads, self.block_size)
+        if part in CODE_TYPES:
+            data = np.full(shape + (int(row_bytes(part, self.head_dim)),), 0x7F if part != "int4" else 0,
+                           dtype=np.uint8)
+            return data, np.full(shape, np.nan, dtype=np.float32)
+        return np.full(shape + (self.head_dim,), np.nan, dtype=np.float32), None
 
     def write(self, slot_mapping, k: np.ndarray, v: np.ndarray) -> None:
         """Reshape-and-cache: token t's K/V ``[num_kv_heads, head_dim]`` to slot_mapping[t].
@@ -99,16 +118,14 @@ class PagedCacheModel:
             blk, off = divmod(slot, bs)
             if blk >= self.num_blocks:
                 raise IndexError(f"slot {slot} outside the pool")
-            if self.dtype in CODE_TYPES:
-                kc, ks = quantize_rows(k[t], self.dtype)
-                vc, vs = quantize_rows(v[t], self.dtype)
-                self.k[blk, :, off, :] = kc
-                self.v[blk, :, off, :] = vc
-                self.k_scale[blk, :, off] = ks
-                self.v_scale[blk, :, off] = vs
-            else:
-                self.k[blk, :, off, :] = k[t]
-                self.v[blk, :, off, :] = v[t]
+            for part, pool, scales, x in ((self.k_type, self.k, self.k_scale, k[t]),
+                                          (self.v_type, self.v, self.v_scale, v[t])):
+                if part in CODE_TYPES:
+                    codes, sc = quantize_rows(x, part)
+                    pool[blk, :, off, :] = codes
+                    scales[blk, :, off] = sc
+                else:
+                    pool[blk, :, off, :] = x
             self.filled[blk, off] = True
 
     def copy_block(self, src: int, dst: int) -> None:
@@ -117,13 +134,15 @@ class PagedCacheModel:
         self.v[dst] = self.v[src]
         if self.k_scale is not None:
             self.k_scale[dst] = self.k_scale[src]
+        if self.v_scale is not None:
             self.v_scale[dst] = self.v_scale[src]
         self.filled[dst] = self.filled[src]
 
-    def _dequant(self, codes_or_vals, scales):
-        if self.dtype in CODE_TYPES:
-            return code_values(codes_or_vals, self.dtype) * scales.astype(np.float64)[..., None]
-        return codes_or_vals.astype(np.float64)
+    @staticmethod
+    def _dequant(part, stored, scales):
+        if part in CODE_TYPES:
+            return code_values(stored, part) * scales.astype(np.float64)[..., None]
+        return stored.astype(np.float64)
 
     def gather(self, table, length: int):
         """Contiguous fp64 K, V ``[length, num_kv_heads, head_dim]`` of one sequence.
@@ -134,23 +153,24 @@ class PagedCacheModel:
         pos = np.arange(length)
         blocks = np.asarray(table, dtype=np.int64)[pos // bs]
         offs = pos % bs
-        k = self.k[blocks, :, offs, :]          # [L, Hkv, D]
-        v = self.v[blocks, :, offs, :]
-        if self.dtype in CODE_TYPES:
-            ks = self.k_scale[blocks, :, offs]
-            vs = self.v_scale[blocks, :, offs]
-            return self._dequant(k, ks), self._dequant(v, vs)
-        return k.astype(np.float64), v.astype(np.float64)
+        out = []
+        for part, pool, scales in ((self.k_type, self.k, self.k_scale), (self.v_type, self.v, self.v_scale)):
+            stored = pool[blocks, :, offs, :]          # [L, Hkv, row]
+            sc = scales[blocks, :, offs] if scales is not None else None
+            out.append(self._dequant(part, stored, sc))
+        return out[0], out[1]
 
 
-def dequantize_rows(x: np.ndarray, dtype: str):
+def dequantize_rows(x: np.ndarray, dtype: str, part: str = "k"):
     """fp64 values a cache of ``dtype`` holds for float32 input rows ``[..., head_dim]``.
 
     The contiguous counterpart of write + gather: what token rows read back
-    as, without the paging.
+    as, without the paging.  ``part`` ("k" or "v") picks the half of a
+    mixed cache type.
     """
     x = np.asarray(x, dtype=np.float32)
-    if dtype in CODE_TYPES:
-        codes, s = quantize_rows(x, dtype)
-        return code_values(codes, dtype) * s.astype(np.float64)[..., None]
+    t = part_types(dtype)[0 if part == "k" else 1]
+    if t in CODE_TYPES:
+        codes, s = quantize_rows(x, t)
+        return code_values(codes, t) * s.astype(np.float64)[..., None]
     return x.astype(np.float64)

@@ -22,6 +22,9 @@ from __future__ import annotations
 BYTES_PER_ELEMENT = {"f16": 2, "bf16": 2, "fp8_e4m3": 1, "fp8_e5m2": 1, "int8": 1, "int4": 0.5}
 # cache types stored as one-byte codes plus one fp32 scale per (token, KV head)
 SCALED_ONE_BYTE = ("fp8_e4m3", "fp8_e5m2", "int8")
+# mixed cache types ("KV Cache优化实战" §3.2: 8-bit keys, 4-bit values), each
+# half with one fp32 scale per (token, KV head): (K bytes, V bytes) per element
+SCALED_MIXED = {"fp8_e4m3_int4": (1, 0.5)}
 
 
 def kv_bytes(layers, kv_heads, head_dim, seq_len, batch, bytes_per_element):
@@ -69,10 +72,17 @@ def max_concurrency(budget_bytes, per_request_bytes):
     return int(budget_bytes // per_request_bytes)
 
 
-def pool_blocks(budget_bytes, layers, kv_heads, head_dim, dtype, block_size=16):
-    """Whole blocks a byte budget buys for every layer's K and V (plus one-byte caches' scales)."""
+def token_head_bytes(head_dim, dtype, scale_bytes=4):
+    """K plus V bytes one token holds for one KV head (scales included)."""
     if dtype in SCALED_ONE_BYTE:
-        per_block = 2 * layers * kv_heads * block_size * (head_dim + 4)
-    else:
-        per_block = 2 * layers * kv_heads * block_size * head_dim * BYTES_PER_ELEMENT[dtype]
+        return 2 * (head_dim + scale_bytes)
+    if dtype in SCALED_MIXED:
+        kb, vb = SCALED_MIXED[dtype]
+        return int(head_dim * kb + head_dim * vb) + 2 * scale_bytes
+    return 2 * head_dim * BYTES_PER_ELEMENT[dtype]
+
+
+def pool_blocks(budget_bytes, layers, kv_heads, head_dim, dtype, block_size=16):
+    """Whole blocks a byte budget buys for every layer's K and V (plus coded caches' scales)."""
+    per_block = layers * kv_heads * block_size * token_head_bytes(head_dim, dtype)
     return int(budget_bytes // per_block)

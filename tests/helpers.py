@@ -40,7 +40,7 @@ def oracle_seq_output(w, seq, q_seq, step=0):
     """fp64 [Hq, D] attention of one sequence from its token rows (paged == contiguous)."""
     L = int(w.context_lens[seq]) + step
     K = dequantize_rows(w.kv_rows(0, seq, 0, L), w.cache_dtype)
-    V = dequantize_rows(w.kv_rows(1, seq, 0, L), w.cache_dtype)
+    V = dequantize_rows(w.kv_rows(1, seq, 0, L), w.cache_dtype, "v")
     return decode_attention(q_seq, K, V, w.scale)
 
 

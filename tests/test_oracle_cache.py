@@ -33,10 +33,10 @@ def play(w, alloc_order=None, layers=1):  # same as helpers.oracle_play
     return o
 
 
-@pytest.mark.parametrize("dtype", ["f16", "bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "fp8_e4m3", "fp8_e4m3_int4"])
 def test_paged_equals_contiguous(dtype):
     w = wl.custom("t", lens=[1, 16, 17, 45, 100], num_q_heads=8, num_kv_heads=2, head_dim=32,
-                  q_dtype="bf16" if dtype == "fp8_e4m3" else dtype, cache_dtype=dtype, outlier_p=0.01)
+                  q_dtype="bf16" if dtype.startswith("fp8") else dtype, cache_dtype=dtype, outlier_p=0.01)
     o = play(w)
     q = w.q_rows()
     out = o.decode(w.seq_ids, q, w.scale)
@@ -44,12 +44,12 @@ def test_paged_equals_contiguous(dtype):
         k = w.kv_rows(0, s, 0, int(L)); v = w.kv_rows(1, s, 0, int(L))
         K, V = o.layers[0].gather(o.alloc.tables[s], int(L))
         assert np.array_equal(K, dequantize_rows(k, dtype))
-        assert np.array_equal(V, dequantize_rows(v, dtype))
+        assert np.array_equal(V, dequantize_rows(v, dtype, "v"))
         # the concatenation cache: tokens appended one by one with np.concatenate
         kc = np.zeros((0, w.num_kv_heads, w.head_dim)); vc = np.zeros_like(kc)
         for t in range(int(L)):
             kc = np.concatenate([kc, dequantize_rows(k[t:t + 1], dtype)])
-            vc = np.concatenate([vc, dequantize_rows(v[t:t + 1], dtype)])
+            vc = np.concatenate([vc, dequantize_rows(v[t:t + 1], dtype, "v")])
         assert np.array_equal(out[s], decode_attention(q[s], kc, vc, w.scale))
     # cache length == tokens processed, and blocks held == ceil(L / 16)
     for s, L in enumerate(w.context_lens):
