@@ -75,8 +75,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
-    ap.add_argument("--cache-dtype", choices=["fp8_e4m3", "fp8_e5m2", "int8"], default=None,
-                    help="swap the workload's cache for this one-byte type (same shapes and values)")
+    ap.add_argument("--cache-dtype", choices=["fp8_e4m3", "fp8_e5m2", "int8", "fp8_e4m3_int4"], default=None,
+                    help="swap the workload's cache for this coded type (same shapes and values)")
     ap.add_argument("--block-size", type=int, choices=[16, 32], default=16,
                     help="tokens per physical block (the pool is sized for it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -128,12 +128,12 @@ def step_accounting(w: wl.Workload, step: int):
     tokens = int(lens.sum())
     kv = w.kv_bytes(step)                                      # K + V (+ scales) of all sequences
     q_bytes = w.num_seqs * w.num_q_heads * w.head_dim * 2
-    table_bytes = int(sum(-(-int(L) // 16) for L in lens)) * 4
+    table_bytes = int(sum(-(-int(L) // w.block_size) for L in lens)) * 4
     lens_bytes = w.num_seqs * 4
     out_bytes = q_bytes
     # Bytes in HBM: a shared prefix's full blocks are held (and need reading) once;
     # every sequence holds its own copy of the partial block and its suffix.
-    shared = (w.prefix_len // 16) * 16
+    shared = (w.prefix_len // w.block_size) * w.block_size
     unique_tokens = shared + int((lens - shared).sum()) if shared else tokens
     kv_unique = kv * unique_tokens // tokens
     return {"tokens": tokens, "kv_bytes": kv, "kv_unique_bytes": kv_unique,
@@ -356,7 +356,7 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.cache_dtype if w.cache_dtype not in wl.ONE_BYTE_CACHES else
+        "dtype": w.cache_dtype if w.cache_dtype not in wl.SCALED_CACHES else
         f"{w.cache_dtype} ({w.q_dtype} q, fp32 accumulate)",
         "data": "synthetic (seeded N(0,1); no dataset or weights)",
         "config": workload_config(w, args.workload, {"parallelism": f"replicas x{world} (sequences sharded)",
@@ -462,8 +462,7 @@ def oracle_steps(w, o, seqs, step0, budget_s, max_steps=None):
         o.decode(list(seqs), q, w.scale)
         t_total += time.perf_counter() - t0
         lens = [int(w.context_lens[s]) + step for s in seqs]
-        per_tok = w.num_kv_heads * (w.head_dim + 4 if w.cache_dtype == "fp8_e4m3" else 2 * w.head_dim)
-        kv += 2 * sum(lens) * per_tok
+        kv += sum(lens) * w.num_kv_heads * wl.token_head_bytes(w.cache_dtype, w.head_dim)
         toks += sum(lens)
         n += 1
         step += 1
@@ -484,7 +483,7 @@ def sample_seqs(w, budget_tokens):
 
 
 def cpu_baseline(w, budget_s):
-    seqs = sample_seqs(w, 6000 if w.cache_dtype != "fp8_e4m3" else 20000)
+    seqs = sample_seqs(w, 20000 if w.cache_dtype in wl.SCALED_CACHES else 6000)
     o = oracle_sample_state(w, seqs)
     t, n, kv, toks = oracle_steps(w, o, seqs, 0, budget_s, max_steps=CPU_MAX_STEPS)
     return {"value": round(kv / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -500,7 +499,7 @@ def run_reference(args, world, rank):
     wid = WORKLOADS[args.workload]
     w = wl.make(wid, extra_steps=max(args.warmup + args.steps + 1, CPU_MAX_STEPS + 1), cache_dtype=args.cache_dtype,
                 block_size=args.block_size)
-    seqs = sample_seqs(w, 3000 if w.cache_dtype != "fp8_e4m3" else 17000)
+    seqs = sample_seqs(w, 17000 if w.cache_dtype in wl.SCALED_CACHES else 3000)
     o = oracle_sample_state(w, seqs, max_steps=args.warmup + args.steps + 1)
     oracle_steps(w, o, seqs, 0, 0.0, max_steps=args.warmup)
     t, n, kv, toks = oracle_steps(w, o, seqs, args.warmup, float("inf"), max_steps=args.steps)

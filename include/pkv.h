@@ -27,9 +27,11 @@
  *  - Device arrays are dense and row-major in the shapes stated, and every
  *    device pointer must be 16-byte aligned.
  *  - Cache layout, per layer: k_cache, v_cache
- *    [num_blocks][num_kv_heads][block_size][head_dim]; one-byte caches
- *    (FP8_E4M3, FP8_E5M2, INT8) also have scales k_scale, v_scale float32
- *    [num_blocks][num_kv_heads][block_size].  block_size is 16 or 32.
+ *    [num_blocks][num_kv_heads][block_size][head_dim] (the V cache of
+ *    FP8_E4M3_INT4 holds head_dim / 2 bytes a row); coded caches
+ *    (FP8_E4M3, FP8_E5M2, INT8, FP8_E4M3_INT4) also have scales k_scale,
+ *    v_scale float32 [num_blocks][num_kv_heads][block_size].  block_size is
+ *    16 or 32.
  *    Token n of a sequence lives at slot
  *    table[n / block_size] * block_size + n % block_size.
  *  - Several layers are several calls with per-layer cache pointers.
@@ -62,14 +64,24 @@ typedef enum {
  * decode output only.  FP8_E4M3, FP8_E5M2, INT8: one-byte cache codes with
  * one fp32 scale per (token, KV head) ("KV Cache优化实战" §3.2-§3.3 names
  * fp8_e4m3, fp8_e5m2 and 8-bit integer caches, and prefers per-token /
- * per-head scales to one scale per tensor). */
+ * per-head scales to one scale per tensor).
+ *
+ * FP8_E4M3_INT4: the mixed scheme of "KV Cache优化实战" §3.2 (8-bit keys,
+ * 4-bit values).  The K cache holds E4M3 codes exactly as FP8_E4M3 does.
+ * The V cache holds symmetric 4-bit integers, two a byte: a V row is
+ * head_dim / 2 bytes, element 2i in the low nibble of byte i, each nibble
+ * code + 8 with code = nearest integer (ties to even) of x / scale clamped
+ * to [-7, 7], scale = amax / 7 (1 for an all-zero row).  So a V pool is
+ * [num_blocks][num_kv_heads][block_size][head_dim / 2] bytes; both halves
+ * keep one fp32 scale per (token, KV head). */
 typedef enum {
   PKV_F16 = 0,
   PKV_BF16 = 1,
   PKV_FP8_E4M3 = 2,
   PKV_F32 = 3,
   PKV_FP8_E5M2 = 4,
-  PKV_INT8 = 5
+  PKV_INT8 = 5,
+  PKV_FP8_E4M3_INT4 = 6
 } pkv_dtype;
 
 /* Bits a kernel ORs into *d_error. */
@@ -205,8 +217,9 @@ pkv_status pkv_prefix_cache_stats(const pkv_bm *bm, pkv_prefix_stats *out);
 
 /* ------------------------------------------------------------------------ */
 /* Sizing ("KV Cache优化实战" §2.1: bytes = 2 x layers x kv_heads x head_dim */
-/* x tokens x bytes per element).  One-byte caches add one fp32 scale per   */
-/* (token, KV head) for K and for V.  Returns -1 on a bad argument.          */
+/* x tokens x bytes per element).  Coded caches add one fp32 scale per      */
+/* (token, KV head) for K and for V; FP8_E4M3_INT4 counts one byte per K    */
+/* element and half a byte per V element.  Returns -1 on a bad argument.    */
 /* ------------------------------------------------------------------------ */
 int64_t pkv_kv_bytes(int32_t layers, int32_t kv_heads, int32_t head_dim, int64_t tokens,
                      pkv_dtype cache_dtype);
@@ -220,8 +233,8 @@ int64_t pkv_pool_blocks(int64_t budget_bytes, int32_t layers, int32_t kv_heads, 
 /* ------------------------------------------------------------------------ */
 
 /* Copy-on-write block copy ("KV Cache 与 vLLM" §3.3): for each pair i, copy
- * all 16 slots of physical block src[i] to dst[i] in k_cache and v_cache
- * (and k_scale / v_scale for one-byte caches; NULL otherwise).
+ * all block_size slots of physical block src[i] to dst[i] in k_cache and
+ * v_cache (and k_scale / v_scale for coded caches; NULL otherwise).
  * src, dst: device int32 [num_pairs]; ids outside [0, num_blocks) set
  * PKV_DEVERR_BAD_BLOCK and that pair is skipped. */
 pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
@@ -244,6 +257,9 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
  *   FP8_E5M2: R = 57344, Q = nearest E5M2 code, ties to even, saturating;
  *   INT8:     R = 127,   Q = nearest integer, ties to even, clamped to
  *             [-127, 127] (two's complement byte);
+ *   FP8_E4M3_INT4: K rows as FP8_E4M3; V rows R = 7, Q = nearest integer,
+ *             ties to even, clamped to [-7, 7], stored two a byte as
+ *             code + 8 (even element in the low nibble);
  * the scale goes to k_scale / v_scale at the same slot. */
 pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int32_t num_tokens,
                            int32_t num_kv_heads, int32_t head_dim, const int32_t *slot_mapping,
@@ -280,8 +296,8 @@ pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads
  * q: [num_seqs][num_q_heads][head_dim] in q_dtype (F16 / BF16); out: same
  * shape in out_dtype, either F32 (the fp32 accumulator result) or q_dtype
  * (that result rounded once to nearest even).  Caches F16 or BF16 (q_dtype must match) or
- * one byte (FP8_E4M3, FP8_E5M2, INT8: code value x scale, dequantised in the
- * kernel with k_scale / v_scale).
+ * coded (FP8_E4M3, FP8_E5M2, INT8, FP8_E4M3_INT4: code value x scale,
+ * dequantised in the kernel with k_scale / v_scale).
  * block_tables: device int32 [num_seqs][max_blocks_per_seq]; context_lens:
  * device int32 [num_seqs]; max_context_len bounds every context_len.
  * A context_len of 0 gives a zero output.  Work is split across the GPU
@@ -365,9 +381,10 @@ typedef struct {
   pkv_dtype q_dtype, cache_dtype;
   void *k_cache, *v_cache;          /* layer 0; layer l at + l * cache_layer_stride bytes */
   int64_t cache_layer_stride;
-  float *k_scale, *v_scale;         /* one-byte caches only (else NULL); layer l at + l * scale_layer_stride bytes */
+  float *k_scale, *v_scale;         /* coded caches only (else NULL); layer l at + l * scale_layer_stride bytes */
   int64_t scale_layer_stride;
   int32_t block_size;               /* 16 or 32: must match the block manager's */
+  int64_t v_cache_layer_stride;     /* V layer stride in bytes; 0: the same as cache_layer_stride */
 } pkv_pool_desc;
 
 typedef struct pkv_stepper pkv_stepper;

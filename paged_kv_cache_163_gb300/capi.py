@@ -17,10 +17,19 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32, PKV_FP8_E5M2, PKV_INT8 = 0, 1, 2, 3, 4, 5
+PKV_FP8_E4M3_INT4 = 6
 DTYPE_NAMES = {"f16": PKV_F16, "bf16": PKV_BF16, "fp8_e4m3": PKV_FP8_E4M3, "f32": PKV_F32,
-               "fp8_e5m2": PKV_FP8_E5M2, "int8": PKV_INT8}
+               "fp8_e5m2": PKV_FP8_E5M2, "int8": PKV_INT8, "fp8_e4m3_int4": PKV_FP8_E4M3_INT4}
 # cache types stored as one-byte codes (uint8 tensors) plus fp32 scales
 ONE_BYTE_CACHES = ("fp8_e4m3", "fp8_e5m2", "int8")
+# cache types with k_scale / v_scale: the one-byte ones, and K FP8 E4M3 + V INT4
+# (uint8 tensors; the V rows hold head_dim / 2 bytes)
+SCALED_CACHES = ONE_BYTE_CACHES + ("fp8_e4m3_int4",)
+
+
+def v_row_elems(cache_dtype: str, head_dim: int) -> int:
+    """Last dimension of a V cache tensor: head_dim, or head_dim / 2 bytes for 4-bit V."""
+    return head_dim // 2 if cache_dtype == "fp8_e4m3_int4" else head_dim
 BLOCK_SIZE = 16
 MAX_SEQS_PER_CALL = 1024
 DEVERR_BAD_SLOT, DEVERR_BAD_BLOCK, DEVERR_BAD_CONTEXT_LEN, DEVERR_WAIT_TIMEOUT = 1, 2, 4, 8
@@ -48,7 +57,8 @@ class PoolDesc(C.Structure):
                 ("num_q_heads", C.c_int32), ("head_dim", C.c_int32), ("q_dtype", C.c_int),
                 ("cache_dtype", C.c_int), ("k_cache", C.c_void_p), ("v_cache", C.c_void_p),
                 ("cache_layer_stride", C.c_int64), ("k_scale", C.c_void_p), ("v_scale", C.c_void_p),
-                ("scale_layer_stride", C.c_int64), ("block_size", C.c_int32)]
+                ("scale_layer_stride", C.c_int64), ("block_size", C.c_int32),
+                ("v_cache_layer_stride", C.c_int64)]
 
 
 _i32p = C.POINTER(C.c_int32)

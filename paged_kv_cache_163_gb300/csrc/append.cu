@@ -2,10 +2,10 @@
 //
 // Append ("KV Cache 与 vLLM" (zwxr.cn) §1.3, "企业官网建设流程全解析" §3.2):
 // every decode step writes the new token's K and V rows into the slot the
-// block manager gave it.  With a one-byte cache ("KV Cache优化实战"
-// §3.2-§3.3: FP8 E4M3 / E5M2, INT8) each (token, KV head) row is quantised
-// with its own scale, amax / R, using IEEE fp32 divisions so the codes are
-// reproducible (common.cuh: append_row).
+// block manager gave it.  With a coded cache ("KV Cache优化实战"
+// §3.2-§3.3: FP8 E4M3 / E5M2, INT8, and 8-bit keys with 4-bit values) each
+// (token, KV head) row is quantised with its own scale, amax / R, using IEEE
+// fp32 divisions so the codes are reproducible (common.cuh: append_row).
 //
 // Copy ("KV Cache 与 vLLM" §3.3): a shared block that must change is
 // copied whole to a fresh block before the new token lands in it.
@@ -56,8 +56,10 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
   const int64_t blk = slot / bs;
   const int off = slot % bs;
   const int64_t row = (blk * num_kv_heads + h) * bs + off;  // index of the cache row
-  append_row<D, IDT, CDT>((kind ? v : k) + th * D * 2, kind ? v_cache : k_cache, kind ? v_scale : k_scale, row,
-                          lane);
+  if (kind)
+    append_row<D, IDT, v_part(CDT)>(v + th * D * 2, v_cache, v_scale, row, lane);
+  else
+    append_row<D, IDT, k_part(CDT)>(k + th * D * 2, k_cache, k_scale, row, lane);
 }
 
 // Step metadata: page-locked host staging -> device, 16-byte vectors.  A
@@ -72,13 +74,13 @@ __global__ void __launch_bounds__(256) copy_meta_kernel(const int4 *__restrict__
 }
 
 // One CTA per (pair, K-or-V): copies a whole physical block (all heads, all
-// 16 slots) and, for one-byte caches, its scales.
+// slots) and, for coded caches, its scales.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t *k_cache, uint8_t *v_cache,
                                                           float *k_scale, float *v_scale,
                                                           const int32_t *__restrict__ src,
                                                           const int32_t *__restrict__ dst,
-                                                          int64_t block_bytes, int32_t scale_elems,
-                                                          int32_t num_blocks, int32_t *err) {
+                                                          int64_t k_block_bytes, int64_t v_block_bytes,
+                                                          int32_t scale_elems, int32_t num_blocks, int32_t *err) {
   const int pair = blockIdx.x;
   const int kind = blockIdx.y;
   const int32_t s = src[pair];
@@ -88,6 +90,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t *k_cache, uint
     return;
   }
   uint8_t *base = kind ? v_cache : k_cache;
+  const int64_t block_bytes = kind ? v_block_bytes : k_block_bytes;
   const uint4 *sp = reinterpret_cast<const uint4 *>(base + s * block_bytes);
   uint4 *dp = reinterpret_cast<uint4 *>(base + d * block_bytes);
   const int64_t n16 = block_bytes / 16;
@@ -125,6 +128,7 @@ static cudaError_t dispatch_append_d(const AppendArgs &a) {
     case PKV_FP8_E4M3: return dispatch_code8<D, PKV_FP8_E4M3>(a);
     case PKV_FP8_E5M2: return dispatch_code8<D, PKV_FP8_E5M2>(a);
     case PKV_INT8: return dispatch_code8<D, PKV_INT8>(a);
+    case PKV_FP8_E4M3_INT4: return dispatch_code8<D, PKV_FP8_E4M3_INT4>(a);
     case PKV_BF16: return launch_append<D, PKV_BF16, PKV_BF16>(a);
     default: return launch_append<D, PKV_F16, PKV_F16>(a);
   }
@@ -146,14 +150,15 @@ cudaError_t run_copy_meta(const int32_t *src, int32_t *dst, int64_t ints, cudaSt
 
 cudaError_t run_copy_blocks(const CopyArgs &a) {
   if (a.num_pairs == 0) return cudaSuccess;
-  const bool code8 = is_code8(a.cache_dtype);
-  const int esz = code8 ? 1 : 2;
-  const int64_t block_bytes = static_cast<int64_t>(a.num_kv_heads) * a.block_size * a.head_dim * esz;
+  const bool scaled = has_scales(a.cache_dtype);
+  const int64_t rows = static_cast<int64_t>(a.num_kv_heads) * a.block_size;
+  const int64_t k_bytes = rows * row_bytes(k_part(a.cache_dtype), a.head_dim);
+  const int64_t v_bytes = rows * row_bytes(v_part(a.cache_dtype), a.head_dim);
   const int32_t scale_elems = a.num_kv_heads * a.block_size;
   dim3 grid(a.num_pairs, 2);
   copy_blocks_kernel<<<grid, 256, 0, a.stream>>>(
       static_cast<uint8_t *>(a.k_cache), static_cast<uint8_t *>(a.v_cache),
-      code8 ? a.k_scale : nullptr, code8 ? a.v_scale : nullptr, a.src, a.dst, block_bytes, scale_elems,
+      scaled ? a.k_scale : nullptr, scaled ? a.v_scale : nullptr, a.src, a.dst, k_bytes, v_bytes, scale_elems,
       a.num_blocks, a.d_error);
   return cudaGetLastError();
 }

@@ -311,15 +311,19 @@ pkv_status pkv_seq_len(const pkv_bm *bm, int64_t seq_id, int32_t *len) {
   return PKV_OK;
 }
 
-static int64_t elem_bytes_per_token_head(int32_t head_dim, pkv_dtype dt) {
+// K plus V bytes of one token for one KV head (codes' scales included).
+static int64_t kv_bytes_per_token_head(int32_t head_dim, pkv_dtype dt) {
+  const int64_t d = head_dim;
   switch (dt) {
     case PKV_F16:
     case PKV_BF16:
-      return 2 * static_cast<int64_t>(head_dim);
+      return 2 * (2 * d);
     case PKV_FP8_E4M3:
     case PKV_FP8_E5M2:
     case PKV_INT8:
-      return static_cast<int64_t>(head_dim) + 4;  // codes + one fp32 scale
+      return 2 * (d + 4);  // codes + one fp32 scale, K and V
+    case PKV_FP8_E4M3_INT4:
+      return (d + 4) + (d / 2 + 4);  // one-byte K codes, 4-bit V codes, a scale each
     default:
       return -1;  // not a cache type
   }
@@ -327,9 +331,9 @@ static int64_t elem_bytes_per_token_head(int32_t head_dim, pkv_dtype dt) {
 
 int64_t pkv_kv_bytes(int32_t layers, int32_t kv_heads, int32_t head_dim, int64_t tokens,
                      pkv_dtype cache_dtype) {
-  int64_t per = elem_bytes_per_token_head(head_dim, cache_dtype);
-  if (layers < 0 || kv_heads < 0 || head_dim <= 0 || tokens < 0 || per < 0) return -1;
-  return 2 * static_cast<int64_t>(layers) * kv_heads * tokens * per;
+  int64_t per = kv_bytes_per_token_head(head_dim, cache_dtype);
+  if (layers < 0 || kv_heads < 0 || head_dim <= 0 || (head_dim & 1) || tokens < 0 || per < 0) return -1;
+  return static_cast<int64_t>(layers) * kv_heads * tokens * per;
 }
 
 int64_t pkv_pool_blocks(int64_t budget_bytes, int32_t layers, int32_t kv_heads, int32_t head_dim,

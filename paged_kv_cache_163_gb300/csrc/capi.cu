@@ -75,6 +75,8 @@ MmaFn pick_mma(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
   if (cache_dtype == PKV_FP8_E5M2 && q_dtype == PKV_BF16) return decode_mma_call_e5m2_bf16;
   if (cache_dtype == PKV_INT8 && q_dtype == PKV_F16) return decode_mma_call_int8_f16;
   if (cache_dtype == PKV_INT8 && q_dtype == PKV_BF16) return decode_mma_call_int8_bf16;
+  if (cache_dtype == PKV_FP8_E4M3_INT4 && q_dtype == PKV_F16) return decode_mma_call_e4m3i4_f16;
+  if (cache_dtype == PKV_FP8_E4M3_INT4 && q_dtype == PKV_BF16) return decode_mma_call_e4m3i4_bf16;
   return nullptr;
 }
 
@@ -140,6 +142,8 @@ DecodeFn pick_decode(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
   if (cache_dtype == PKV_FP8_E5M2 && q_dtype == PKV_BF16) return decode_call_e5m2_bf16;
   if (cache_dtype == PKV_INT8 && q_dtype == PKV_F16) return decode_call_int8_f16;
   if (cache_dtype == PKV_INT8 && q_dtype == PKV_BF16) return decode_call_int8_bf16;
+  if (cache_dtype == PKV_FP8_E4M3_INT4 && q_dtype == PKV_F16) return decode_call_e4m3i4_f16;
+  if (cache_dtype == PKV_FP8_E4M3_INT4 && q_dtype == PKV_BF16) return decode_call_e4m3i4_bf16;
   return nullptr;
 }
 
@@ -217,14 +221,13 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
     return fail(PKV_ERR_UNSUPPORTED, "paged_kv_copy_blocks: block_size must be 16 or 32");
   if (head_dim != 64 && head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "paged_kv_copy_blocks: head_dim must be 64 or 128");
-  if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16 && !is_code8(cache_dtype))
-    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: bad cache dtype");
+  if (!is_cache_type(cache_dtype)) return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: bad cache dtype");
   if (num_pairs == 0) return PKV_OK;
   if (num_pairs > 65535) return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: at most 65535 pairs per call");
   if (!k_cache || !v_cache || !src || !dst || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: NULL or misaligned pointer");
-  if (is_code8(cache_dtype) && (!k_scale || !v_scale))
-    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: a one-byte cache needs k_scale and v_scale");
+  if (has_scales(cache_dtype) && (!k_scale || !v_scale))
+    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: a coded cache needs k_scale and v_scale");
   CopyArgs a{k_cache, v_cache, k_scale, v_scale, src, dst, num_pairs, num_kv_heads,
              head_dim, cache_dtype, num_blocks, d_error, reinterpret_cast<cudaStream_t>(stream), block_size};
   cudaError_t e = run_copy_blocks(a);
@@ -246,14 +249,15 @@ pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int
     return fail(PKV_ERR_UNSUPPORTED, "paged_kv_append: head_dim must be 64 or 128");
   if (in_dtype != PKV_F16 && in_dtype != PKV_BF16)
     return fail(PKV_ERR_INVALID, "paged_kv_append: input rows must be F16 or BF16");
-  if (!is_code8(cache_dtype) && cache_dtype != in_dtype)
+  if (!is_cache_type(cache_dtype)) return fail(PKV_ERR_INVALID, "paged_kv_append: bad cache dtype");
+  if (!has_scales(cache_dtype) && cache_dtype != in_dtype)
     return fail(PKV_ERR_UNSUPPORTED, "paged_kv_append: a 16-bit cache must match the input dtype");
   if (num_tokens == 0) return PKV_OK;
   if (!k || !v || !slot_mapping || !k_cache || !v_cache || !aligned16(k) || !aligned16(v) ||
       !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PKV_ERR_INVALID, "paged_kv_append: NULL or misaligned pointer");
-  if (is_code8(cache_dtype) && (!k_scale || !v_scale))
-    return fail(PKV_ERR_INVALID, "paged_kv_append: a one-byte cache needs k_scale and v_scale");
+  if (has_scales(cache_dtype) && (!k_scale || !v_scale))
+    return fail(PKV_ERR_INVALID, "paged_kv_append: a coded cache needs k_scale and v_scale");
   AppendArgs a{k, v, in_dtype, num_tokens, num_kv_heads, head_dim, slot_mapping, k_cache, v_cache,
                cache_dtype, k_scale, v_scale, num_blocks, d_error,
                reinterpret_cast<cudaStream_t>(stream), block_size};
@@ -330,9 +334,9 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
       !aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(workspace))
     return fail(PKV_ERR_INVALID, "paged_attention_decode: NULL or misaligned pointer");
-  if (is_code8(cache_dtype) &&
+  if (has_scales(cache_dtype) &&
       (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
-    return fail(PKV_ERR_INVALID, "paged_attention_decode: a one-byte cache needs aligned k_scale and v_scale");
+    return fail(PKV_ERR_INVALID, "paged_attention_decode: a coded cache needs aligned k_scale and v_scale");
   if ((k_new != nullptr) != (v_new != nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
     return fail(PKV_ERR_INVALID, "paged_attention_decode_append: k_new and v_new must both be given, 16-byte aligned");
   DecodeLayout lay;
@@ -387,12 +391,16 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
   cudaError_t e;
   if (mma) {
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
-    const int esz = is_code8(cache_dtype) ? 1 : 2;
+    const int esz = is_code8(k_part(cache_dtype)) ? 1 : 2;
     CUtensorMap tmk, tmv;
     s = cache_tensor_map(k_cache, rows, esz, &tmk);
     if (s != PKV_OK) return s;
-    s = cache_tensor_map(v_cache, rows, esz, &tmv);
-    if (s != PKV_OK) return s;
+    if (v_part(cache_dtype) == kInt4) {
+      tmv = tmk;  // not read: 4-bit V tiles arrive by plain bulk copies
+    } else {
+      s = cache_tensor_map(v_cache, rows, esz, &tmv);
+      if (s != PKV_OK) return s;
+    }
     e = pick_mma(q_dtype, cache_dtype)(num_q_heads / num_kv_heads, kDecodeLaunch, &p, &tmk, &tmv,
                                        static_cast<int>(grid), &t_launches, nullptr);
   } else {

@@ -42,11 +42,11 @@ __device__ __forceinline__ float2 unpack2<PKV_F16>(uint32_t w) {
 // FP8 E4M3, FP8 E5M2 and INT8 caches store one byte per element and one
 // fp32 scale per (token, KV head); the value is code value x scale.
 
-// Largest code value R of a one-byte type: scale = amax / R.
+// Largest code value R of a coded storage type: scale = amax / R.
 template <int DT>
-__device__ __forceinline__ float code8_range() {
-  static_assert(is_code8(DT), "one-byte cache type");
-  return DT == PKV_FP8_E4M3 ? 448.f : (DT == PKV_FP8_E5M2 ? 57344.f : 127.f);
+__device__ __forceinline__ float code_range() {
+  static_assert(is_coded(DT), "coded storage type");
+  return DT == PKV_FP8_E4M3 ? 448.f : (DT == PKV_FP8_E5M2 ? 57344.f : (DT == PKV_INT8 ? 127.f : 7.f));
 }
 
 // Four codes (byte 0 first) -> two f16x2 words (codes 0, 1 and codes 2, 3).
@@ -90,12 +90,54 @@ __device__ __forceinline__ void unpack_code4(uint32_t w, float *out) {
   out[3] = b.y;
 }
 
-// Two float32 quotients -> two codes (a in the low byte): nearest code,
-// ties to even, saturating (FP8) or clamped to [-127, 127] (INT8).
+// ---- 4-bit V codes (the V half of FP8_E4M3_INT4) ------------------------------
+// Two codes a byte, element 2i in the low nibble of byte i; a nibble holds
+// code + 8 for a code in [-7, 7].  Decoding goes through the binary16
+// word 0x6400 | n, whose value is 1024 + n: one subtraction of 1032 leaves
+// the code, exactly.  The high nibble is decoded in place as 0x6400 | 16 n
+// = 1024 + 16 n, scaled by 1/16 and offset by -72 in one exact fused
+// multiply-add.
+
+// Bytes 0 and 2 of w (one from each of two rows) -> f16x2 words of their
+// low nibbles' codes and of their high nibbles' codes.
+__device__ __forceinline__ void int4_pair_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  uint32_t a, b;
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(a) : "r"(w));  // (w & m) | c
+  asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(b) : "r"(w));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64086408u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(b), "r"(0x2C002C00u), "r"(0xD480D480u));
+}
+
+// n bytes (n = 1 or 2) of a 4-bit row -> 2 n floats, element order.
+template <int NBYTES>
+__device__ __forceinline__ void unpack_int4(const uint8_t *src, float *out) {
+  static_assert(NBYTES == 1 || NBYTES == 2, "4-bit row slice");
+  uint32_t w = NBYTES == 2 ? *reinterpret_cast<const uint16_t *>(src) : *src;
+  // byte 0 stays at byte 0, byte 1 moves to byte 2
+  asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(w) : "r"(w));
+  uint32_t lo, hi;
+  int4_pair_to_f16x2(w, lo, hi);
+  const float2 l = __half22float2(*reinterpret_cast<__half2 *>(&lo));
+  const float2 h = __half22float2(*reinterpret_cast<__half2 *>(&hi));
+  out[0] = l.x;
+  out[1] = h.x;
+  if constexpr (NBYTES == 2) {
+    out[2] = l.y;
+    out[3] = h.y;
+  }
+}
+
+// Two float32 quotients -> two codes (a in the low byte, or the low nibble
+// for 4-bit codes): nearest code, ties to even, saturating (FP8) or clamped
+// to [-127, 127] (INT8) or [-7, 7] (4-bit).
 template <int DT>
 __device__ __forceinline__ uint32_t encode2(float a, float b) {
-  static_assert(is_code8(DT), "one-byte cache type");
-  if constexpr (DT == PKV_FP8_E4M3) {
+  static_assert(is_coded(DT), "coded storage type");
+  if constexpr (DT == kInt4) {
+    const int ia = min(max(__float2int_rn(a), -7), 7);
+    const int ib = min(max(__float2int_rn(b), -7), 7);
+    return static_cast<uint32_t>(ia + 8) | (static_cast<uint32_t>(ib + 8) << 4);
+  } else if constexpr (DT == PKV_FP8_E4M3) {
     return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   } else if constexpr (DT == PKV_FP8_E5M2) {
     return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E5M2);
@@ -156,20 +198,21 @@ __device__ __forceinline__ uint32_t pack2<PKV_F16>(float a, float b) {
 
 // ---- reshape-and-cache of one row --------------------------------------------
 // One warp encodes one (token, KV head) row of K or V: head_dim elements of
-// 16-bit input into the cache's representation.  16-bit caches keep the
-// bits.  One-byte caches store per-row absmax codes: scale = amax / R in
-// IEEE fp32 (1 for an all-zero row), code = Q(x / scale) with an IEEE fp32
-// division.  Lane i holds elements [i * D/32, (i + 1) * D/32): its slice of
-// the cache row is kSliceBytes bytes, returned in the low bytes of a uint2.
+// 16-bit input into a storage type (CDT: a 16-bit type, a one-byte code
+// type or kInt4).  16-bit storage keeps the bits.  Coded storage keeps
+// per-row absmax codes: scale = amax / R in IEEE fp32 (1 for an all-zero
+// row), code = Q(x / scale) with an IEEE fp32 division.  Lane i holds
+// elements [i * D/32, (i + 1) * D/32): its slice of the cache row is
+// slice_bytes bytes, returned in the low bytes of a uint2.
 template <int D, int CDT>
-__host__ __device__ constexpr int slice_bytes() { return is_code8(CDT) ? D / 32 : D / 16; }
+__host__ __device__ constexpr int slice_bytes() { return row_bytes(CDT, D) / 32; }
 
 template <int D, int IDT, int CDT>
 __device__ __forceinline__ uint2 encode_slice(const uint8_t *src_row, int lane, float &scale) {
   constexpr int EPL = D / 32;  // elements per lane
   const uint8_t *src = src_row + lane * EPL * 2;
   uint2 r = make_uint2(0u, 0u);
-  if constexpr (!is_code8(CDT)) {
+  if constexpr (!is_coded(CDT)) {
     if constexpr (EPL == 4) {
       r = *reinterpret_cast<const uint2 *>(src);
     } else {
@@ -184,11 +227,12 @@ __device__ __forceinline__ uint2 encode_slice(const uint8_t *src_row, int lane, 
     for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, code8_range<CDT>());
+    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, code_range<CDT>());
+    constexpr int kBits = CDT == kInt4 ? 4 : 8;  // per element
 #pragma unroll
     for (int e = 0; e < EPL; e += 2) {
-      const uint32_t c2 = encode2<CDT>(__fdiv_rn(x[e], s), __fdiv_rn(x[e + 1], s));  // x[e] -> low byte
-      r.x |= c2 << (8 * e);
+      const uint32_t c2 = encode2<CDT>(__fdiv_rn(x[e], s), __fdiv_rn(x[e + 1], s));  // x[e] -> low bits
+      r.x |= c2 << (kBits * e);
     }
     scale = s;
   }
@@ -202,13 +246,15 @@ __device__ __forceinline__ void store_slice(uint8_t *dst, uint2 r) {
     *reinterpret_cast<uint2 *>(dst) = r;
   } else if constexpr (B == 4) {
     *reinterpret_cast<uint32_t *>(dst) = r.x;
-  } else {
+  } else if constexpr (B == 2) {
     *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(r.x);
+  } else {
+    *dst = static_cast<uint8_t>(r.x);
   }
 }
 
 // Encode `src_row` and store it as cache row `row` (index into
-// [blocks][heads][16]); lane 0 stores the scale of a one-byte cache.
+// [blocks][heads][block_size]); lane 0 stores the scale of coded storage.
 template <int D, int IDT, int CDT>
 __device__ __forceinline__ void append_row(const uint8_t *src_row, uint8_t *cache, float *scales, int64_t row,
                                            int lane) {
@@ -216,7 +262,7 @@ __device__ __forceinline__ void append_row(const uint8_t *src_row, uint8_t *cach
   const uint2 r = encode_slice<D, IDT, CDT>(src_row, lane, s);
   constexpr int B = slice_bytes<D, CDT>();
   store_slice<D, CDT>(cache + row * (B * 32) + lane * B, r);
-  if constexpr (is_code8(CDT)) {
+  if constexpr (is_coded(CDT)) {
     if (lane == 0) scales[row] = s;
   }
 }

@@ -42,9 +42,12 @@ template <int D, int G, int CDT, int QDT>
 struct DecodeCfg {
   static constexpr int kWarps = 8;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kEsz = is_code8(CDT) ? 1 : 2;
-  static constexpr int kRow = D * kEsz;                     // bytes of one token's row
-  static constexpr int kTile = kBS * kRow;                  // one (block, head) tile of K or V
+  static constexpr int KT = k_part(CDT), VT = v_part(CDT);  // storage types of K and of V
+  static constexpr int kEsz = is_code8(KT) ? 1 : 2;         // K bytes per element
+  static constexpr int kRow = row_bytes(KT, D);             // bytes of one token's K row
+  static constexpr int kVRow = row_bytes(VT, D);            // bytes of one token's V row
+  static constexpr int kTile = kBS * kRow;                  // one 16-token (block, head) tile of K
+  static constexpr int kVTile = kBS * kVRow;                // ... and of V
   static constexpr int kLPT = (D == 128 && G == 8) ? 16 : 8;  // lanes per token in q.K
   static constexpr int kTPP = 32 / kLPT;                    // tokens per pass
   static constexpr int kPasses = kBS / kTPP;
@@ -53,12 +56,13 @@ struct DecodeCfg {
   static constexpr int kEPC = kChunk / kEsz;                // elements per load
   static constexpr int kEPT = kEPC * kNChunk;               // q elements per lane
   static constexpr int kDPL = D / 32;                       // output elements per lane
-  static constexpr int kScale = is_code8(CDT) ? kBS * 4 : 0;
+  static constexpr int kVSlice = kVRow / 32;                // V row bytes per lane
+  static constexpr int kScale = has_scales(CDT) ? kBS * 4 : 0;
   static constexpr int kQ = G * D * 2;
   static constexpr int kOffV = kTile;
-  static constexpr int kOffKS = 2 * kTile;
-  static constexpr int kOffVS = 2 * kTile + kScale;
-  static constexpr int kOffQ = 2 * kTile + 2 * kScale;
+  static constexpr int kOffKS = kTile + kVTile;
+  static constexpr int kOffVS = kTile + kVTile + kScale;
+  static constexpr int kOffQ = kTile + kVTile + 2 * kScale;
   static constexpr int kNew = 2 * D * 2;                    // fused append: the new token's K and V rows
   static constexpr int kOffNew = kOffQ + kQ;
   static constexpr int kStage = round_up_c(kOffNew + kNew, 128);
@@ -402,7 +406,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
   int2 *desc = desc_all + warp * 64;
   uint8_t *stages = stage_all + warp * C::kStages * C::kStage;
   const uint64_t pol = policy_evict_first();
-  const size_t head_tile = static_cast<size_t>(C::kTile);
 
   auto fill_window = [&](int w) {  // descriptors of warp-local tiles [32 w, 32 w + 32)
     const int64_t t = t0 + 32 * static_cast<int64_t>(w) + lane;
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
       const bool need_q = (m == 0) || ((d.y >> 6) & 1);
       const bool need_new = p.k_new && d.x >= 0 && ((d.y >> 5) & 1);  // the item's last tile: its new token
       const uint32_t bytes =
-          (d.x >= 0 ? 2 * C::kTile + 2 * C::kScale : 0) + (need_q ? C::kQ : 0) + (need_new ? C::kNew : 0);
+          (d.x >= 0 ? C::kTile + C::kVTile + 2 * C::kScale : 0) + (need_q ? C::kQ : 0) + (need_new ? C::kNew : 0);
       fence_proxy_async_smem();
       if (bytes == 0) {
         mbar_arrive(bars + st);
@@ -428,8 +431,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
         mbar_arrive_expect_tx(bars + st, bytes);
         if (d.x >= 0) {
           const size_t tile = static_cast<size_t>(d.x);
-          bulk_g2s(sb, p.k_cache + tile * head_tile, C::kTile, bars + st, pol);
-          bulk_g2s(sb + C::kOffV, p.v_cache + tile * head_tile, C::kTile, bars + st, pol);
+          bulk_g2s(sb, p.k_cache + tile * C::kTile, C::kTile, bars + st, pol);
+          bulk_g2s(sb + C::kOffV, p.v_cache + tile * C::kVTile, C::kVTile, bars + st, pol);
           if constexpr (C::kScale > 0) {
             bulk_g2s(sb + C::kOffKS, p.k_scale + tile * kBS, C::kScale, bars + st, pol);
             bulk_g2s(sb + C::kOffVS, p.v_scale + tile * kBS, C::kScale, bars + st, pol);
@@ -569,14 +572,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
       const int r = (d.y & 31) - 1;
       const int64_t grow = static_cast<int64_t>(d.x) * kBS + r;
       float kscl, vscl;
-      const uint2 kb = encode_slice<D, QDT, CDT>(sb + C::kOffNew, lane, kscl);
-      const uint2 vb = encode_slice<D, QDT, CDT>(sb + C::kOffNew + D * 2, lane, vscl);
-      constexpr int B = slice_bytes<D, CDT>();
-      store_slice<D, CDT>(sb + r * C::kRow + lane * B, kb);
-      store_slice<D, CDT>(sb + C::kOffV + r * C::kRow + lane * B, vb);
+      const uint2 kb = encode_slice<D, QDT, C::KT>(sb + C::kOffNew, lane, kscl);
+      const uint2 vb = encode_slice<D, QDT, C::VT>(sb + C::kOffNew + D * 2, lane, vscl);
+      constexpr int BK = slice_bytes<D, C::KT>(), BV = slice_bytes<D, C::VT>();
+      store_slice<D, C::KT>(sb + r * C::kRow + lane * BK, kb);
+      store_slice<D, C::VT>(sb + C::kOffV + r * C::kVRow + lane * BV, vb);
       // the caches are read-only everywhere else in the kernel
-      store_slice<D, CDT>(const_cast<uint8_t *>(p.k_cache) + grow * C::kRow + lane * B, kb);
-      store_slice<D, CDT>(const_cast<uint8_t *>(p.v_cache) + grow * C::kRow + lane * B, vb);
+      store_slice<D, C::KT>(const_cast<uint8_t *>(p.k_cache) + grow * C::kRow + lane * BK, kb);
+      store_slice<D, C::VT>(const_cast<uint8_t *>(p.v_cache) + grow * C::kVRow + lane * BV, vb);
       if constexpr (C::kScale > 0) {
         if (lane == 0) {
           reinterpret_cast<float *>(sb + C::kOffKS)[r] = kscl;
@@ -602,14 +605,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::kNChunk; ++c) {
           float x[C::kEPC];
-          unpack_row<CDT, C::kChunk>(ks + tok * C::kRow + (jl + c * C::kLPT) * C::kChunk, x);
+          unpack_row<C::KT, C::kChunk>(ks + tok * C::kRow + (jl + c * C::kLPT) * C::kChunk, x);
 #pragma unroll
           for (int g = 0; g < G; ++g)
 #pragma unroll
             for (int e = 0; e < C::kEPC; ++e) part[g] = fmaf(qreg[g][c * C::kEPC + e], x[e], part[g]);
         }
         float r = reduce_heads<G, C::kLPT>(part, lane);
-        if constexpr (is_code8(CDT)) r *= reinterpret_cast<const float *>(sb + C::kOffKS)[tok];
+        if constexpr (is_coded(C::KT)) r *= reinterpret_cast<const float *>(sb + C::kOffKS)[tok];
         sc[ps] = tok < ntok ? r : -INFINITY;
       }
       // -- online softmax over this tile (per head) --
@@ -637,7 +640,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
         for (int ps = 0; ps < C::kPasses; ++ps) {
           const int tok = ps * C::kTPP + tg;
           float pv = pr[ps];
-          if constexpr (is_code8(CDT)) pv *= reinterpret_cast<const float *>(sb + C::kOffVS)[tok];
+          if constexpr (is_coded(C::VT)) pv *= reinterpret_cast<const float *>(sb + C::kOffVS)[tok];
           pbuf[tok * G + hd] = pv;
         }
         if (tg == 0) {
@@ -660,7 +663,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
       for (int t = 0; t < kBS; ++t) {
         if (t < ntok) {
           float x[C::kDPL];
-          unpack_row<CDT, C::kDPL * C::kEsz>(vs + t * C::kRow + lane * C::kDPL * C::kEsz, x);
+          if constexpr (C::VT == kInt4) {
+            unpack_int4<C::kVSlice>(vs + t * C::kVRow + lane * C::kVSlice, x);
+          } else {
+            unpack_row<C::VT, C::kVSlice>(vs + t * C::kVRow + lane * C::kVSlice, x);
+          }
           float pw[G];
 #pragma unroll
           for (int g = 0; g < G; ++g) pw[g] = pbuf[t * G + g];

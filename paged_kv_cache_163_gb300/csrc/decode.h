@@ -86,9 +86,15 @@ cudaError_t decode_call_int8_f16(int head_dim, int group, int op, const DecodePa
                                  int64_t *launches, DecodeShape *shape);
 cudaError_t decode_call_int8_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
                                  int64_t *launches, DecodeShape *shape);
+cudaError_t decode_call_e4m3i4_f16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                                   int64_t *launches, DecodeShape *shape);
+cudaError_t decode_call_e4m3i4_bf16(int head_dim, int group, int op, const DecodeParams *p, int grid,
+                                    int64_t *launches, DecodeShape *shape);
 
 // Tensor-core variant (head_dim 128 only); tmk / tmv map the K and V pools as
-// 2D [rows = num_blocks * num_kv_heads * 16][128 elements] with 128-byte swizzle.
+// 2D [rows = num_blocks * num_kv_heads * block_size][128 elements] with
+// 128-byte swizzle (a 4-bit V pool is read by plain bulk copies; its tmv is
+// not used).
 cudaError_t decode_mma_call_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                 const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 cudaError_t decode_mma_call_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
@@ -105,6 +111,10 @@ cudaError_t decode_mma_call_int8_f16(int group, int op, const DecodeParams *p, c
                                      const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 cudaError_t decode_mma_call_int8_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                      const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
+cudaError_t decode_mma_call_e4m3i4_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                       const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
+cudaError_t decode_mma_call_e4m3i4_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
+                                        const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 
 // paged_attention_decode (k_new == v_new == NULL) or
 // paged_attention_decode_append, with a choice of launch: programmatic ==

@@ -10,9 +10,9 @@
 // are conflict-free because the head_dim order inside the MMAs is permuted
 // (a dot product and the output rows do not depend on the order, only on
 // using the same order for K and Q, and writing O with the matching d).
-// One-byte codes (FP8 E4M3 / E5M2, INT8) become fp16 in registers (exact);
-// a bf16 P is split into a high and a low bf16 half so the probabilities
-// keep fp16-class precision.
+// One-byte codes (FP8 E4M3 / E5M2, INT8) and 4-bit V codes become fp16 in
+// registers (exact); a bf16 P is split into a high and a low bf16 half so
+// the probabilities keep fp16-class precision.
 #pragma once
 
 #include <cuda.h>
@@ -68,7 +68,9 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 template <int G, int CDT, int QDT>
 struct MmaCfg {
   static constexpr int kD = 128;
-  static constexpr bool kCode8 = is_code8(CDT);  // one-byte codes (FP8 E4M3 / E5M2, INT8) with scales
+  static constexpr int KT = k_part(CDT), VT = v_part(CDT);  // storage types of K and of V
+  static constexpr bool kCode8 = is_code8(KT);  // one-byte K codes (FP8 E4M3 / E5M2, INT8) with scales
+  static constexpr bool kVInt4 = VT == kInt4;   // 4-bit V codes: plain 64-byte rows, no swizzle
   // One-byte tiles are half the bytes, so an SM holds twice the warps (with
   // at most 128 registers a thread).  They form one 16-warp CTA: two 8-warp
   // CTAs on an SM were measured to run unevenly (the CTA launched first
@@ -77,9 +79,10 @@ struct MmaCfg {
   static constexpr int kThreads = kWarps * 32;
   static constexpr bool kBf16 = !kCode8 && CDT == PKV_BF16;  // MMA operand type: bf16, else f16
   static constexpr int kEsz = kCode8 ? 1 : 2;
-  static constexpr int kTile = kBS * kD * kEsz;  // K or V tile bytes (1024-aligned in shared memory)
-  static constexpr int kKV = 2 * kTile;
-  static constexpr int kScale = kCode8 ? kBS * 4 : 0;
+  static constexpr int kTile = kBS * kD * kEsz;  // K tile bytes (1024-aligned in shared memory)
+  static constexpr int kVTile = kVInt4 ? kBS * kD / 2 : kTile;
+  static constexpr int kKV = kTile + kVTile;
+  static constexpr int kScale = has_scales(CDT) ? kBS * 4 : 0;
   static constexpr int kQ = G * kD * 2;
   static constexpr int kNew = 2 * kD * 2;  // fused append: the new token's K and V rows (query dtype)
   static constexpr int kOffNew = 2 * kScale + kQ;
@@ -97,6 +100,8 @@ struct MmaCfg {
   static constexpr int kSmem = 1024 + kTilesOff + kWarps * kStages * (kKV + kAux);
   static_assert(G >= 1 && G <= 8, "group size");
   static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kKV % 1024 == 0, "swizzled K tiles stay 1024-aligned");
+  static_assert(!kVInt4 || kCode8, "4-bit V only beside one-byte K");
 };
 
 // head_dim index of output row m (0..15) of m-tile i for lane group g (see kernel comment).
@@ -169,7 +174,11 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
           const int row = static_cast<int>(tile * kBS);
           if constexpr (C::kCode8) {
             tma_load_2d(tb, &tmk, 0, row, bars + st, pol);
-            tma_load_2d(tb + C::kTile, &tmv, 0, row, bars + st, pol);
+            if constexpr (C::kVInt4) {  // a 16-token V tile is one contiguous kilobyte
+              bulk_g2s(tb + C::kTile, p.v_cache + tile * C::kVTile, C::kVTile, bars + st, pol);
+            } else {
+              tma_load_2d(tb + C::kTile, &tmv, 0, row, bars + st, pol);
+            }
             bulk_g2s(ab, p.k_scale + tile * kBS, C::kScale, bars + st, pol);
             bulk_g2s(ab + C::kScale, p.v_scale + tile * kBS, C::kScale, bars + st, pol);
           } else {
@@ -258,6 +267,12 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
 
   // tokens whose V rows this lane reads (B-fragment k rows of P^T)
   const int tk0 = 2 * q4, tk1 = 2 * q4 + 1, tk2 = 2 * q4 + 8, tk3 = 2 * q4 + 9;
+  const int tks[4] = {tk0, tk1, tk2, tk3};
+  // 4-bit V: byte permutes that put byte b of the pair's first token at
+  // byte 0 and of its second token at byte 2 (operands swapped for odd q4)
+  uint32_t vsel[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) vsel[b] = (0x4400u + 0x1111u * b) ^ ((q4 & 1) ? 0x4444u : 0u);
 
 #pragma unroll 1
   for (int n = 0; n < count; ++n) {
@@ -317,16 +332,17 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       const int r = (d.y & 31) - 1;
       const int64_t grow = static_cast<int64_t>(d.x) * kBS + r;
       float ks, vs;
-      const uint2 kb = encode_slice<D, QDT, CDT>(ab + C::kOffNew, lane, ks);
-      const uint2 vb = encode_slice<D, QDT, CDT>(ab + C::kOffNew + D * 2, lane, vs);
+      const uint2 kb = encode_slice<D, QDT, C::KT>(ab + C::kOffNew, lane, ks);
+      const uint2 vb = encode_slice<D, QDT, C::VT>(ab + C::kOffNew + D * 2, lane, vs);
       const int off = C::kCode8 ? r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4
                                 : (lane >> 4) * 2048 + r * 128 + ((((lane & 15) >> 1) ^ (r & 7)) << 4) + (lane & 1) * 8;
-      store_slice<D, CDT>(tiles + st * C::kKV + off, kb);
-      store_slice<D, CDT>(tiles + st * C::kKV + C::kTile + off, vb);
-      constexpr int B = slice_bytes<D, CDT>();
+      constexpr int BK = slice_bytes<D, C::KT>(), BV = slice_bytes<D, C::VT>();
+      const int voff = C::kVInt4 ? r * (D / 2) + lane * BV : off;
+      store_slice<D, C::KT>(tiles + st * C::kKV + off, kb);
+      store_slice<D, C::VT>(tiles + st * C::kKV + C::kTile + voff, vb);
       // the caches are read-only everywhere else in the kernel
-      store_slice<D, CDT>(const_cast<uint8_t *>(p.k_cache) + grow * (B * 32) + lane * B, kb);
-      store_slice<D, CDT>(const_cast<uint8_t *>(p.v_cache) + grow * (B * 32) + lane * B, vb);
+      store_slice<D, C::KT>(const_cast<uint8_t *>(p.k_cache) + grow * (BK * 32) + lane * BK, kb);
+      store_slice<D, C::VT>(const_cast<uint8_t *>(p.v_cache) + grow * (BV * 32) + lane * BV, vb);
       if constexpr (C::kCode8) {
         if (lane == 0) {
           float *sab = reinterpret_cast<float *>(aux + st * C::kAux);
@@ -354,8 +370,8 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           uint32_t a[4];
-          code4_to_f16x2<CDT>(word(kr[0][s >> 2], s & 3), a[0], a[2]);
-          code4_to_f16x2<CDT>(word(kr[1][s >> 2], s & 3), a[1], a[3]);
+          code4_to_f16x2<C::KT>(word(kr[0][s >> 2], s & 3), a[0], a[2]);
+          code4_to_f16x2<C::KT>(word(kr[1][s >> 2], s & 3), a[1], a[3]);
           mma_16816(sacc4[s & 3], a, qb[s][0], qb[s][1], false);
         }
       } else {
@@ -447,9 +463,34 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       }
       // ---- O^T += V^T P^T ----
       const bool tail = ntok < kBS;
-      if constexpr (C::kCode8) {
+      if constexpr (C::kVInt4) {
+        // 4-bit V: lane group g holds bytes 8 g .. 8 g + 7 of a row, i.e.
+        // head_dim 16 g .. 16 g + 15, the same rows out_d gives the
+        // one-byte layout.  Byte i gives m-tile i: its low nibbles are row
+        // g, its high nibbles row g + 8.  Lanes with odd q4 read the two
+        // tokens of a pair in the other order (rows of the other parity),
+        // so each load spreads over all 32 banks; the byte permute's
+        // selector swaps them back.  Masked tokens need no clearing: every
+        // nibble decodes to a finite value and their P is 0.
+        uint2 vr[4];
+        const int flip = q4 & 1;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          vr[k] = *reinterpret_cast<const uint2 *>(vt + (tks[k] ^ flip) * (D / 2) + g * 8);
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t x0 = w ? vr[0].y : vr[0].x, y0 = w ? vr[1].y : vr[1].x;
+          const uint32_t x1 = w ? vr[2].y : vr[2].x, y1 = w ? vr[3].y : vr[3].x;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            uint32_t a[4];
+            int4_pair_to_f16x2(prmt(x0, y0, vsel[b]), a[0], a[1]);
+            int4_pair_to_f16x2(prmt(x1, y1, vsel[b]), a[2], a[3]);
+            mma_16816(oacc[4 * w + b], a, pb[0][0], pb[0][1], false);
+          }
+        }
+      } else if constexpr (C::kCode8) {
         uint4 vr[4];  // tokens tk0..tk3, chunk g (head_dim 16 g .. 16 g + 15)
-        const int tks[4] = {tk0, tk1, tk2, tk3};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           vr[k] = *reinterpret_cast<const uint4 *>(vt + tks[k] * 128 + ((g ^ (tks[k] & 7)) << 4));
@@ -459,16 +500,15 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
         for (int w = 0; w < 4; ++w) {
           const uint32_t x0 = word(vr[0], w), y0 = word(vr[1], w), x1 = word(vr[2], w), y1 = word(vr[3], w);
           uint32_t a[4], b[4];
-          code4_to_f16x2<CDT>(prmt(x0, y0, 0x5140), a[0], a[1]);
-          code4_to_f16x2<CDT>(prmt(x1, y1, 0x5140), a[2], a[3]);
-          code4_to_f16x2<CDT>(prmt(x0, y0, 0x7362), b[0], b[1]);
-          code4_to_f16x2<CDT>(prmt(x1, y1, 0x7362), b[2], b[3]);
+          code4_to_f16x2<C::VT>(prmt(x0, y0, 0x5140), a[0], a[1]);
+          code4_to_f16x2<C::VT>(prmt(x1, y1, 0x5140), a[2], a[3]);
+          code4_to_f16x2<C::VT>(prmt(x0, y0, 0x7362), b[0], b[1]);
+          code4_to_f16x2<C::VT>(prmt(x1, y1, 0x7362), b[2], b[3]);
           mma_16816(oacc[2 * w], a, pb[0][0], pb[0][1], false);
           mma_16816(oacc[2 * w + 1], b, pb[0][0], pb[0][1], false);
         }
       } else {
         uint4 vr[4][2];  // [token][half], chunk g
-        const int tks[4] = {tk0, tk1, tk2, tk3};
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll

@@ -75,7 +75,7 @@ pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32
   if (pool->block_size != PKV_BLOCK_SIZE && pool->block_size != PKV_BLOCK_SIZE_32)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_stepper_create: block_size must be 16 or 32");
   if (pool->num_layers <= 0 || pool->num_blocks <= 0 || pool->num_kv_heads <= 0 || !pool->k_cache ||
-      !pool->v_cache || (pkv::is_code8(pool->cache_dtype) && (!pool->k_scale || !pool->v_scale)))
+      !pool->v_cache || (pkv::has_scales(pool->cache_dtype) && (!pool->k_scale || !pool->v_scale)))
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: bad pool descriptor");
   if (!host_staging || host_staging_bytes < pkv_stepper_host_bytes(max_seqs, max_blocks_per_seq) ||
       !dev_meta || dev_meta_bytes < pkv_stepper_device_bytes(max_seqs, max_blocks_per_seq))
@@ -192,6 +192,7 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   auto layer_ptr = [](const void *base, int64_t stride, int32_t l) {
     return static_cast<uint8_t *>(const_cast<void *>(base)) + l * stride;
   };
+  const int64_t v_stride = P.v_cache_layer_stride ? P.v_cache_layer_stride : P.cache_layer_stride;
   auto scale_ptr = [&](float *base, int32_t l) {
     return base ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(base) + l * P.scale_layer_stride) : nullptr;
   };
@@ -203,7 +204,7 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   }
   if (ncow) {  // copy-on-write: every layer's shared blocks, before any append writes into the copies
     for (int32_t l = 0; l < P.num_layers; ++l) {
-      pkv::CopyArgs c{layer_ptr(P.k_cache, P.cache_layer_stride, l), layer_ptr(P.v_cache, P.cache_layer_stride, l),
+      pkv::CopyArgs c{layer_ptr(P.k_cache, P.cache_layer_stride, l), layer_ptr(P.v_cache, v_stride, l),
                       scale_ptr(P.k_scale, l), scale_ptr(P.v_scale, l), Hd + n, Hd + 2 * n, ncow,
                       P.num_kv_heads, P.head_dim, P.cache_dtype, P.num_blocks, d_error, cs, P.block_size};
       s = pkv::copy_blocks_unchecked(c);
@@ -226,7 +227,7 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     s = pkv::attention_decode(true, layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l),
                               layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l),
                               P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
-                              layer_ptr(P.v_cache, P.cache_layer_stride, l), P.cache_dtype, scale_ptr(P.k_scale, l),
+                              layer_ptr(P.v_cache, v_stride, l), P.cache_dtype, scale_ptr(P.k_scale, l),
                               scale_ptr(P.v_scale, l), t_tables, mb, t_lens, max_len, n, P.num_q_heads,
                               P.num_kv_heads, P.head_dim, P.num_blocks, P.block_size, scale, st->workspace,
                               st->workspace_bytes, d_error, stream);

@@ -28,7 +28,7 @@ def torch_dtype(name: str):
     if _TORCH_DTYPES is None:
         # one-byte caches hold their codes as bytes; the type is passed by name
         _TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8,
-                         "fp8_e5m2": torch.uint8, "int8": torch.uint8}
+                         "fp8_e5m2": torch.uint8, "int8": torch.uint8, "fp8_e4m3_int4": torch.uint8}
     return _TORCH_DTYPES[name]
 
 
@@ -69,8 +69,8 @@ class PagedKVCache:
         shape = (num_layers, num_blocks, num_kv_heads, block_size, head_dim)
         tdt = torch_dtype(cache_dtype)
         self.k = torch.empty(shape, dtype=tdt, device=self.device)
-        self.v = torch.empty(shape, dtype=tdt, device=self.device)
-        if cache_dtype in capi.ONE_BYTE_CACHES:
+        self.v = torch.empty(shape[:4] + (capi.v_row_elems(cache_dtype, head_dim),), dtype=tdt, device=self.device)
+        if cache_dtype in capi.SCALED_CACHES:
             self.k_scale = torch.empty(shape[:4], dtype=torch.float32, device=self.device)
             self.v_scale = torch.empty(shape[:4], dtype=torch.float32, device=self.device)
         else:
@@ -264,7 +264,7 @@ class PagedKVCache:
             k_scale=self.k_scale.data_ptr() if self.k_scale is not None else None,
             v_scale=self.v_scale.data_ptr() if self.v_scale is not None else None,
             scale_layer_stride=self.k_scale.stride(0) * 4 if self.k_scale is not None else 0,
-            block_size=self.block_size)
+            block_size=self.block_size, v_cache_layer_stride=self.v.stride(0) * self.v.element_size())
         self._stepper = capi.pkv_stepper_create(pool, n, max_blocks, host, dev, ws)
         self._stepper_bufs = (host, dev, ws)
         self._stepper_key = key

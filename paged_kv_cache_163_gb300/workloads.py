@@ -55,6 +55,17 @@ def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
 
 # cache types stored as one-byte codes plus an fp32 scale per (token, KV head)
 ONE_BYTE_CACHES = ("fp8_e4m3", "fp8_e5m2", "int8")
+# ... and every cache type with scales: K FP8 E4M3 codes + V 4-bit codes as well
+SCALED_CACHES = ONE_BYTE_CACHES + ("fp8_e4m3_int4",)
+
+
+def token_head_bytes(cache_dtype: str, head_dim: int) -> int:
+    """K plus V bytes one token holds for one KV head, scales included."""
+    if cache_dtype in ONE_BYTE_CACHES:
+        return 2 * (head_dim + 4)
+    if cache_dtype == "fp8_e4m3_int4":
+        return head_dim + head_dim // 2 + 8
+    return 4 * head_dim
 
 
 @dataclass
@@ -66,7 +77,7 @@ class Workload:
     num_kv_heads: int
     head_dim: int
     q_dtype: str              # 'f16' | 'bf16'  (also the dtype of appended K/V rows)
-    cache_dtype: str          # 'f16' | 'bf16' | 'fp8_e4m3' | 'fp8_e5m2' | 'int8'
+    cache_dtype: str          # 'f16' | 'bf16' | 'fp8_e4m3' | 'fp8_e5m2' | 'int8' | 'fp8_e4m3_int4'
     num_layers: int
     context_lens: np.ndarray  # int64 [B], post-append
     num_blocks: int
@@ -158,11 +169,9 @@ class Workload:
         return round_to(x, self.q_dtype)
 
     def kv_bytes(self, step: int = 0) -> int:
-        """Bytes of K and V (codes + fp32 scales for FP8) the decode step reads per layer."""
+        """Bytes of K and V (codes + fp32 scales for coded caches) the decode step reads per layer."""
         tokens = int(self.context_lens.sum()) + step * self.num_seqs
-        per = self.num_kv_heads * (self.head_dim + 4 if self.cache_dtype in ONE_BYTE_CACHES
-                                   else self.head_dim * 2)
-        return 2 * tokens * per
+        return tokens * self.num_kv_heads * token_head_bytes(self.cache_dtype, self.head_dim)
 
 
 def _pool(need_blocks: int, slack=0.10) -> int:
@@ -186,9 +195,9 @@ def make(wid: int, *, extra_steps: int = 0, num_seqs: int | None = None,
         w = _resize_blocks(w, block_size, extra_steps)
     if cache_dtype is None or cache_dtype == w.cache_dtype:
         return w
-    if cache_dtype not in ONE_BYTE_CACHES:
-        raise ValueError(f"a workload's cache can only be swapped for a one-byte type, not {cache_dtype}")
-    if w.cache_dtype in ONE_BYTE_CACHES:
+    if cache_dtype not in SCALED_CACHES:
+        raise ValueError(f"a workload's cache can only be swapped for a coded type, not {cache_dtype}")
+    if w.cache_dtype in SCALED_CACHES:
         name = w.name.rsplit("-", 1)[0]
         desc = w.description.replace(w.cache_dtype.replace("_", " "), cache_dtype.replace("_", " "))
     else:

@@ -188,6 +188,8 @@ def test_sizing_calls_match_oracle():
         assert capi.pkv_kv_bytes(layers, hkv, d, tokens, "fp8_e4m3") == \
             sizing.fp8_bytes_per_token(layers, hkv, d) * tokens
         budget = 80 * 10 ** 9
-        for dt in ("bf16", "fp8_e4m3"):
+        assert capi.pkv_kv_bytes(layers, hkv, d, tokens, "fp8_e4m3_int4") == \
+            layers * hkv * tokens * sizing.token_head_bytes(d, "fp8_e4m3_int4")
+        for dt in ("bf16", "fp8_e4m3", "int8", "fp8_e4m3_int4"):
             assert capi.pkv_pool_blocks(budget, layers, hkv, d, dt) == sizing.pool_blocks(budget, layers, hkv, d, dt)
     assert capi.pkv_kv_bytes(-1, 1, 64, 1, "f16") == -1

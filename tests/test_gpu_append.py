@@ -1,10 +1,10 @@
 """GPU parity of reshape-and-cache (append) and copy-on-write block copies.
 
-Bit-exact against the oracle: 16-bit caches hold the input bits; one-byte
-caches (FP8 E4M3, FP8 E5M2, INT8) hold the oracle's codes and fp32 scales,
-including exhaustive sweeps over every code value and every midpoint
-between two neighbours (round-to-nearest-even ties), subnormals, +-0 and
-saturation.
+Bit-exact against the oracle: 16-bit caches hold the input bits; coded
+caches (FP8 E4M3, FP8 E5M2, INT8, and K FP8 E4M3 with 4-bit V) hold the
+oracle's codes and fp32 scales, including exhaustive sweeps over every
+code value and every midpoint between two neighbours (round-to-nearest-even
+ties), subnormals, +-0 and saturation.
 """
 import numpy as np
 import pytest
@@ -12,6 +12,7 @@ import pytest
 from oracle import fp8
 from oracle.cache import CODE_TYPES, PagedCacheModel
 from paged_kv_cache_163_gb300 import workloads as wl
+from paged_kv_cache_163_gb300.capi import SCALED_CACHES, v_row_elems
 
 from helpers import cache_bits, oracle_bits
 
@@ -30,11 +31,11 @@ def run_append(capi, rows_k, rows_v, slots, num_blocks, hkv, d, in_dtype, cache_
     from paged_kv_cache_163_gb300.engine import torch_dtype
     dev = torch.device("cuda")
     kc = torch.empty((num_blocks, hkv, 16, d), dtype=torch_dtype(cache_dtype), device=dev)
-    vc = torch.empty_like(kc)
+    vc = torch.empty((num_blocks, hkv, 16, v_row_elems(cache_dtype, d)), dtype=kc.dtype, device=dev)
     kc.view(torch.uint8).fill_(0xFF)
     vc.view(torch.uint8).fill_(0xFF)
     ks = vs = None
-    if cache_dtype in CODE_TYPES:
+    if cache_dtype in SCALED_CACHES:
         ks = torch.full((num_blocks, hkv, 16), float("nan"), device=dev)
         vs = torch.full_like(ks, float("nan"))
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -48,7 +49,7 @@ def run_append(capi, rows_k, rows_v, slots, num_blocks, hkv, d, in_dtype, cache_
 
 def compare_with_oracle(kc, vc, ks, vs, model: PagedCacheModel, cache_dtype):
     filled = model.filled            # [blocks, 16]
-    if cache_dtype in CODE_TYPES:
+    if cache_dtype in SCALED_CACHES:
         for got, want in ((cache_bits(kc), model.k), (cache_bits(vc), model.v)):
             g = got.transpose(0, 2, 1, 3)[filled]      # [n, hkv, d]
             w = want.transpose(0, 2, 1, 3)[filled]
@@ -68,7 +69,8 @@ def compare_with_oracle(kc, vc, ks, vs, model: PagedCacheModel, cache_dtype):
 @pytest.mark.parametrize("in_dtype,cache_dtype", [("f16", "f16"), ("bf16", "bf16"),
                                                   ("bf16", "fp8_e4m3"), ("f16", "fp8_e4m3"),
                                                   ("bf16", "fp8_e5m2"), ("f16", "fp8_e5m2"),
-                                                  ("bf16", "int8"), ("f16", "int8")])
+                                                  ("bf16", "int8"), ("f16", "int8"),
+                                                  ("bf16", "fp8_e4m3_int4"), ("f16", "fp8_e4m3_int4")])
 def test_append_random_rows_bit_exact(capi, d, in_dtype, cache_dtype):
     rng = np.random.default_rng(d + len(cache_dtype))
     nb, hkv, t = 37, 4, 300
@@ -181,6 +183,44 @@ def test_onebyte_scale_ties(capi, cache_dtype):
     compare_with_oracle(kc, vc, ks, vs, model, cache_dtype)
 
 
+@pytest.mark.parametrize("in_dtype", ["bf16", "f16"])
+def test_int4_grid_and_midpoint_sweep(capi, in_dtype):
+    """4-bit V rows whose amax is 7 (scale exactly 1): every code, every tie, values near ties."""
+    grid = np.arange(8, dtype=np.float64)                 # 0 .. 7
+    mids = grid[:-1] + 0.5
+    near = np.concatenate([mids - 2.0 ** -4, mids + 2.0 ** -4])
+    vals = np.concatenate([grid, mids, near, -grid, -mids, -near, [-0.0]])
+    rows = np.tile(_grid_rows(vals, 7.0), (3, 1))         # several rows: both nibbles see every value
+    rows[1] = np.roll(rows[1], 1)
+    rows[2] = rows[2][::-1]
+    assert np.array_equal(wl.round_to(rows, in_dtype), rows)
+    x = rows[:, None, :]
+    n = x.shape[0]
+    slots = np.arange(n, dtype=np.int32)
+    kc, vc, ks, vs, flag = run_append(capi, x, x, slots, 1, 1, 128, in_dtype, "fp8_e4m3_int4")
+    assert flag == 0
+    model = PagedCacheModel(1, 1, 128, "fp8_e4m3_int4")
+    model.write(slots, x, x)
+    assert np.all(model.v_scale.reshape(-1)[:n] == 1.0)
+    compare_with_oracle(kc, vc, ks, vs, model, "fp8_e4m3_int4")
+
+
+def test_int4_scale_ties(capi):
+    """4-bit V rows of half-integers times amax / 7: quotients land on or next to ties after a real division."""
+    rng = np.random.default_rng(8)
+    d, hkv, t = 128, 2, 512
+    amax = wl.round_to(rng.uniform(1e-6, 1e4, (t, hkv)).astype(np.float32), "bf16")
+    base = (rng.integers(-7, 8, (t, hkv, d)) + rng.choice([0.0, 0.5], (t, hkv, d))) / 7.0
+    x = wl.round_to((np.clip(base, -1, 1) * amax[..., None]).astype(np.float32), "bf16")
+    x[..., 0] = amax
+    slots = rng.permutation(64 * 16)[:t].astype(np.int32)
+    kc, vc, ks, vs, flag = run_append(capi, x[::-1].copy(), x, slots, 64, hkv, d, "bf16", "fp8_e4m3_int4")
+    assert flag == 0
+    model = PagedCacheModel(64, hkv, d, "fp8_e4m3_int4")
+    model.write(slots, x[::-1].copy(), x)
+    compare_with_oracle(kc, vc, ks, vs, model, "fp8_e4m3_int4")
+
+
 def test_fp8_scale_ties_and_tiny_rows(capi):
     """Rows whose amax makes x / s land on ties and subnormals after a real division."""
     rng = np.random.default_rng(5)
@@ -207,25 +247,27 @@ def test_bad_slot_sets_flag_and_skips(capi):
     assert np.all(raw[0, :, 0] == 0x3F80) and np.all(raw[1, :, 1] == 0x3F80)
 
 
-@pytest.mark.parametrize("cache_dtype,d", [("bf16", 128), ("f16", 64), ("fp8_e4m3", 128)])
+@pytest.mark.parametrize("cache_dtype,d", [("bf16", 128), ("f16", 64), ("fp8_e4m3", 128),
+                                           ("fp8_e4m3_int4", 128), ("fp8_e4m3_int4", 64)])
 def test_copy_blocks(capi, cache_dtype, d):
     from paged_kv_cache_163_gb300.engine import torch_dtype
     dev = torch.device("cuda")
     nb, hkv = 20, 8
     g = torch.Generator(device="cpu").manual_seed(3)
-    kc = torch.randint(0, 255, (nb, hkv, 16, d * (1 if cache_dtype == "fp8_e4m3" else 2)), generator=g,
-                       dtype=torch.uint8).to(dev)
-    vc = torch.randint(0, 255, kc.shape, generator=g, dtype=torch.uint8).to(dev)
+    kbytes = d * (1 if cache_dtype in SCALED_CACHES else 2)
+    vbytes = d // 2 if cache_dtype == "fp8_e4m3_int4" else kbytes
+    kc = torch.randint(0, 255, (nb, hkv, 16, kbytes), generator=g, dtype=torch.uint8).to(dev)
+    vc = torch.randint(0, 255, (nb, hkv, 16, vbytes), generator=g, dtype=torch.uint8).to(dev)
     kc_t, vc_t = kc.view(torch_dtype(cache_dtype)), vc.view(torch_dtype(cache_dtype))
     ks = vs = None
-    if cache_dtype == "fp8_e4m3":
+    if cache_dtype in SCALED_CACHES:
         ks = torch.rand((nb, hkv, 16), generator=g).to(dev)
         vs = torch.rand((nb, hkv, 16), generator=g).to(dev)
     before = [t.clone() if t is not None else None for t in (kc, vc, ks, vs)]
     src = torch.tensor([3, 7, 11], dtype=torch.int32, device=dev)
     dst = torch.tensor([15, 0, 19], dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    capi.paged_kv_copy_blocks(kc_t, vc_t, ks, vs, src, dst, d_error=err)
+    capi.paged_kv_copy_blocks(kc_t, vc_t, ks, vs, src, dst, d_error=err, cache_dtype=cache_dtype)
     assert capi.pkv_read_device_error(err) == 0
     for now, old in zip((kc, vc, ks, vs), before):
         if now is None:
@@ -234,5 +276,5 @@ def test_copy_blocks(capi, cache_dtype, d):
         exp[dst.long()] = old[src.long()]
         assert torch.equal(now, exp)
     bad = torch.tensor([25], dtype=torch.int32, device=dev)
-    capi.paged_kv_copy_blocks(kc_t, vc_t, ks, vs, bad, src[:1], d_error=err)
+    capi.paged_kv_copy_blocks(kc_t, vc_t, ks, vs, bad, src[:1], d_error=err, cache_dtype=cache_dtype)
     assert capi.pkv_read_device_error(err) & capi.DEVERR_BAD_BLOCK

@@ -13,7 +13,8 @@ import numpy as np
 import pytest
 
 from oracle.allocator import AllocatorModel
-from oracle.cache import CODE_TYPES, quantize_rows
+from oracle.cache import quantize_rows
+from paged_kv_cache_163_gb300.capi import SCALED_CACHES
 from paged_kv_cache_163_gb300 import workloads as wl
 
 from helpers import (assert_close, cache_bits, check_rounding, oracle_bits, oracle_play, oracle_seq_output,
@@ -48,7 +49,7 @@ def check_tables(cache, o, seqs):
 def check_cache_bytes(cache, o, w, layer=0):
     model = o.layers[0]
     filled = model.filled
-    if w.cache_dtype in CODE_TYPES:
+    if w.cache_dtype in SCALED_CACHES:
         for got, want in ((cache.k[layer], model.k), (cache.v[layer], model.v)):
             g = cache_bits(got).transpose(0, 2, 1, 3)[filled]
             assert np.array_equal(g, want.transpose(0, 2, 1, 3)[filled])
@@ -159,7 +160,8 @@ def test_long_context_fp8_sampled(play, kernel_kind):
 @pytest.mark.parametrize("q_dtype,cache_dtype", [("f16", "f16"), ("bf16", "bf16"),
                                                  ("bf16", "fp8_e4m3"), ("f16", "fp8_e4m3"),
                                                  ("bf16", "fp8_e5m2"), ("f16", "fp8_e5m2"),
-                                                 ("bf16", "int8"), ("f16", "int8")])
+                                                 ("bf16", "int8"), ("f16", "int8"),
+                                                 ("bf16", "fp8_e4m3_int4"), ("f16", "fp8_e4m3_int4")])
 def test_every_instance_ragged(play, kernel_kind, d, group, q_dtype, cache_dtype):
     hkv = 2
     lens = [1, 15, 16, 17, 31, 33, 200, 777, 2]
@@ -296,7 +298,8 @@ def test_repeated_calls_reuse_the_workspace(play, kernel_kind):
 
 @pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
 @pytest.mark.parametrize("q_dtype,cache_dtype,d", [("bf16", "bf16", 128), ("f16", "f16", 64),
-                                                   ("bf16", "fp8_e4m3", 128), ("f16", "int8", 128)])
+                                                   ("bf16", "fp8_e4m3", 128), ("f16", "int8", 128),
+                                                   ("bf16", "fp8_e4m3_int4", 128), ("f16", "fp8_e4m3_int4", 64)])
 def test_block_size_32(play, kernel_kind, q_dtype, cache_dtype, d):
     """32-token blocks: two 16-token tiles per block; a shared prefix with copy-on-write in the step."""
     prefix = 70                              # two full 32-token blocks + 6 tokens: the partial block is shared

@@ -44,7 +44,8 @@ def _two_caches(play, w):
 @pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("q_dtype,cache_dtype", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "fp8_e4m3"),
-                                                 ("f16", "int8"), ("bf16", "fp8_e5m2")])
+                                                 ("f16", "int8"), ("bf16", "fp8_e5m2"),
+                                                 ("bf16", "fp8_e4m3_int4"), ("f16", "fp8_e4m3_int4")])
 def test_fused_equals_separate(play, kernel_kind, d, q_dtype, cache_dtype):
     from paged_kv_cache_163_gb300 import capi
     # lengths before the step's token: block starts, block ends, mid-block, an empty cache

@@ -40,7 +40,7 @@ def test_block_permutation_bit_identical(play, wid):
     c1.close(); c2.close()
 
 
-@pytest.mark.parametrize("cache_dtype", ["bf16", "fp8_e4m3", "fp8_e5m2", "int8"])
+@pytest.mark.parametrize("cache_dtype", ["bf16", "fp8_e4m3", "fp8_e5m2", "int8", "fp8_e4m3_int4"])
 def test_shared_prefix_equals_private_copies(play, cache_dtype):
     prefix = 1500
     lens = [prefix + s for s in (64, 100, 512, 77, 1, 300, 250, 129)]
@@ -65,16 +65,16 @@ def test_shared_prefix_equals_private_copies(play, cache_dtype):
 
 
 @pytest.mark.parametrize("q_dtype,cache_dtype", [("f16", "f16"), ("bf16", "bf16"), ("bf16", "fp8_e4m3"),
-                                                 ("bf16", "fp8_e5m2"), ("f16", "int8")])
+                                                 ("bf16", "fp8_e5m2"), ("f16", "int8"), ("bf16", "fp8_e4m3_int4")])
 def test_length_one_returns_v(play, q_dtype, cache_dtype):
     w = wl.custom("one", lens=[1, 1, 1], num_q_heads=16, num_kv_heads=4, head_dim=128, q_dtype=q_dtype,
                   cache_dtype=cache_dtype, outlier_p=0.01, seed=2)
     cache, out = play.run(w)
     v = w.step_rows(1)                                  # [B, Hkv, D]
     got = to_f64(out[0])
-    if cache_dtype in ("fp8_e4m3", "fp8_e5m2", "int8"):
+    if cache_dtype in ("fp8_e4m3", "fp8_e5m2", "int8", "fp8_e4m3_int4"):
         from oracle.cache import dequantize_rows
-        want = np.repeat(dequantize_rows(v, cache_dtype), 4, axis=1)
+        want = np.repeat(dequantize_rows(v, cache_dtype, "v"), 4, axis=1)
         assert np.allclose(got, want, rtol=2 ** -8, atol=0)
     else:
         want = np.repeat(v.astype(np.float64), 4, axis=1)
