@@ -79,6 +79,8 @@ def parse_args(argv=None):
                     help="swap the workload's cache for this coded type (same shapes and values)")
     ap.add_argument("--block-size", type=int, choices=[16, 32], default=16,
                     help="tokens per physical block (the pool is sized for it)")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each step's launches from a CUDA graph (inputs refilled into fixed buffers)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
@@ -266,7 +268,8 @@ def run_ours(args, world, rank, local):
     wid = WORKLOADS[args.workload]
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
     attn_steps = max(3, min(args.steps, 30))
-    total_steps = args.warmup + args.steps + attn_steps + e2e_steps
+    host_steps = max(3, min(args.steps, 10))
+    total_steps = args.warmup + args.steps + attn_steps + host_steps + e2e_steps
     w = wl.make(wid, extra_steps=max(total_steps, CPU_MAX_STEPS) + 1, cache_dtype=args.cache_dtype,
                 block_size=args.block_size)
     cache = play.new_cache(w, device=dev)
@@ -275,13 +278,24 @@ def run_ours(args, world, rank, local):
     assert cache.check() == 0
 
     # every step's inputs resident in HBM before timing
-    ins = [play.step_inputs(w, s, device=dev) for s in range(args.warmup + args.steps + attn_steps)]
+    ins = [play.step_inputs(w, s, device=dev) for s in range(args.warmup + args.steps + attn_steps + host_steps)]
     out = torch.empty_like(ins[0][2])
     scrub = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
+    if args.graph:
+        # graph replay: the step reads fixed buffers, refilled before each step (before the L2 flush)
+        cache.use_graphs(True)
+        static = [torch.empty_like(t) for t in ins[0]]
+
+    def feed(s):
+        if not args.graph:
+            return ins[s]
+        for dst, src in zip(static, ins[s]):
+            dst.copy_(src)
+        return static
 
     for s in range(args.warmup):
-        k, v, q = ins[s]
+        k, v, q = feed(s)
         scrub(s)
         cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out)
     torch.cuda.synchronize()
@@ -296,7 +310,7 @@ def run_ours(args, world, rank, local):
     launches0 = capi.pkv_launch_count()
     clocks.mark("t0")
     for i in range(args.steps):
-        k, v, q = ins[args.warmup + i]
+        k, v, q = feed(args.warmup + i)
         scrub(i + 7)
         ev[i][0].record(stream)
         cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out)
@@ -315,11 +329,24 @@ def run_ours(args, world, rank, local):
     marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(attn_steps)]
     first_attn = args.warmup + args.steps
     for i in range(attn_steps):
-        k, v, q = ins[first_attn + i]
+        k, v, q = feed(first_attn + i)
         scrub(i + 3)
         cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out, marks=marks[i])
     torch.cuda.synchronize()
     attn_ms = [a.elapsed_time(b) for a, b in marks]
+    assert cache.check() == 0
+
+    # host cost of one step call (block manager, staging, launches): the
+    # device is idle before each call, so the call never waits for it
+    first_host = first_attn + attn_steps
+    host_us = []
+    for i in range(host_steps):
+        k, v, q = feed(first_host + i)
+        torch.cuda.synchronize()
+        h0 = time.perf_counter()
+        cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out)
+        host_us.append((time.perf_counter() - h0) * 1e6)
+    torch.cuda.synchronize()
     assert cache.check() == 0
 
     steps_acc = [step_accounting(w, args.warmup + i) for i in range(args.steps)]
@@ -334,7 +361,7 @@ def run_ours(args, world, rank, local):
     # end to end: inputs from pinned host memory, result read back, every step
     e2e = None
     if e2e_steps:
-        e2e = run_e2e(w, cache, e2e_steps, first_attn + attn_steps, dev, scrub)
+        e2e = run_e2e(w, cache, e2e_steps, first_host + host_steps, dev, scrub)
 
     peak, peak_kind = measured_peak()
     per_launch_bytes = statistics.mean(a["roofline_bytes"] for a in attn_acc)
@@ -360,7 +387,8 @@ def run_ours(args, world, rank, local):
         f"{w.cache_dtype} ({w.q_dtype} q, fp32 accumulate)",
         "data": "synthetic (seeded N(0,1); no dataset or weights)",
         "config": workload_config(w, args.workload, {"parallelism": f"replicas x{world} (sequences sharded)",
-                                                     "decode_kernel": args.kernel}),
+                                                     "decode_kernel": args.kernel,
+                                                     "step_launch": "cuda graph replay" if args.graph else "eager"}),
         "hbm_frac_step": round(value / world / peak, 4),
         "seq_tokens_per_s_per_layer": round(world * tok_total / (t_total / w.num_layers), 1),
         "attn_only": {"kv_read_gbs": round(kv_attn / t_attn / 1e9, 2),
@@ -373,6 +401,7 @@ def run_ours(args, world, rank, local):
                      "traffic": traffic, "algorithmic_bytes_per_launch": int(per_launch_bytes),
                      "launch_us": round(per_launch_s * 1e6, 3)},
         "gpu_launches": int(launches),
+        "host_us_per_step": round(statistics.median(host_us), 1),
         "clocks": clk,
         "kv_utilisation": kv_utilisation(w),
     }

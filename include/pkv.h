@@ -424,13 +424,33 @@ void pkv_stepper_destroy(pkv_stepper *st);
  * copies and appends are enqueued before the first layer's attention; the
  * optional CUDA events attn_begin / attn_end (cudaEvent_t, may be NULL) are
  * recorded on `stream` just before the first and just after the last
- * attention launch, so a caller can time the attention alone. */
+ * attention launch (the metadata copy of a multi-layer step included), so a
+ * caller can time the attention alone. */
 pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids, int32_t n,
                             const void *k_new, const void *v_new, int64_t kv_layer_stride,
                             const void *q, int64_t q_layer_stride, void *out, pkv_dtype out_dtype,
                             int64_t out_layer_stride, float scale, int32_t *cow_src, int32_t *cow_dst,
                             int32_t *num_cow, int32_t *d_error, void *attn_begin, void *attn_end,
                             pkv_stream_t stream);
+
+/* CUDA-graph replay of the step's attention launches ("KV Cache 与 vLLM"
+ * §4.2: CUDA graphs instead of eager launches).  With enable != 0, a step
+ * without copy-on-write copies launches one graph instead of its kernels:
+ * the metadata copy (more than one layer) and every layer's fused append +
+ * attention.  One graph is kept per metadata half; it is captured on a
+ * private stream the first time and captured again when the step's batch
+ * size, buffers (k_new, v_new, q, out, d_error), their strides, out_dtype or
+ * scale differ from those it was captured with, so replays pay off when the
+ * caller reuses its buffers from step to step (the usual pattern around
+ * graphs).  While enabled, a step's block tables are as wide as the next
+ * power of two of its longest table (at most max_blocks_per_seq), and a
+ * graph is also captured again when that width changes.  Results are those
+ * of eager steps.  Steps with copy-on-write
+ * copies run eagerly.  Disabling frees the graphs.  The capture counts as no
+ * launch; each replay adds its kernels to pkv_launch_count. */
+pkv_status pkv_stepper_use_graphs(pkv_stepper *st, int32_t enable);
+/* Graphs captured and replayed so far by this stepper. */
+pkv_status pkv_stepper_graph_stats(const pkv_stepper *st, int64_t *captures, int64_t *replays);
 
 /* Synchronise `stream`, copy *d_error to *h_error and, if clear != 0, zero
  * it.  Returns PKV_ERR_DEVICE_CHECK when any bit was set. */

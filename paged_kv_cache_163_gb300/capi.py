@@ -113,6 +113,8 @@ _PROTOS = {
     "pkv_stepper_create": (C.c_int, [C.POINTER(PoolDesc), C.c_int32, C.c_int32, _vp, C.c_size_t, _vp, C.c_size_t,
                                      _vp, C.c_size_t, C.POINTER(_vp)]),
     "pkv_stepper_destroy": (None, [_vp]),
+    "pkv_stepper_use_graphs": (C.c_int, [_vp, C.c_int32]),
+    "pkv_stepper_graph_stats": (C.c_int, [_vp, _i64p, _i64p]),
     # pointer arguments as addresses (ints): the per-step call marshals no ctypes pointer objects
     "pkv_stepper_step": (C.c_int, [_vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int64, _vp, C.c_int64, _vp, C.c_int,
                                    C.c_int64, C.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -444,6 +446,17 @@ def pkv_stepper_create(pool: PoolDesc, max_seqs, max_blocks_per_seq, host_stagin
 
 def pkv_stepper_destroy(st) -> None:
     load().pkv_stepper_destroy(st)
+
+
+def pkv_stepper_use_graphs(st, enable: bool) -> None:
+    _check(load().pkv_stepper_use_graphs(st, 1 if enable else 0), "pkv_stepper_use_graphs")
+
+
+def pkv_stepper_graph_stats(st):
+    """(graphs captured, graphs replayed) by this stepper."""
+    c, r = C.c_int64(0), C.c_int64(0)
+    _check(load().pkv_stepper_graph_stats(st, C.byref(c), C.byref(r)), "pkv_stepper_graph_stats")
+    return int(c.value), int(r.value)
 
 
 def _layer_stride(t, layers):

@@ -286,6 +286,13 @@ pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads
 
 namespace pkv {
 
+void add_launches(int64_t delta) { t_launches += delta; }
+
+pkv_status prepare_decode_workspace(void *workspace, int32_t num_seqs, int32_t num_kv_heads, cudaStream_t stream) {
+  const int64_t bytes = round256(2 * static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
+  return prepare_counters(workspace, num_seqs, num_kv_heads, workspace, static_cast<size_t>(bytes), stream);
+}
+
 pkv_status append_unchecked(const AppendArgs &a) {
   cudaError_t e = run_append(a);
   if (e != cudaSuccess) return cuda_fail(e, "paged_kv_append");
@@ -314,7 +321,7 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
                             const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                             int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
-                            int32_t *d_error, pkv_stream_t stream) {
+                            int32_t *d_error, pkv_stream_t stream, int64_t epoch) {
   if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS_PER_CALL)
     return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: num_seqs must be in [0, 1024]");
   pkv_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
@@ -367,7 +374,7 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
   p.ws_ctr = reinterpret_cast<uint32_t *>(ws);
   p.ws_ml = reinterpret_cast<float *>(ws + lay.ctr_bytes);
   p.ws_o = reinterpret_cast<float *>(ws + lay.ctr_bytes + lay.ml_bytes);
-  p.epoch = ++g_epoch;
+  p.epoch = epoch >= 0 ? static_cast<uint32_t>(epoch) : ++g_epoch;
   p.d_error = d_error;
   p.stream = reinterpret_cast<cudaStream_t>(stream);
   p.programmatic = programmatic ? 1 : 0;

@@ -8,6 +8,19 @@
 // one launch of the decode kernel with the append fused in.  Staging and
 // device metadata are double-buffered; half h is rewritten only after the
 // kernels of the step that last used it are done (one event per half).
+//
+// Graph mode ("KV Cache 与 vLLM" §4.2: serving engines capture the decode
+// step in CUDA graphs unless run eagerly): the launches of a step without
+// copy-on-write copies are captured once per metadata half into a CUDA
+// graph and replayed.  The graph bakes the kernels' arguments, so the step's
+// metadata keeps a layout that changes rarely (tables as wide as the next
+// power of two of the longest table, the context bound that many blocks),
+// and a graph is captured again when that width, the batch size or the
+// caller's buffers change.  Every decode
+// call, eager or replayed, takes its split-counter bank from the stepper's
+// own call count: a half's graph was captured at a count of the same parity
+// as every later step that uses the half, because each step advances the
+// count by the number of layers and the half by one.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -20,6 +33,22 @@
 #include "dtypes.h"
 #include "pkv.h"
 #include "status.h"
+
+// What a captured step graph baked in besides the stepper's own buffers.
+struct GraphKey {
+  int32_t n = -1, mb = 0;
+  const void *k_new = nullptr, *v_new = nullptr, *q = nullptr;
+  void *out = nullptr;
+  int64_t kv_stride = 0, q_stride = 0, out_stride = 0;
+  int32_t out_dtype = -1;
+  uint32_t scale_bits = 0;
+  int32_t *d_error = nullptr;
+  bool same(const GraphKey &o) const {
+    return n == o.n && mb == o.mb && k_new == o.k_new && v_new == o.v_new && q == o.q && out == o.out &&
+           kv_stride == o.kv_stride && q_stride == o.q_stride && out_stride == o.out_stride &&
+           out_dtype == o.out_dtype && scale_bits == o.scale_bits && d_error == o.d_error;
+  }
+};
 
 struct pkv_stepper {
   pkv_pool_desc pool;
@@ -35,6 +64,13 @@ struct pkv_stepper {
   bool recorded[2] = {false, false};
   std::vector<int64_t> ids;      // scratch for the duplicate check
   int next = 0;
+  int64_t calls = 0;             // decode calls issued (eager or in graphs); bank = parity
+  bool graphs = false;
+  cudaStream_t cap = nullptr;    // capture stream
+  cudaGraphExec_t exec[2] = {nullptr, nullptr};  // per metadata half
+  GraphKey key[2];
+  int64_t graph_kernels[2] = {0, 0};
+  int64_t replays = 0, captures = 0;
 };
 
 namespace {
@@ -50,6 +86,48 @@ size_t meta_ints(int32_t max_seqs, int32_t max_blocks) {
 pkv_status cuda_fail(cudaError_t e, const char *where) {
   std::string msg = std::string(where) + ": " + cudaGetErrorString(e);
   return pkv::fail(PKV_ERR_CUDA, msg.c_str());
+}
+
+// Capture a step's attention launches for metadata half h into a graph.
+// Nothing runs during the capture; the launch count it added is taken back
+// and added again on every replay.
+template <class Issue>
+pkv_status capture_step(pkv_stepper *st, int h, const GraphKey &k, Issue &issue_layers, cudaStream_t cs) {
+  // a first call on the workspace clears its counters: do that on the
+  // caller's stream now rather than inside every replay
+  pkv_status s = pkv::prepare_decode_workspace(st->workspace, k.n, st->pool.num_kv_heads, cs);
+  if (s != PKV_OK) return s;
+  const int64_t before = pkv_launch_count();
+  cudaError_t e = cudaStreamBeginCapture(st->cap, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaStreamBeginCapture");
+  s = issue_layers(st->cap, st->calls);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(st->cap, &g);  // the capture always ends, also after a failed launch
+  const int64_t launched = pkv_launch_count() - before;
+  pkv::add_launches(-launched);
+  if (s != PKV_OK) {
+    if (g) cudaGraphDestroy(g);
+    return s;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaStreamEndCapture");
+  cudaGraphExec_t x = nullptr;
+  e = cudaGraphInstantiate(&x, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaGraphInstantiate");
+  if (st->exec[h]) cudaGraphExecDestroy(st->exec[h]);  // freed once its last replay is done
+  st->exec[h] = x;
+  st->key[h] = k;
+  st->graph_kernels[h] = launched;
+  ++st->captures;
+  return PKV_OK;
+}
+
+void drop_graphs(pkv_stepper *st) {
+  for (int h = 0; h < 2; ++h) {
+    if (st->exec[h]) cudaGraphExecDestroy(st->exec[h]);
+    st->exec[h] = nullptr;
+    st->key[h] = GraphKey{};
+  }
 }
 
 }  // namespace
@@ -124,7 +202,27 @@ void pkv_stepper_destroy(pkv_stepper *st) {
       cudaEventSynchronize(e);  // the buffers may be freed after this returns
       cudaEventDestroy(e);
     }
+  drop_graphs(st);
+  if (st->cap) cudaStreamDestroy(st->cap);
   delete st;
+}
+
+pkv_status pkv_stepper_use_graphs(pkv_stepper *st, int32_t enable) {
+  if (!st) return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_use_graphs: NULL stepper");
+  if (enable && !st->cap) {
+    cudaError_t e = cudaStreamCreateWithFlags(&st->cap, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_use_graphs: capture stream");
+  }
+  if (!enable) drop_graphs(st);
+  st->graphs = enable != 0;
+  return PKV_OK;
+}
+
+pkv_status pkv_stepper_graph_stats(const pkv_stepper *st, int64_t *captures, int64_t *replays) {
+  if (!st || !captures || !replays) return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_graph_stats: bad argument");
+  *captures = st->captures;
+  *replays = st->replays;
+  return PKV_OK;
 }
 
 pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids, int32_t n,
@@ -162,6 +260,12 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     mb = std::max(mb, blocks);
     max_len = std::max(max_len, after);
   }
+  if (st->graphs) {  // a layout that changes rarely, so that captured launches stay valid
+    int32_t w = 1;
+    while (w < mb) w *= 2;
+    mb = std::min(w, st->max_blocks);
+    max_len = mb * P.block_size;
+  }
   // Half h was last used two steps ago: its kernels must be done before the
   // host rewrites the staging, and (on another stream) before this step's
   // kernels rewrite the device half.
@@ -196,12 +300,6 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   auto scale_ptr = [&](float *base, int32_t l) {
     return base ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(base) + l * P.scale_layer_stride) : nullptr;
   };
-  // Layer 0 reads the staging in place; with more layers one small kernel
-  // copies it to Dh for the others.
-  if (P.num_layers > 1) {
-    s = pkv::copy_meta_unchecked(Hd, Dh, ints, cs);
-    if (s != PKV_OK) return s;
-  }
   if (ncow) {  // copy-on-write: every layer's shared blocks, before any append writes into the copies
     for (int32_t l = 0; l < P.num_layers; ++l) {
       pkv::CopyArgs c{layer_ptr(P.k_cache, P.cache_layer_stride, l), layer_ptr(P.v_cache, v_stride, l),
@@ -211,28 +309,67 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
       if (s != PKV_OK) return s;
     }
   }
+  // The step's attention launches: with more layers one small kernel first
+  // copies the staging to Dh; layer 0 reads the staging in place.
+  auto issue_layers = [&](cudaStream_t ls, int64_t call0) -> pkv_status {
+    if (P.num_layers > 1) {
+      pkv_status r = pkv::copy_meta_unchecked(Hd, Dh, ints, ls);
+      if (r != PKV_OK) return r;
+    }
+    for (int32_t l = 0; l < P.num_layers; ++l) {
+      // Each layer is one launch: the new token's K/V rows are written by the
+      // warp that owns each sequence's last tile, then the query attends.  A
+      // decode reads the lengths and tables before it waits for the kernel
+      // launched just before it, so it may start early (programmatic launch):
+      // layer 0 reads them from the staging, later layers from Dh, which the
+      // copy kernel finished before layer 0 got past its wait.
+      const int32_t *t_lens = l == 0 ? Hd + 3 * n : d_lens;
+      const int32_t *t_tables = l == 0 ? Hd + 4 * n : d_tables;
+      pkv_status r = pkv::attention_decode(
+          true, layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l),
+          layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l), P.q_dtype,
+          layer_ptr(P.k_cache, P.cache_layer_stride, l), layer_ptr(P.v_cache, v_stride, l), P.cache_dtype,
+          scale_ptr(P.k_scale, l), scale_ptr(P.v_scale, l), t_tables, mb, t_lens, max_len, n, P.num_q_heads,
+          P.num_kv_heads, P.head_dim, P.num_blocks, P.block_size, scale, st->workspace, st->workspace_bytes,
+          d_error, reinterpret_cast<pkv_stream_t>(ls), call0 + l);
+      if (r != PKV_OK) return r;
+    }
+    return PKV_OK;
+  };
+  const bool replay = st->graphs && ncow == 0;
+  if (replay) {
+    GraphKey k;
+    k.n = n;
+    k.mb = mb;
+    k.k_new = k_new;
+    k.v_new = v_new;
+    k.q = q;
+    k.out = out;
+    k.kv_stride = kv_layer_stride;
+    k.q_stride = q_layer_stride;
+    k.out_stride = out_layer_stride;
+    k.out_dtype = out_dtype;
+    std::memcpy(&k.scale_bits, &scale, sizeof(scale));
+    k.d_error = d_error;
+    if (!st->exec[h] || !st->key[h].same(k)) {
+      s = capture_step(st, h, k, issue_layers, cs);
+      if (s != PKV_OK) return s;
+    }
+  }
   if (attn_begin) {
     e = cudaEventRecord(static_cast<cudaEvent_t>(attn_begin), cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");
   }
-  for (int32_t l = 0; l < P.num_layers; ++l) {
-    // Each layer is one launch: the new token's K/V rows are written by the
-    // warp that owns each sequence's last tile, then the query attends.  A
-    // decode reads the lengths and tables before it waits for the kernel
-    // launched just before it, so it may start early (programmatic launch):
-    // layer 0 reads them from the staging, later layers from Dh, which the
-    // copy kernel finished before layer 0 got past its wait.
-    const int32_t *t_lens = l == 0 ? Hd + 3 * n : d_lens;
-    const int32_t *t_tables = l == 0 ? Hd + 4 * n : d_tables;
-    s = pkv::attention_decode(true, layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l),
-                              layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l),
-                              P.q_dtype, layer_ptr(P.k_cache, P.cache_layer_stride, l),
-                              layer_ptr(P.v_cache, v_stride, l), P.cache_dtype, scale_ptr(P.k_scale, l),
-                              scale_ptr(P.v_scale, l), t_tables, mb, t_lens, max_len, n, P.num_q_heads,
-                              P.num_kv_heads, P.head_dim, P.num_blocks, P.block_size, scale, st->workspace,
-                              st->workspace_bytes, d_error, stream);
+  if (replay) {
+    e = cudaGraphLaunch(st->exec[h], cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaGraphLaunch");
+    pkv::add_launches(st->graph_kernels[h]);
+    ++st->replays;
+  } else {
+    s = issue_layers(cs, st->calls);
     if (s != PKV_OK) return s;
   }
+  st->calls += P.num_layers;
   if (attn_end) {
     e = cudaEventRecord(static_cast<cudaEvent_t>(attn_end), cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");

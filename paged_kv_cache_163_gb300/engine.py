@@ -87,6 +87,7 @@ class PagedKVCache:
         self._stepper_key = None
         self._stepper_bufs = None
         self._scratch = None
+        self._graphs = False
         self._device_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
         self._default_scale = float(np.float32(1.0) / np.sqrt(np.float32(head_dim)))
         self.cow_pairs = []          # every (src, dst) copy, in order
@@ -266,6 +267,8 @@ class PagedKVCache:
             scale_layer_stride=self.k_scale.stride(0) * 4 if self.k_scale is not None else 0,
             block_size=self.block_size, v_cache_layer_stride=self.v.stride(0) * self.v.element_size())
         self._stepper = capi.pkv_stepper_create(pool, n, max_blocks, host, dev, ws)
+        if self._graphs:
+            capi.pkv_stepper_use_graphs(self._stepper, True)
         self._stepper_bufs = (host, dev, ws)
         self._stepper_key = key
         self._scratch = capi.StepScratch(n)
@@ -296,6 +299,20 @@ class PagedKVCache:
         if len(cs):
             self.cow_pairs.extend(zip(cs.tolist(), cd.tolist()))
         return out
+
+    def use_graphs(self, enable: bool = True) -> None:
+        """Replay each step's attention launches from a CUDA graph (steps without copy-on-write copies).
+
+        Pays off when the step's k/v/q/out buffers stay the same from step to
+        step; a change of buffers or batch size captures the graph again.
+        """
+        self._graphs = bool(enable)
+        if self._stepper is not None:
+            capi.pkv_stepper_use_graphs(self._stepper, self._graphs)
+
+    def graph_stats(self):
+        """(graphs captured, graphs replayed) by the current step executor."""
+        return capi.pkv_stepper_graph_stats(self._stepper) if self._stepper is not None else (0, 0)
 
     def check(self, stream=None) -> int:
         """Synchronise and return (and clear) the device error bits."""
