@@ -42,23 +42,40 @@ int sm_count() {
 }
 
 std::atomic<int> g_decode_kind{PKV_DECODE_AUTO};
-std::atomic<uint32_t> g_epoch{0};  // per decode call; its low bit picks the split-item counter bank
 
-// The counter banks sit at a shape-dependent offset of the workspace.  The
-// first call on a workspace, and any call whose shape differs from the last
-// call on it, clears them (the kernels keep them clear from then on).
+// Per-workspace state of the split counters.  A decode call with epoch e
+// counts in bank e & 1 and clears the other bank for the next call, so the
+// calls on one workspace take consecutive epochs from the workspace's own
+// count.  The banks sit at a shape-dependent offset: the first call on a
+// workspace, and any call whose shape differs from the last call on it,
+// clears them first (the kernels keep them clear from then on).  A
+// forgotten workspace (the table is bounded) is cleared again on its next
+// use, so its restarted count is safe.
+struct WorkspaceState {
+  int64_t shape = -1;
+  uint32_t epoch = 0;
+};
+
+// Clear the counters if needed (on `st`) and reserve `take` consecutive
+// epochs (the first returned in *epoch; take may be 0).
 pkv_status prepare_counters(void *workspace, int32_t num_seqs, int32_t num_kv_heads, const void *ctr, size_t bytes,
-                            cudaStream_t st) {
+                            cudaStream_t st, int32_t take, uint32_t *epoch) {
   static std::mutex mu;
-  static std::unordered_map<uintptr_t, int64_t> shapes;
+  static std::unordered_map<uintptr_t, WorkspaceState> table;
   const int64_t shape = (static_cast<int64_t>(num_seqs) << 32) | static_cast<uint32_t>(num_kv_heads);
   std::lock_guard<std::mutex> lock(mu);
-  auto it = shapes.find(reinterpret_cast<uintptr_t>(workspace));
-  if (it != shapes.end() && it->second == shape) return PKV_OK;
-  cudaError_t e = cudaMemsetAsync(const_cast<void *>(ctr), 0, bytes, st);
-  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "paged_attention_decode: clearing the split counters failed");
-  if (shapes.size() > 4096) shapes.clear();
-  shapes[reinterpret_cast<uintptr_t>(workspace)] = shape;
+  auto it = table.find(reinterpret_cast<uintptr_t>(workspace));
+  if (it == table.end() || it->second.shape != shape) {
+    cudaError_t e = cudaMemsetAsync(const_cast<void *>(ctr), 0, bytes, st);
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "paged_attention_decode: clearing the split counters failed");
+    if (it == table.end()) {
+      if (table.size() > 4096) table.clear();
+      it = table.emplace(reinterpret_cast<uintptr_t>(workspace), WorkspaceState{}).first;
+    }
+    it->second.shape = shape;
+  }
+  if (epoch) *epoch = it->second.epoch;
+  it->second.epoch += static_cast<uint32_t>(take);
   return PKV_OK;
 }
 
@@ -149,6 +166,11 @@ DecodeFn pick_decode(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
 
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
+// Split counters: two banks of one per (sequence, KV head).
+int64_t ctr_bytes(int32_t num_seqs, int32_t num_kv_heads) {
+  return round256(2 * static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
+}
+
 struct DecodeLayout {
   int64_t ctr_bytes, ml_bytes, o_bytes, total;
   DecodeShape simt, mma;  // residency of the two kernel variants (mma: head_dim 128 only)
@@ -179,7 +201,7 @@ pkv_status decode_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   lay->sms = sm_count();
   if (lay->sms <= 0) return fail(PKV_ERR_CUDA, "decode: cannot query the SM count");
   const int64_t slots = lay->sms * warps_per_sm + static_cast<int64_t>(num_seqs) * num_kv_heads;
-  lay->ctr_bytes = round256(2 * static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
+  lay->ctr_bytes = ctr_bytes(num_seqs, num_kv_heads);
   lay->ml_bytes = round256(slots * group * 2 * 4);
   lay->o_bytes = round256(slots * group * head_dim * 4);
   lay->total = lay->ctr_bytes + lay->ml_bytes + lay->o_bytes;
@@ -288,9 +310,11 @@ namespace pkv {
 
 void add_launches(int64_t delta) { t_launches += delta; }
 
-pkv_status prepare_decode_workspace(void *workspace, int32_t num_seqs, int32_t num_kv_heads, cudaStream_t stream) {
-  const int64_t bytes = round256(2 * static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
-  return prepare_counters(workspace, num_seqs, num_kv_heads, workspace, static_cast<size_t>(bytes), stream);
+pkv_status take_epochs(void *workspace, int32_t num_seqs, int32_t num_kv_heads, int32_t count,
+                       cudaStream_t stream, uint32_t *first) {
+  const int64_t bytes = ctr_bytes(num_seqs, num_kv_heads);
+  return prepare_counters(workspace, num_seqs, num_kv_heads, workspace, static_cast<size_t>(bytes), stream, count,
+                          first);
 }
 
 pkv_status append_unchecked(const AppendArgs &a) {
@@ -374,14 +398,17 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
   p.ws_ctr = reinterpret_cast<uint32_t *>(ws);
   p.ws_ml = reinterpret_cast<float *>(ws + lay.ctr_bytes);
   p.ws_o = reinterpret_cast<float *>(ws + lay.ctr_bytes + lay.ml_bytes);
-  p.epoch = epoch >= 0 ? static_cast<uint32_t>(epoch) : ++g_epoch;
+
   p.d_error = d_error;
   p.stream = reinterpret_cast<cudaStream_t>(stream);
   p.programmatic = programmatic ? 1 : 0;
   p.k_new = static_cast<const uint8_t *>(k_new);
   p.v_new = static_cast<const uint8_t *>(v_new);
-  s = prepare_counters(workspace, num_seqs, num_kv_heads, p.ws_ctr, static_cast<size_t>(lay.ctr_bytes), p.stream);
+  uint32_t ep = 0;
+  s = prepare_counters(workspace, num_seqs, num_kv_heads, p.ws_ctr, static_cast<size_t>(lay.ctr_bytes), p.stream,
+                       epoch >= 0 ? 0 : 1, &ep);
   if (s != PKV_OK) return s;
+  p.epoch = epoch >= 0 ? static_cast<uint32_t>(epoch) : ep;
 
   // Grid: enough warps that each gets a few tiles of the largest possible
   // share, capped at one wave of resident CTAs of the variant that runs.

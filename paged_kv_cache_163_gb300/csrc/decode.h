@@ -121,8 +121,8 @@ cudaError_t decode_mma_call_e4m3i4_bf16(int group, int op, const DecodeParams *p
 // true lets the kernel start while the stream's previous kernel finishes.
 // Only for callers that know that kernel writes neither the block tables nor
 // the context lengths (the decode kernel reads those before it waits).
-// `epoch` >= 0 fixes the call's counter bank (epoch & 1) for a caller that
-// sequences the calls on a workspace itself; -1 takes the next global value.
+// `epoch` >= 0 is one the caller reserved with take_epochs; -1 takes the
+// workspace's next one.
 pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_new, void *out, pkv_dtype out_dtype,
                             const void *q, pkv_dtype q_dtype,
                             const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
@@ -136,9 +136,12 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
 // a stream capture records launches that run only when the graph is replayed.
 void add_launches(int64_t delta);
 
-// Clear the workspace's split counters on `stream` now if the next decode
-// call on it (these shapes) would (its first call, or new shapes), so that
-// a stream capture of that call records no clearing.
-pkv_status prepare_decode_workspace(void *workspace, int32_t num_seqs, int32_t num_kv_heads, cudaStream_t stream);
+// Reserve `count` consecutive epochs (counter-bank numbers) of a decode
+// workspace for calls the caller issues itself, the first in *first; clear
+// the split counters on `stream` first if a call with these shapes would
+// (the workspace's first call, or new shapes), so that a stream capture of
+// those calls records no clearing.
+pkv_status take_epochs(void *workspace, int32_t num_seqs, int32_t num_kv_heads, int32_t count,
+                       cudaStream_t stream, uint32_t *first);
 
 }  // namespace pkv

@@ -16,11 +16,13 @@
 // metadata keeps a layout that changes rarely (tables as wide as the next
 // power of two of the longest table, the context bound that many blocks),
 // and a graph is captured again when that width, the batch size or the
-// caller's buffers change.  Every decode
-// call, eager or replayed, takes its split-counter bank from the stepper's
-// own call count: a half's graph was captured at a count of the same parity
-// as every later step that uses the half, because each step advances the
-// count by the number of layers and the half by one.
+// caller's buffers change.  A decode call's split-counter bank is the
+// parity of an epoch drawn from its workspace's own count; a graph bakes
+// its layers' epochs.  Each step draws as many epochs as it has layers and
+// moves to the other half, so while the stepper alone uses its workspace,
+// every step that uses a half starts at the parity its graph was captured
+// with; a step whose parity differs (another caller used the workspace)
+// runs eagerly.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -64,11 +66,11 @@ struct pkv_stepper {
   bool recorded[2] = {false, false};
   std::vector<int64_t> ids;      // scratch for the duplicate check
   int next = 0;
-  int64_t calls = 0;             // decode calls issued (eager or in graphs); bank = parity
   bool graphs = false;
   cudaStream_t cap = nullptr;    // capture stream
   cudaGraphExec_t exec[2] = {nullptr, nullptr};  // per metadata half
   GraphKey key[2];
+  uint32_t parity[2] = {0, 0};   // of the first epoch each graph was captured with
   int64_t graph_kernels[2] = {0, 0};
   int64_t replays = 0, captures = 0;
 };
@@ -92,15 +94,11 @@ pkv_status cuda_fail(cudaError_t e, const char *where) {
 // Nothing runs during the capture; the launch count it added is taken back
 // and added again on every replay.
 template <class Issue>
-pkv_status capture_step(pkv_stepper *st, int h, const GraphKey &k, Issue &issue_layers, cudaStream_t cs) {
-  // a first call on the workspace clears its counters: do that on the
-  // caller's stream now rather than inside every replay
-  pkv_status s = pkv::prepare_decode_workspace(st->workspace, k.n, st->pool.num_kv_heads, cs);
-  if (s != PKV_OK) return s;
+pkv_status capture_step(pkv_stepper *st, int h, const GraphKey &k, Issue &issue_layers, uint32_t epoch0) {
   const int64_t before = pkv_launch_count();
   cudaError_t e = cudaStreamBeginCapture(st->cap, cudaStreamCaptureModeThreadLocal);
   if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaStreamBeginCapture");
-  s = issue_layers(st->cap, st->calls);
+  pkv_status s = issue_layers(st->cap, epoch0);
   cudaGraph_t g = nullptr;
   e = cudaStreamEndCapture(st->cap, &g);  // the capture always ends, also after a failed launch
   const int64_t launched = pkv_launch_count() - before;
@@ -117,6 +115,7 @@ pkv_status capture_step(pkv_stepper *st, int h, const GraphKey &k, Issue &issue_
   if (st->exec[h]) cudaGraphExecDestroy(st->exec[h]);  // freed once its last replay is done
   st->exec[h] = x;
   st->key[h] = k;
+  st->parity[h] = epoch0 & 1u;
   st->graph_kernels[h] = launched;
   ++st->captures;
   return PKV_OK;
@@ -311,7 +310,7 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   }
   // The step's attention launches: with more layers one small kernel first
   // copies the staging to Dh; layer 0 reads the staging in place.
-  auto issue_layers = [&](cudaStream_t ls, int64_t call0) -> pkv_status {
+  auto issue_layers = [&](cudaStream_t ls, uint32_t epoch0) -> pkv_status {
     if (P.num_layers > 1) {
       pkv_status r = pkv::copy_meta_unchecked(Hd, Dh, ints, ls);
       if (r != PKV_OK) return r;
@@ -331,12 +330,18 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
           layer_ptr(P.k_cache, P.cache_layer_stride, l), layer_ptr(P.v_cache, v_stride, l), P.cache_dtype,
           scale_ptr(P.k_scale, l), scale_ptr(P.v_scale, l), t_tables, mb, t_lens, max_len, n, P.num_q_heads,
           P.num_kv_heads, P.head_dim, P.num_blocks, P.block_size, scale, st->workspace, st->workspace_bytes,
-          d_error, reinterpret_cast<pkv_stream_t>(ls), call0 + l);
+          d_error, reinterpret_cast<pkv_stream_t>(ls), static_cast<int64_t>(epoch0 + static_cast<uint32_t>(l)));
       if (r != PKV_OK) return r;
     }
     return PKV_OK;
   };
-  const bool replay = st->graphs && ncow == 0;
+  // The step's decode calls take consecutive epochs of the workspace (the
+  // counters are cleared first if these shapes are new to it); a graph
+  // replays only from an epoch of the parity it was captured with.
+  uint32_t epoch0 = 0;
+  s = pkv::take_epochs(st->workspace, n, P.num_kv_heads, P.num_layers, cs, &epoch0);
+  if (s != PKV_OK) return s;
+  bool replay = st->graphs && ncow == 0;
   if (replay) {
     GraphKey k;
     k.n = n;
@@ -352,8 +357,10 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     std::memcpy(&k.scale_bits, &scale, sizeof(scale));
     k.d_error = d_error;
     if (!st->exec[h] || !st->key[h].same(k)) {
-      s = capture_step(st, h, k, issue_layers, cs);
+      s = capture_step(st, h, k, issue_layers, epoch0);
       if (s != PKV_OK) return s;
+    } else if (st->parity[h] != (epoch0 & 1u)) {
+      replay = false;  // another caller used the workspace in between: this step runs eagerly
     }
   }
   if (attn_begin) {
@@ -366,10 +373,9 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     pkv::add_launches(st->graph_kernels[h]);
     ++st->replays;
   } else {
-    s = issue_layers(cs, st->calls);
+    s = issue_layers(cs, epoch0);
     if (s != PKV_OK) return s;
   }
-  st->calls += P.num_layers;
   if (attn_end) {
     e = cudaEventRecord(static_cast<cudaEvent_t>(attn_end), cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaEventRecord");

@@ -140,3 +140,27 @@ def test_new_buffers_capture_again(play):
     assert graph.check() == 0
     eager.close()
     graph.close()
+
+
+def test_other_calls_on_the_workspace_between_replays(play):
+    """A public decode call on the stepper's workspace shifts the counter-bank parity: steps stay right."""
+    w = _workload("bf16", 1, seed=72)
+    eager, graph = play.new_cache(w, poison=True), play.new_cache(w, poison=True)
+    play.prefill(w, eager)
+    play.prefill(w, graph)
+    graph.use_graphs(True)
+    be, bg = _bufs(w), _bufs(w)
+    for step in range(6):
+        oe = _static_step(eager, w, step, be, play)
+        og = _static_step(graph, w, step, bg, play)
+        assert torch.equal(oe, og), f"step {step}"
+        if step in (1, 3):                   # one extra decode call on each cache's workspace
+            q = play.to_device(w.q_rows(0, step), "bf16", "cuda")
+            a = eager.decode(w.seq_ids, q, scale=w.scale, out=torch.empty(q.shape, device="cuda"))
+            b = graph.decode(w.seq_ids, q, scale=w.scale, out=torch.empty(q.shape, device="cuda"))
+            assert torch.equal(a, b) and torch.equal(a, oe[0])
+    captures, replays = graph.graph_stats()
+    assert captures == 2 and replays < 6                # steps after an odd shift ran eagerly
+    assert eager.check() == 0 and graph.check() == 0
+    eager.close()
+    graph.close()
