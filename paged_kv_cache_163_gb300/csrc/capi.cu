@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstring>
 #include <cstdio>
 #include <mutex>
 #include <string>
@@ -345,7 +346,7 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
                             const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                             int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
-                            int32_t *d_error, pkv_stream_t stream, int64_t epoch) {
+                            int32_t *d_error, pkv_stream_t stream, int64_t epoch, const int32_t *host_lens) {
   if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS_PER_CALL)
     return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: num_seqs must be in [0, 1024]");
   pkv_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
@@ -404,6 +405,10 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
   p.programmatic = programmatic ? 1 : 0;
   p.k_new = static_cast<const uint8_t *>(k_new);
   p.v_new = static_cast<const uint8_t *>(v_new);
+  if (host_lens && num_seqs <= kInlineLens) {
+    std::memcpy(p.lens_inline, host_lens, sizeof(int32_t) * static_cast<size_t>(num_seqs));
+    p.lens_inline_n = num_seqs;
+  }
   uint32_t ep = 0;
   s = prepare_counters(workspace, num_seqs, num_kv_heads, p.ws_ctr, static_cast<size_t>(lay.ctr_bytes), p.stream,
                        epoch >= 0 ? 0 : 1, &ep);

@@ -103,6 +103,12 @@ __device__ __forceinline__ float reduce_heads(float (&v)[G], int lane) {
   return v[0];
 }
 
+// Context length of sequence b: from the launch parameters when they carry
+// the lengths, else from memory.
+__device__ __forceinline__ int seq_len(const DecodeParams &p, int b) {
+  return p.lens_inline_n ? p.lens_inline[b] : __ldg(p.context_lens + b);
+}
+
 // Tile index t -> (sequence, KV head, block) using the exclusive prefix sum
 // cum[] of blocks per sequence (in shared memory).
 __device__ __forceinline__ int find_seq(const int32_t *cum, int num_seqs, int hkv, int64_t t) {
@@ -125,7 +131,7 @@ __device__ __forceinline__ int2 tile_desc(const DecodeParams &p, const int32_t *
   const int64_t r = t - static_cast<int64_t>(p.num_kv_heads) * cum[b];
   const int kvh = static_cast<int>(r / nb);
   const int lb = static_cast<int>(r - static_cast<int64_t>(kvh) * nb);
-  const int L = __ldg(p.context_lens + b);
+  const int L = seq_len(p, b);
   const int ntok = min(kBS, L - lb * kBS);
   const int tpb = p.tiles_per_block;
   const int32_t blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + lb / tpb);
@@ -154,7 +160,7 @@ __device__ __forceinline__ void scan_blocks(const DecodeParams &p, int32_t *cum,
     const int s = tid * PER + i;
     int nb = 0;
     if (s < p.num_seqs) {
-      const int L = p.context_lens[s];
+      const int L = seq_len(p, s);
       if (L < 0 || L > p.max_context_len ||
           static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size) {
         report(p.d_error, PKV_DEVERR_BAD_CONTEXT_LEN);
@@ -379,7 +385,7 @@ __device__ __forceinline__ void finish_partial(const DecodeParams &p, const int3
 
 template <int D, int G, int CDT, int QDT>
 __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
-    paged_decode_kernel(const DecodeParams p) {
+    paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D, G, CDT, QDT>;
   extern __shared__ __align__(128) uint8_t smem[];
   int32_t *cum = reinterpret_cast<int32_t *>(smem);

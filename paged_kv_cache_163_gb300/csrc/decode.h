@@ -15,6 +15,10 @@ struct DecodeShape {
   int warps_per_cta;
 };
 
+// Context lengths a launch can carry in its parameters (for batches up to
+// this size): the prologue then reads no lengths from memory.
+constexpr int kInlineLens = 128;
+
 struct DecodeParams {
   uint8_t *out;
   int32_t out_f32;   // 1: out is float32, 0: out has the query's 16-bit type
@@ -44,6 +48,9 @@ struct DecodeParams {
   // query dtype) is written at position context_lens[b] - 1 before that tile is read.  NULL: none.
   const uint8_t *k_new;
   const uint8_t *v_new;
+  // 0, or num_seqs: lens_inline[b] == context_lens[b] for every b (read instead of memory)
+  int32_t lens_inline_n;
+  int32_t lens_inline[kInlineLens];
 };
 
 // Launch `kernel` on `stream`; with programmatic != 0 the launch may begin
@@ -122,7 +129,8 @@ cudaError_t decode_mma_call_e4m3i4_bf16(int group, int op, const DecodeParams *p
 // Only for callers that know that kernel writes neither the block tables nor
 // the context lengths (the decode kernel reads those before it waits).
 // `epoch` >= 0 is one the caller reserved with take_epochs; -1 takes the
-// workspace's next one.
+// workspace's next one.  `host_lens`: optional host copy of context_lens,
+// passed in the launch parameters when the batch is small enough.
 pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_new, void *out, pkv_dtype out_dtype,
                             const void *q, pkv_dtype q_dtype,
                             const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
@@ -130,7 +138,8 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
                             const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                             int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
-                            int32_t *d_error, pkv_stream_t stream, int64_t epoch = -1);
+                            int32_t *d_error, pkv_stream_t stream, int64_t epoch = -1,
+                            const int32_t *host_lens = nullptr);
 
 // The calling thread's launch count (pkv_launch_count), adjusted by `delta`:
 // a stream capture records launches that run only when the graph is replayed.

@@ -112,7 +112,7 @@ __device__ __forceinline__ int out_d(int g, int i, int hrow) {
 
 template <int G, int CDT, int QDT>
 __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, QDT>::kMinBlocks)
-    paged_decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+    paged_decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv) {
   using C = MmaCfg<G, CDT, QDT>;
   constexpr int D = C::kD;

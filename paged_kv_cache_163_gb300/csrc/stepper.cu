@@ -98,7 +98,7 @@ pkv_status capture_step(pkv_stepper *st, int h, const GraphKey &k, Issue &issue_
   const int64_t before = pkv_launch_count();
   cudaError_t e = cudaStreamBeginCapture(st->cap, cudaStreamCaptureModeThreadLocal);
   if (e != cudaSuccess) return cuda_fail(e, "pkv_stepper_step: cudaStreamBeginCapture");
-  pkv_status s = issue_layers(st->cap, epoch0);
+  pkv_status s = issue_layers(st->cap, epoch0, false);
   cudaGraph_t g = nullptr;
   e = cudaStreamEndCapture(st->cap, &g);  // the capture always ends, also after a failed launch
   const int64_t launched = pkv_launch_count() - before;
@@ -310,7 +310,9 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   }
   // The step's attention launches: with more layers one small kernel first
   // copies the staging to Dh; layer 0 reads the staging in place.
-  auto issue_layers = [&](cudaStream_t ls, uint32_t epoch0) -> pkv_status {
+  // Eager launches carry the lengths in their parameters; a captured graph
+  // reads them from the staging, which every step rewrites.
+  auto issue_layers = [&](cudaStream_t ls, uint32_t epoch0, bool eager) -> pkv_status {
     if (P.num_layers > 1) {
       pkv_status r = pkv::copy_meta_unchecked(Hd, Dh, ints, ls);
       if (r != PKV_OK) return r;
@@ -330,7 +332,8 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
           layer_ptr(P.k_cache, P.cache_layer_stride, l), layer_ptr(P.v_cache, v_stride, l), P.cache_dtype,
           scale_ptr(P.k_scale, l), scale_ptr(P.v_scale, l), t_tables, mb, t_lens, max_len, n, P.num_q_heads,
           P.num_kv_heads, P.head_dim, P.num_blocks, P.block_size, scale, st->workspace, st->workspace_bytes,
-          d_error, reinterpret_cast<pkv_stream_t>(ls), static_cast<int64_t>(epoch0 + static_cast<uint32_t>(l)));
+          d_error, reinterpret_cast<pkv_stream_t>(ls), static_cast<int64_t>(epoch0 + static_cast<uint32_t>(l)),
+          eager ? lens : nullptr);
       if (r != PKV_OK) return r;
     }
     return PKV_OK;
@@ -373,7 +376,7 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
     pkv::add_launches(st->graph_kernels[h]);
     ++st->replays;
   } else {
-    s = issue_layers(cs, epoch0);
+    s = issue_layers(cs, epoch0, true);
     if (s != PKV_OK) return s;
   }
   if (attn_end) {
