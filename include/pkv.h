@@ -417,6 +417,8 @@ void pkv_stepper_destroy(pkv_stepper *st);
  * the new token in q_dtype (stride 0 reuses one tensor for every layer);
  * q + l * q_layer_stride: [n][num_q_heads][head_dim] in q_dtype;
  * out + l * out_layer_stride: same shape in out_dtype (F32 or q_dtype).
+ * k_new, v_new and q are device memory (the kernels bulk-copy them); out
+ * may also be page-locked host memory, which the kernels store to directly.
  * Validated before anything changes: n <= max_seqs, every table stays within
  * max_blocks_per_seq.  PKV_ERR_NO_BLOCKS leaves the block manager as it was.
  * The copy pairs of the step are written to cow_src / cow_dst (host, [n],
@@ -456,6 +458,23 @@ pkv_status pkv_stepper_graph_stats(const pkv_stepper *st, int64_t *captures, int
  * it.  Returns PKV_ERR_DEVICE_CHECK when any bit was set. */
 pkv_status pkv_read_device_error(int32_t *d_error, int32_t *h_error, int32_t clear,
                                  pkv_stream_t stream);
+
+/* Several copies in one kernel launch, for step inputs and outputs that live
+ * in page-locked host memory: the kernel reads and writes them in place over
+ * the host link (16-byte vectors), so one launch replaces a memcpy per
+ * tensor.  dst and src: device memory or page-locked host memory
+ * (cudaHostAlloc / cudaHostRegister, or a pinned tensor), 16-byte aligned;
+ * bytes a multiple of 16; segments must not overlap.  At most
+ * PKV_MAX_COPY_SEGMENTS segments a call; enqueued on `stream`.  A decode
+ * launched after it as a programmatic dependent (the step executor's) may
+ * start its prologue during the copy. */
+#define PKV_MAX_COPY_SEGMENTS 8
+typedef struct {
+  void *dst;
+  const void *src;
+  int64_t bytes;
+} pkv_copy_segment;
+pkv_status pkv_copy_segments(const pkv_copy_segment *segs, int32_t num_segs, pkv_stream_t stream);
 
 /* Number of kernel launches the calling thread has made through this
  * library (for launch accounting). */

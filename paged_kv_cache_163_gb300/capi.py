@@ -51,6 +51,14 @@ class NoBlocksError(PkvError):
 _lib = None
 
 
+class CopySegment(C.Structure):
+    """pkv_copy_segment."""
+    _fields_ = [("dst", C.c_void_p), ("src", C.c_void_p), ("bytes", C.c_int64)]
+
+
+MAX_COPY_SEGMENTS = 8
+
+
 class PoolDesc(C.Structure):
     """pkv_pool_desc: per-layer pools as base pointers plus byte strides."""
     _fields_ = [("num_layers", C.c_int32), ("num_blocks", C.c_int32), ("num_kv_heads", C.c_int32),
@@ -120,6 +128,7 @@ _PROTOS = {
                                    C.c_int64, C.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "pkv_read_device_error": (C.c_int, [_vp, _i32p, C.c_int32, _vp]),
     "pkv_launch_count": (C.c_int64, []),
+    "pkv_copy_segments": (C.c_int, [C.c_void_p, C.c_int32, _vp]),
     "pkv_set_decode_kernel": (C.c_int, [C.c_int]),
     "pkv_get_decode_kernel": (C.c_int, []),
     "pkv_status_string": (C.c_char_p, [C.c_int]),
@@ -472,6 +481,17 @@ class StepScratch:
         self.dst = np.empty(max(max_seqs, 1), np.int32)
         self.ncow = np.zeros(1, np.int32)
         self.addr = (self.src.ctypes.data, self.dst.ctypes.data, self.ncow.ctypes.data)
+
+
+def pkv_copy_segments(pairs, stream) -> None:
+    """One-launch copy of [(dst tensor, src tensor), ...] (same byte sizes; device or pinned host memory)."""
+    segs = (CopySegment * max(1, len(pairs)))()
+    for i, (dst, src) in enumerate(pairs):
+        nb = src.numel() * src.element_size()
+        if dst.numel() * dst.element_size() != nb:
+            raise ValueError("pkv_copy_segments: sizes differ")
+        segs[i].dst, segs[i].src, segs[i].bytes = dst.data_ptr(), src.data_ptr(), nb
+    _check(load().pkv_copy_segments(segs, len(pairs), stream), "pkv_copy_segments")
 
 
 def current_stream_handle(device_index: int) -> int:

@@ -139,6 +139,31 @@ cudaError_t run_append(const AppendArgs &a) {
   return a.head_dim == 128 ? dispatch_append_d<128>(a) : dispatch_append_d<64>(a);
 }
 
+// Grid-stride copy over the concatenation of the segments; vector i lies in
+// the first segment whose prefix end exceeds it.
+__global__ void __launch_bounds__(256) copy_segments_kernel(const CopySegs c) {
+  // a decode launched after it as a programmatic dependent may start its
+  // prologue (lengths and tables only); it waits for this grid before it
+  // reads what this kernel writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t total = c.end[c.n - 1];
+  const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int seg = 0;
+#pragma unroll 4
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += nth) {
+    while (i >= c.end[seg]) ++seg;  // i only grows
+    const int64_t j = i - (seg ? c.end[seg - 1] : 0);
+    c.dst[seg][j] = c.src[seg][j];
+  }
+}
+
+cudaError_t run_copy_segments(const CopySegs &c, cudaStream_t stream) {
+  if (c.n <= 0 || c.end[c.n - 1] == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((c.end[c.n - 1] + 255) / 256, 1024);
+  copy_segments_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(c);
+  return cudaGetLastError();
+}
+
 cudaError_t run_copy_meta(const int32_t *src, int32_t *dst, int64_t ints, cudaStream_t stream) {
   const int64_t vecs = (ints + 3) / 4;
   if (vecs <= 0) return cudaSuccess;

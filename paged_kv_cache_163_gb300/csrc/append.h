@@ -45,6 +45,15 @@ cudaError_t run_copy_blocks(const CopyArgs &a);
 // memory (device address) to device memory; both 16-byte aligned.
 cudaError_t run_copy_meta(const int32_t *src, int32_t *dst, int64_t ints, cudaStream_t stream);
 
+// Copy segments (16-byte vectors; sizes validated by the caller): one launch.
+struct CopySegs {
+  int4 *dst[PKV_MAX_COPY_SEGMENTS];
+  const int4 *src[PKV_MAX_COPY_SEGMENTS];
+  int64_t end[PKV_MAX_COPY_SEGMENTS];  // inclusive prefix sums of the segments' vector counts
+  int32_t n;
+};
+cudaError_t run_copy_segments(const CopySegs &c, cudaStream_t stream);
+
 // Launch with the caller's validation (the step executor's); count the launch.
 pkv_status append_unchecked(const AppendArgs &a);
 pkv_status copy_blocks_unchecked(const CopyArgs &a);

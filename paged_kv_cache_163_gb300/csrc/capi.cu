@@ -290,6 +290,28 @@ pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int
   return PKV_OK;
 }
 
+pkv_status pkv_copy_segments(const pkv_copy_segment *segs, int32_t num_segs, pkv_stream_t stream) {
+  if (num_segs < 0 || num_segs > PKV_MAX_COPY_SEGMENTS || (num_segs > 0 && !segs))
+    return fail(PKV_ERR_INVALID, "pkv_copy_segments: bad segment count");
+  CopySegs c{};
+  int64_t run = 0;
+  for (int32_t i = 0; i < num_segs; ++i) {
+    const pkv_copy_segment &g = segs[i];
+    if (g.bytes < 0 || (g.bytes & 15) || (g.bytes && (!g.dst || !g.src || !aligned16(g.dst) || !aligned16(g.src))))
+      return fail(PKV_ERR_INVALID, "pkv_copy_segments: NULL or misaligned pointer, or a size not a multiple of 16");
+    c.dst[c.n] = static_cast<int4 *>(g.dst);
+    c.src[c.n] = static_cast<const int4 *>(g.src);
+    run += g.bytes / 16;
+    c.end[c.n] = run;
+    ++c.n;
+  }
+  if (run == 0) return PKV_OK;
+  cudaError_t e = run_copy_segments(c, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_copy_segments");
+  ++t_launches;
+  return PKV_OK;
+}
+
 pkv_status paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                            int32_t num_kv_heads, int32_t head_dim,
                                            pkv_dtype q_dtype, pkv_dtype cache_dtype,

@@ -360,15 +360,22 @@ __device__ __noinline__ void merge_item(const DecodeParams &p, int item, int64_t
   for (int g = 0; g < G; ++g) {
     const float inv = den[g] > 0.f ? 1.f / den[g] : 0.f;
     const size_t at = obase + g * D;
-    if (p.out_f32) {
-      float *dst = reinterpret_cast<float *>(p.out) + at;
-#pragma unroll
-      for (int e = 0; e < DPL; e += 2)
-        *reinterpret_cast<float2 *>(dst + e) = make_float2(acc[g][e] * inv, acc[g][e + 1] * inv);
+    // one vector store a lane (whole sectors, also into page-locked host memory)
+    if constexpr (DPL == 4) {
+      if (p.out_f32) {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + at) =
+            make_float4(acc[g][0] * inv, acc[g][1] * inv, acc[g][2] * inv, acc[g][3] * inv);
+      } else {
+        *reinterpret_cast<uint2 *>(p.out + at * 2) =
+            make_uint2(pack2<QDT>(acc[g][0] * inv, acc[g][1] * inv), pack2<QDT>(acc[g][2] * inv, acc[g][3] * inv));
+      }
     } else {
-#pragma unroll
-      for (int e = 0; e < DPL; e += 2)
-        *reinterpret_cast<uint32_t *>(p.out + (at + e) * 2) = pack2<QDT>(acc[g][e] * inv, acc[g][e + 1] * inv);
+      if (p.out_f32) {
+        *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.out) + at) =
+            make_float2(acc[g][0] * inv, acc[g][1] * inv);
+      } else {
+        *reinterpret_cast<uint32_t *>(p.out + at * 2) = pack2<QDT>(acc[g][0] * inv, acc[g][1] * inv);
+      }
     }
   }
 }

@@ -235,26 +235,42 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
     for (int j = 0; j < 2; ++j) {
       const int n = 2 * q4 + j;
       if (n >= G) continue;
+      // m-tiles ib .. ib + 3 hold 8 consecutive head_dim values of this lane
+      // (out_d(g, ib + c, 0) = out_d(g, ib, 0) + 2 c): 16-byte stores, which
+      // also keep writes to page-locked host memory whole
       if (whole) {
         const float inv = (lt[j] > 0.f ? 1.f / lt[j] : 0.f) * vunit;
         const size_t row = (static_cast<size_t>(item) * G + n) * D;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int d0 = out_d<C::kCode8>(g, i, 0);
-          const float r0 = oacc[i][j] * inv, r1 = oacc[i][2 + j] * inv;
+        for (int ib = 0; ib < 8; ib += 4) {
+          const int d0 = out_d<C::kCode8>(g, ib, 0);
+          float r[8];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            r[2 * c] = oacc[ib + c][j] * inv;
+            r[2 * c + 1] = oacc[ib + c][2 + j] * inv;
+          }
           if (p.out_f32) {
-            *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.out) + row + d0) = make_float2(r0, r1);
+            float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + row + d0);
+            dst[0] = make_float4(r[0], r[1], r[2], r[3]);
+            dst[1] = make_float4(r[4], r[5], r[6], r[7]);
           } else {
-            *reinterpret_cast<uint32_t *>(p.out + (row + d0) * 2) = pack2<QDT>(r0, r1);
+            *reinterpret_cast<uint4 *>(p.out + (row + d0) * 2) =
+                make_uint4(pack2<QDT>(r[0], r[1]), pack2<QDT>(r[2], r[3]), pack2<QDT>(r[4], r[5]),
+                           pack2<QDT>(r[6], r[7]));
           }
         }
       } else {
         const int64_t slot = gw + item;
         float *op = p.ws_o + (slot * G + n) * D;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float2 *>(op + out_d<C::kCode8>(g, i, 0)) =
-              make_float2(oacc[i][j] * vunit, oacc[i][2 + j] * vunit);
+        for (int ib = 0; ib < 8; ib += 4) {
+          float4 *dst = reinterpret_cast<float4 *>(op + out_d<C::kCode8>(g, ib, 0));
+          dst[0] = make_float4(oacc[ib][j] * vunit, oacc[ib][2 + j] * vunit, oacc[ib + 1][j] * vunit,
+                               oacc[ib + 1][2 + j] * vunit);
+          dst[1] = make_float4(oacc[ib + 2][j] * vunit, oacc[ib + 2][2 + j] * vunit, oacc[ib + 3][j] * vunit,
+                               oacc[ib + 3][2 + j] * vunit);
+        }
         if (g == 0) {
           p.ws_ml[(slot * G + n) * 2] = m_run[j];
           p.ws_ml[(slot * G + n) * 2 + 1] = lt[j];

@@ -88,6 +88,8 @@ class PagedKVCache:
         self._stepper_bufs = None
         self._scratch = None
         self._graphs = False
+        self._io = None
+        self._io_key = None
         self._device_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
         self._default_scale = float(np.float32(1.0) / np.sqrt(np.float32(head_dim)))
         self.cow_pairs = []          # every (src, dst) copy, in order
@@ -287,6 +289,11 @@ class PagedKVCache:
         if out is None:
             import torch
             out = torch.empty_like(q)
+        if not (q.is_cuda and k_rows.is_cuda and v_rows.is_cuda and out.is_cuda):
+            return self._step_host_io(seq_ids, k_rows, v_rows, q, scale, out, stream, marks)
+        return self._step_native(seq_ids, k_rows, v_rows, q, scale, out, stream, marks)
+
+    def _step_native(self, seq_ids, k_rows, v_rows, q, scale, out, stream, marks):
         key = (len(seq_ids), q.shape[-2], q.dtype)
         st = self._stepper if key == self._stepper_key else self._stepper_for(*key)
         if marks is not None:
@@ -299,6 +306,33 @@ class PagedKVCache:
         if len(cs):
             self.cow_pairs.extend(zip(cs.tolist(), cd.tolist()))
         return out
+
+    def _step_host_io(self, seq_ids, k_rows, v_rows, q, scale, out, stream, marks):
+        """A step whose inputs and output are page-locked host tensors.
+
+        One copy kernel moves the step's K/V rows and queries from host to
+        device buffers (read in place over the host link; the step's first
+        decode starts its prologue meanwhile), and the decode kernels store
+        the output straight into the host tensor.  Synchronise the stream
+        before reading ``out`` on the host.
+        """
+        import torch
+        for t in (k_rows, v_rows, q, out):
+            if not t.is_cuda and not t.is_pinned():
+                raise ValueError("host tensors of a step must be page-locked (pin_memory())")
+            if not t.is_contiguous():
+                raise ValueError("tensors of a step must be contiguous")
+        key = tuple((tuple(t.shape), t.dtype) for t in (k_rows, v_rows, q))
+        if self._io_key != key:
+            self._io = [torch.empty(t.shape, dtype=t.dtype, device=self.device) for t in (k_rows, v_rows, q)]
+            self._io_key = key
+        kd, vd, qd = self._io
+        sh = capi.current_stream_handle(self._device_index) if stream is None else stream
+        ins = [(d, h) for d, h in ((kd, k_rows), (vd, v_rows), (qd, q)) if not h.is_cuda]
+        if ins:
+            capi.pkv_copy_segments(ins, sh)
+        return self._step_native(seq_ids, k_rows if k_rows.is_cuda else kd, v_rows if v_rows.is_cuda else vd,
+                                 q if q.is_cuda else qd, scale, out, stream, marks)
 
     def use_graphs(self, enable: bool = True) -> None:
         """Replay each step's attention launches from a CUDA graph (steps without copy-on-write copies).
