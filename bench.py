@@ -46,17 +46,19 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu capture), keyed by workload and by the hash of the decode kernel source it
 # was taken on; reported only while the source is unchanged.
 NCU_TRAFFIC = {
-    # decode kernel source f5d4af69c6427c89: tensor-core kernel with the step's append fused in,
-    # 16-warp CTAs for one-byte caches, one-pass merge; default "auto" variant.  dram__bytes_read.sum
-    # + dram__bytes_write.sum of one launch (the fifth decode call of a --steps 4 --warmup 3 run)
-    ("llama3-8b", "f5d4af69c6427c89"): 146_437_888,              # full capture: 142.76 MB read + 3.68 MB written
-    ("llama3-8b:bs32", "f5d4af69c6427c89"): 145_819_904,
-    ("mha7b-40layer", "f5d4af69c6427c89"): 271_355_392,
-    ("prefix-share", "f5d4af69c6427c89"): 47_947_008,
-    ("long-fp8", "f5d4af69c6427c89"): 813_543_680,               # full capture: 810.19 MB read + 3.35 MB written
-    ("long-fp8:fp8_e5m2", "f5d4af69c6427c89"): 813_330_688,
-    ("long-fp8:int8", "f5d4af69c6427c89"): 813_372_416,
-    ("long-fp8:bs32", "f5d4af69c6427c89"): 797_106_688,
+    # decode kernel source dfbcb1ed16419f52: tensor-core kernel with the step's append fused in,
+    # 16-warp CTAs for one-byte caches, 4-bit V for the mixed cache, 16-byte output stores; default
+    # "auto" variant.  dram__bytes_read.sum + dram__bytes_write.sum of one launch (the fifth decode
+    # call of a --steps 4 --warmup 3 run)
+    ("llama3-8b", "dfbcb1ed16419f52"): 146_223_360,              # full capture: 142.75 MB read + 3.47 MB written
+    ("llama3-8b:bs32", "dfbcb1ed16419f52"): 145_833_728,
+    ("mha7b-40layer", "dfbcb1ed16419f52"): 271_597_056,
+    ("prefix-share", "dfbcb1ed16419f52"): 47_972_096,
+    ("long-fp8", "dfbcb1ed16419f52"): 813_543_680,               # full capture: 810.21 MB read + 3.33 MB written
+    ("long-fp8:fp8_e5m2", "dfbcb1ed16419f52"): 813_450_496,
+    ("long-fp8:int8", "dfbcb1ed16419f52"): 813_331_968,
+    ("long-fp8:fp8_e4m3_int4", "dfbcb1ed16419f52"): 619_787_776,
+    ("long-fp8:bs32", "dfbcb1ed16419f52"): 797_107_200,
 }
 
 
