@@ -64,7 +64,7 @@ NCU_TRAFFIC = {
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cuh", "decode_mma.cuh", "common.cuh", "dtypes.h"):
+    for f in ("decode.cuh", "decode_mma.cuh", "decode_prefix.cuh", "common.cuh", "dtypes.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_163_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -451,6 +451,19 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
  * copies run eagerly.  Disabling frees the graphs.  The capture counts as no
  * launch; each replay adds its kernels to pkv_launch_count. */
 pkv_status pkv_stepper_use_graphs(pkv_stepper *st, int32_t enable);
+/* Cascade for shared prefixes (on by default; head_dim 128 with the
+ * tensor-core decode, eager steps of up to 128 sequences).  Sequences whose
+ * block tables start with the same physical blocks (forks, prefix-cache
+ * hits) form a group; when their common leading blocks that lie wholly
+ * before each member's last token make at least 16 tiles of 16 tokens, a
+ * prefix kernel streams those tiles once per KV head and attends them for
+ * every member's queries (up to 128 query rows a CTA), leaving fp32
+ * partials; the decode then attends each member's remaining tiles and merges
+ * the partials in.  The result is the same softmax, summed in another order.
+ * pkv_stepper_cascade_count: steps that used it. */
+pkv_status pkv_stepper_use_cascade(pkv_stepper *st, int32_t enable);
+int64_t pkv_stepper_cascade_count(const pkv_stepper *st);
+
 /* Graphs captured and replayed so far by this stepper. */
 pkv_status pkv_stepper_graph_stats(const pkv_stepper *st, int64_t *captures, int64_t *replays);
 

@@ -122,6 +122,8 @@ _PROTOS = {
                                      _vp, C.c_size_t, C.POINTER(_vp)]),
     "pkv_stepper_destroy": (None, [_vp]),
     "pkv_stepper_use_graphs": (C.c_int, [_vp, C.c_int32]),
+    "pkv_stepper_use_cascade": (C.c_int, [_vp, C.c_int32]),
+    "pkv_stepper_cascade_count": (C.c_int64, [_vp]),
     "pkv_stepper_graph_stats": (C.c_int, [_vp, _i64p, _i64p]),
     # pointer arguments as addresses (ints): the per-step call marshals no ctypes pointer objects
     "pkv_stepper_step": (C.c_int, [_vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int64, _vp, C.c_int64, _vp, C.c_int,
@@ -459,6 +461,14 @@ def pkv_stepper_destroy(st) -> None:
 
 def pkv_stepper_use_graphs(st, enable: bool) -> None:
     _check(load().pkv_stepper_use_graphs(st, 1 if enable else 0), "pkv_stepper_use_graphs")
+
+
+def pkv_stepper_use_cascade(st, enable: bool) -> None:
+    _check(load().pkv_stepper_use_cascade(st, 1 if enable else 0), "pkv_stepper_use_cascade")
+
+
+def pkv_stepper_cascade_count(st) -> int:
+    return int(load().pkv_stepper_cascade_count(st))
 
 
 def pkv_stepper_graph_stats(st):

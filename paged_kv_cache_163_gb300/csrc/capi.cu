@@ -98,6 +98,22 @@ MmaFn pick_mma(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
   return nullptr;
 }
 
+using PrefixFn = cudaError_t (*)(int, const DecodeParams *, const PrefixParams *, const CUtensorMap *,
+                                 const CUtensorMap *, int);
+
+PrefixFn pick_prefix(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
+  if (cache_dtype == PKV_F16 && q_dtype == PKV_F16) return prefix_call_f16;
+  if (cache_dtype == PKV_BF16 && q_dtype == PKV_BF16) return prefix_call_bf16;
+  if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_F16) return prefix_call_fp8_f16;
+  if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_BF16) return prefix_call_fp8_bf16;
+  if (cache_dtype == PKV_FP8_E5M2 && q_dtype == PKV_F16) return prefix_call_e5m2_f16;
+  if (cache_dtype == PKV_FP8_E5M2 && q_dtype == PKV_BF16) return prefix_call_e5m2_bf16;
+  if (cache_dtype == PKV_INT8 && q_dtype == PKV_F16) return prefix_call_int8_f16;
+  if (cache_dtype == PKV_INT8 && q_dtype == PKV_BF16) return prefix_call_int8_bf16;
+  if (cache_dtype == PKV_FP8_E4M3_INT4 && q_dtype == PKV_F16) return prefix_call_e4m3i4_f16;
+  return prefix_call_e4m3i4_bf16;  // dtypes validated before
+}
+
 bool use_mma(int32_t head_dim) {
   const int k = g_decode_kind.load();
   return head_dim == 128 && k != PKV_DECODE_SIMT;
@@ -173,7 +189,7 @@ int64_t ctr_bytes(int32_t num_seqs, int32_t num_kv_heads) {
 }
 
 struct DecodeLayout {
-  int64_t ctr_bytes, ml_bytes, o_bytes, total;
+  int64_t ctr_bytes, ml_bytes, o_bytes, pfx_ml_bytes, pfx_o_bytes, total;
   DecodeShape simt, mma;  // residency of the two kernel variants (mma: head_dim 128 only)
   int sms;
 };
@@ -205,7 +221,12 @@ pkv_status decode_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   lay->ctr_bytes = ctr_bytes(num_seqs, num_kv_heads);
   lay->ml_bytes = round256(slots * group * 2 * 4);
   lay->o_bytes = round256(slots * group * head_dim * 4);
-  lay->total = lay->ctr_bytes + lay->ml_bytes + lay->o_bytes;
+  // the prefix kernel's partials (cascade): up to kMaxPrefixChunks per (sequence, KV head)
+  const int64_t pfx_slots = static_cast<int64_t>(std::min<int32_t>(num_seqs, kInlineLens)) * num_kv_heads *
+                            kMaxPrefixChunks;
+  lay->pfx_ml_bytes = head_dim == 128 ? round256(pfx_slots * group * 2 * 4) : 0;
+  lay->pfx_o_bytes = head_dim == 128 ? round256(pfx_slots * group * head_dim * 4) : 0;
+  lay->total = lay->ctr_bytes + lay->ml_bytes + lay->o_bytes + lay->pfx_ml_bytes + lay->pfx_o_bytes;
   return PKV_OK;
 }
 
@@ -368,7 +389,8 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
                             const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                             int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
-                            int32_t *d_error, pkv_stream_t stream, int64_t epoch, const int32_t *host_lens) {
+                            int32_t *d_error, pkv_stream_t stream, int64_t epoch, const int32_t *host_lens,
+                            const CascadePlan *plan) {
   if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS_PER_CALL)
     return fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: num_seqs must be in [0, 1024]");
   pkv_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
@@ -461,6 +483,23 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
     } else {
       s = cache_tensor_map(v_cache, rows, esz, &tmv);
       if (s != PKV_OK) return s;
+    }
+    if (plan && plan->units > 0 && num_seqs <= kInlineLens) {
+      // the decode shares the GPU with the prefix grid: it takes the other SMs
+      grid = std::max<int64_t>(1, std::min<int64_t>(grid, static_cast<int64_t>(lay.sms) * shape.ctas_per_sm - plan->units));
+      // cascade: the prefix kernel attends the groups' shared tiles, the decode the rest
+      PrefixParams pp = plan->pp;
+      pp.ml = reinterpret_cast<float *>(ws + lay.ctr_bytes + lay.ml_bytes + lay.o_bytes);
+      pp.o = reinterpret_cast<float *>(ws + lay.ctr_bytes + lay.ml_bytes + lay.o_bytes + lay.pfx_ml_bytes);
+      p.pfx_n = num_seqs;
+      std::memcpy(p.pfx_start, plan->start, sizeof(int32_t) * static_cast<size_t>(num_seqs));
+      std::memcpy(p.pfx_chunks, plan->chunks, sizeof(int32_t) * static_cast<size_t>(num_seqs));
+      std::memcpy(p.pfx_base, plan->pp.base, sizeof(int32_t) * static_cast<size_t>(num_seqs));
+      p.pfx_ml = pp.ml;
+      p.pfx_o = pp.o;
+      e = pick_prefix(q_dtype, cache_dtype)(num_q_heads / num_kv_heads, &p, &pp, &tmk, &tmv, plan->units);
+      if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode: prefix kernel");
+      ++t_launches;
     }
     e = pick_mma(q_dtype, cache_dtype)(num_q_heads / num_kv_heads, kDecodeLaunch, &p, &tmk, &tmv,
                                        static_cast<int>(grid), &t_launches, nullptr);

@@ -130,7 +130,9 @@ __device__ __forceinline__ int2 tile_desc(const DecodeParams &p, const int32_t *
   const int nb = cum[b + 1] - cum[b];
   const int64_t r = t - static_cast<int64_t>(p.num_kv_heads) * cum[b];
   const int kvh = static_cast<int>(r / nb);
-  const int lb = static_cast<int>(r - static_cast<int64_t>(kvh) * nb);
+  const int skip = p.pfx_n ? p.pfx_start[b] : 0;  // tiles the prefix kernel attended
+  const int ls = static_cast<int>(r - static_cast<int64_t>(kvh) * nb);
+  const int lb = ls + skip;
   const int L = seq_len(p, b);
   const int ntok = min(kBS, L - lb * kBS);
   const int tpb = p.tiles_per_block;
@@ -142,7 +144,7 @@ __device__ __forceinline__ int2 tile_desc(const DecodeParams &p, const int32_t *
     x = (blk * p.num_kv_heads + kvh) * tpb + lb % tpb;
   }
   const int item = b * p.num_kv_heads + kvh;
-  return make_int2(x, (item << 7) | ((lb == 0) << 6) | ((lb == nb - 1) << 5) | ntok);
+  return make_int2(x, (item << 7) | ((ls == 0) << 6) | ((ls == nb - 1) << 5) | ntok);
 }
 
 // CTA prologue shared by the decode kernels, reading only the context lengths:
@@ -166,6 +168,7 @@ __device__ __forceinline__ void scan_blocks(const DecodeParams &p, int32_t *cum,
         report(p.d_error, PKV_DEVERR_BAD_CONTEXT_LEN);
       } else {
         nb = (L + kBS - 1) / kBS;
+        if (p.pfx_n) nb -= p.pfx_start[s];  // the prefix kernel's tiles (fewer than nb)
       }
     }
     nbk[i] = nb;
@@ -290,9 +293,17 @@ __device__ __noinline__ void merge_item(const DecodeParams &p, int item, int64_t
   const int lane = threadIdx.x & 31;
   const bool all_own = total >= nwarps;
   auto owns = [&](int64_t w) { return all_own || (w * total / nwarps) != ((w + 1) * total / nwarps); };
-  const int np = static_cast<int>(w_last - w_first + 1);
+  const int nw = static_cast<int>(w_last - w_first + 1);  // warps' partials
   const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + (w_first + item) * G;  // [k][g] = (m, l)
   const float *po = p.ws_o + (w_first + item) * G * D;                                 // [k][g][D]
+  // then the prefix kernel's partials of this item, if any (always valid)
+  const int bs = item / p.num_kv_heads;
+  const int nx = p.pfx_n ? p.pfx_chunks[bs] : 0;
+  const int64_t xs = nx ? p.pfx_base[bs] + static_cast<int64_t>(item - bs * p.num_kv_heads) * nx : 0;
+  const float2 *xml = reinterpret_cast<const float2 *>(p.pfx_ml) + xs * G;
+  const float *xo = p.pfx_o + xs * G * D;
+  const int np = nw + nx;
+  if (nx) griddep_wait();  // the prefix kernel, running beside this grid, has finished its partials
   float acc[G][DPL], run_m[G], den[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -308,7 +319,8 @@ __device__ __noinline__ void merge_item(const DecodeParams &p, int item, int64_t
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int kk = k0 + min(j0 + b, nk - 1);  // stays inside the item's slots
-      const float *src = po + static_cast<int64_t>(kk) * G * D + lane * DPL;
+      const float *src = (kk < nw ? po + static_cast<int64_t>(kk) * G * D : xo + static_cast<int64_t>(kk - nw) * G * D) +
+                         lane * DPL;
 #pragma unroll
       for (int g = 0; g < G; ++g) v[b][g] = __ldcg(reinterpret_cast<const Vec *>(src + g * D));
     }
@@ -316,10 +328,11 @@ __device__ __noinline__ void merge_item(const DecodeParams &p, int item, int64_t
   for (int k0 = 0; k0 < np; k0 += 32) {
     const int k = k0 + lane;
     const int nk = min(32, np - k0);
-    const bool mine = k < np && owns(w_first + k);
+    const bool mine = k < nw ? owns(w_first + k) : k < np;
+    const float2 *mk = k < nw ? ml + static_cast<int64_t>(k) * G : xml + static_cast<int64_t>(k - nw) * G;
     float2 mlk[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) mlk[g] = mine ? __ldcg(ml + static_cast<int64_t>(k) * G + g) : make_float2(-INFINITY, 0.f);
+    for (int g = 0; g < G; ++g) mlk[g] = mine ? __ldcg(mk + g) : make_float2(-INFINITY, 0.f);
     load_batch(k0, 0, nk);  // in flight while the weights are formed
     float wk[G];
 #pragma unroll

@@ -51,6 +51,57 @@ struct DecodeParams {
   // 0, or num_seqs: lens_inline[b] == context_lens[b] for every b (read instead of memory)
   int32_t lens_inline_n;
   int32_t lens_inline[kInlineLens];
+  // Cascade (0, or num_seqs): sequence b's first pfx_start[b] 16-token tiles
+  // were attended by the prefix kernel, which left pfx_chunks[b] partials per
+  // KV head at slots pfx_base[b] + kvh * pfx_chunks[b] of pfx_ml / pfx_o
+  // (same layout as ws_ml / ws_o); this call attends the rest and merges them in.
+  int32_t pfx_n;
+  int32_t pfx_start[kInlineLens];
+  int32_t pfx_chunks[kInlineLens];
+  int32_t pfx_base[kInlineLens];
+  const float *pfx_ml;
+  const float *pfx_o;
+};
+
+// Cascade: groups of sequences whose first tiles are the same physical
+// blocks, attended once for all members by the prefix kernel
+// (decode_prefix.cuh).
+constexpr int kMaxPrefixGroups = 16;
+constexpr int kPrefixRows = 128;  // query rows a CTA attends: 8 warps x 16
+
+struct PrefixGroup {
+  int32_t lead;        // batch index of a member (its table row holds the shared blocks)
+  int32_t tiles;       // shared 16-token tiles
+  int32_t chunks;      // tile ranges the prefix is split into
+  int32_t members;     // members in the group
+  int32_t member0;     // offset of the members in PrefixParams::member
+  int32_t row_blocks;  // ceil(members * G / 128)
+  int32_t unit0;       // first CTA of the group; CTAs [unit0, unit0 + row_blocks * chunks * Hkv)
+};
+
+struct PrefixParams {
+  int32_t num_groups;
+  PrefixGroup group[kMaxPrefixGroups];
+  int32_t member[kInlineLens];  // batch indices, group after group
+  int32_t base[kInlineLens];    // per batch index: first partial slot ([KV head][chunk] from there)
+  float *ml;                    // [slots][G][2] (max, sum), base-2 domain
+  float *o;                     // [slots][G][head_dim] unnormalised outputs
+};
+
+// Up to this many chunks of a prefix (and partials per member and KV head).
+constexpr int kMaxPrefixChunks = 16;
+// Fewer shared tiles than this are left to the decode kernel.
+constexpr int kMinPrefixTiles = 16;
+
+// A step's cascade, planned on the host from its block tables (batches of up
+// to kInlineLens sequences): the prefix kernel's groups, and per batch index
+// the tiles it attends (start), its partials per KV head (chunks) and their
+// first slot (pp.base).  attention_decode fills in pp.ml / pp.o.
+struct CascadePlan {
+  PrefixParams pp;
+  int32_t units;  // prefix kernel CTAs
+  int32_t start[kInlineLens];
+  int32_t chunks[kInlineLens];
 };
 
 // Launch `kernel` on `stream`; with programmatic != 0 the launch may begin
@@ -123,6 +174,22 @@ cudaError_t decode_mma_call_e4m3i4_f16(int group, int op, const DecodeParams *p,
 cudaError_t decode_mma_call_e4m3i4_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                         const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape);
 
+// Prefix kernel (head_dim 128): grid = the groups' units; tmk / tmv as for the tensor-core decode.
+#define PKV_PREFIX_DECL(SUF)                                                                        \
+  cudaError_t prefix_call_##SUF(int group, const DecodeParams *p, const PrefixParams *pp, const CUtensorMap *tmk, \
+                                const CUtensorMap *tmv, int grid);
+PKV_PREFIX_DECL(f16)
+PKV_PREFIX_DECL(bf16)
+PKV_PREFIX_DECL(fp8_f16)
+PKV_PREFIX_DECL(fp8_bf16)
+PKV_PREFIX_DECL(e5m2_f16)
+PKV_PREFIX_DECL(e5m2_bf16)
+PKV_PREFIX_DECL(int8_f16)
+PKV_PREFIX_DECL(int8_bf16)
+PKV_PREFIX_DECL(e4m3i4_f16)
+PKV_PREFIX_DECL(e4m3i4_bf16)
+#undef PKV_PREFIX_DECL
+
 // paged_attention_decode (k_new == v_new == NULL) or
 // paged_attention_decode_append, with a choice of launch: programmatic ==
 // true lets the kernel start while the stream's previous kernel finishes.
@@ -130,7 +197,9 @@ cudaError_t decode_mma_call_e4m3i4_bf16(int group, int op, const DecodeParams *p
 // the context lengths (the decode kernel reads those before it waits).
 // `epoch` >= 0 is one the caller reserved with take_epochs; -1 takes the
 // workspace's next one.  `host_lens`: optional host copy of context_lens,
-// passed in the launch parameters when the batch is small enough.
+// passed in the launch parameters when the batch is small enough.  `plan`:
+// optional cascade (tensor-core path only): the prefix kernel runs first and
+// the decode folds its partials in.
 pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_new, void *out, pkv_dtype out_dtype,
                             const void *q, pkv_dtype q_dtype,
                             const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
@@ -139,7 +208,7 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                             int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
                             int32_t *d_error, pkv_stream_t stream, int64_t epoch = -1,
-                            const int32_t *host_lens = nullptr);
+                            const int32_t *host_lens = nullptr, const CascadePlan *plan = nullptr);
 
 // The calling thread's launch count (pkv_launch_count), adjusted by `delta`:
 // a stream capture records launches that run only when the graph is replayed.

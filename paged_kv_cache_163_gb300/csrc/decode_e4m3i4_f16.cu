@@ -1,6 +1,7 @@
 // Decode kernel instances: cache K FP8 E4M3 + V INT4, query F16.
 #include "decode.cuh"
 #include "decode_mma.cuh"
+#include "decode_prefix.cuh"
 
 namespace pkv {
 
@@ -12,6 +13,11 @@ cudaError_t decode_call_e4m3i4_f16(int head_dim, int group, int op, const Decode
 cudaError_t decode_mma_call_e4m3i4_f16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                      const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape) {
   return decode_mma_family<PKV_FP8_E4M3_INT4, PKV_F16>(group, op, p, tmk, tmv, grid, launches, shape);
+}
+
+cudaError_t prefix_call_e4m3i4_f16(int group, const DecodeParams *p, const PrefixParams *pp, const CUtensorMap *tmk,
+                                   const CUtensorMap *tmv, int grid) {
+  return prefix_family<PKV_FP8_E4M3_INT4, PKV_F16>(group, p, pp, tmk, tmv, grid);
 }
 
 }  // namespace pkv

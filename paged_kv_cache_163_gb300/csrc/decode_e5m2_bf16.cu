@@ -1,6 +1,7 @@
 // Decode kernel instances: cache FP8 E5M2, query BF16.
 #include "decode.cuh"
 #include "decode_mma.cuh"
+#include "decode_prefix.cuh"
 
 namespace pkv {
 
@@ -12,6 +13,11 @@ cudaError_t decode_call_e5m2_bf16(int head_dim, int group, int op, const DecodeP
 cudaError_t decode_mma_call_e5m2_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                  const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape) {
   return decode_mma_family<PKV_FP8_E5M2, PKV_BF16>(group, op, p, tmk, tmv, grid, launches, shape);
+}
+
+cudaError_t prefix_call_e5m2_bf16(int group, const DecodeParams *p, const PrefixParams *pp, const CUtensorMap *tmk,
+                                  const CUtensorMap *tmv, int grid) {
+  return prefix_family<PKV_FP8_E5M2, PKV_BF16>(group, p, pp, tmk, tmv, grid);
 }
 
 }  // namespace pkv

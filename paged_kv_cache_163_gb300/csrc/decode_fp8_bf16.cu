@@ -1,6 +1,7 @@
 // Decode kernel instances: cache FP8_E4M3, query BF16.
 #include "decode.cuh"
 #include "decode_mma.cuh"
+#include "decode_prefix.cuh"
 
 namespace pkv {
 
@@ -12,6 +13,11 @@ cudaError_t decode_call_fp8_bf16(int head_dim, int group, int op, const DecodePa
 cudaError_t decode_mma_call_fp8_bf16(int group, int op, const DecodeParams *p, const CUtensorMap *tmk,
                                  const CUtensorMap *tmv, int grid, int64_t *launches, DecodeShape *shape) {
   return decode_mma_family<PKV_FP8_E4M3, PKV_BF16>(group, op, p, tmk, tmv, grid, launches, shape);
+}
+
+cudaError_t prefix_call_fp8_bf16(int group, const DecodeParams *p, const PrefixParams *pp, const CUtensorMap *tmk,
+                                 const CUtensorMap *tmv, int grid) {
+  return prefix_family<PKV_FP8_E4M3, PKV_BF16>(group, p, pp, tmk, tmv, grid);
 }
 
 }  // namespace pkv

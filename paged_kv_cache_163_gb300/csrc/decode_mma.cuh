@@ -201,7 +201,11 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
     fill_window(0);
     fill_window(1);
   }
-  griddep_wait();  // from here the previous kernel's writes are visible
+  // from here the previous kernel's writes are visible.  Behind a prefix
+  // kernel (cascade) that kernel's predecessors are done already (it waited
+  // for them before it let this grid start), and its own partials are
+  // waited for before the first merge that reads them.
+  if (!p.pfx_n) griddep_wait();
   publish_scan<C::kThreads>(p, cum, G * D * p.num_kv_heads);
   if (count <= 0) {
     griddep_launch_dependents();
@@ -222,6 +226,9 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
   bool whole_start = false, saw_last = false;
 
   auto flush = [&](int item, bool whole) {
+    // an item with prefix-kernel partials always merges (its own share is one partial)
+    const bool prefixed = p.pfx_n && p.pfx_chunks[item / p.num_kv_heads] > 0;
+    const bool direct = whole && !prefixed;
     float lt[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -238,7 +245,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       // m-tiles ib .. ib + 3 hold 8 consecutive head_dim values of this lane
       // (out_d(g, ib + c, 0) = out_d(g, ib, 0) + 2 c): 16-byte stores, which
       // also keep writes to page-locked host memory whole
-      if (whole) {
+      if (direct) {
         const float inv = (lt[j] > 0.f ? 1.f / lt[j] : 0.f) * vunit;
         const size_t row = (static_cast<size_t>(item) * G + n) * D;
 #pragma unroll
@@ -278,7 +285,13 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       }
     }
     // merge batches sized to the register budget (one-byte instances: 128 a thread)
-    if (!whole) finish_partial<D, G, QDT, C::kCode8 ? 8 : 32>(p, cum, item, total, nwarps);
+    if (!whole) {
+      finish_partial<D, G, QDT, C::kCode8 ? 8 : 32>(p, cum, item, total, nwarps);
+    } else if (prefixed) {  // the only share of the item: merge with the prefix partials now
+      __threadfence_block();
+      __syncwarp();
+      merge_item<D, G, QDT, C::kCode8 ? 8 : 32>(p, item, gw, gw, total, nwarps);
+    }
   };
 
   // tokens whose V rows this lane reads (B-fragment k rows of P^T)

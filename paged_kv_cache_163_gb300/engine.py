@@ -88,6 +88,7 @@ class PagedKVCache:
         self._stepper_bufs = None
         self._scratch = None
         self._graphs = False
+        self._cascade = True
         self._io = None
         self._io_key = None
         self._device_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
@@ -271,6 +272,8 @@ class PagedKVCache:
         self._stepper = capi.pkv_stepper_create(pool, n, max_blocks, host, dev, ws)
         if self._graphs:
             capi.pkv_stepper_use_graphs(self._stepper, True)
+        if not self._cascade:
+            capi.pkv_stepper_use_cascade(self._stepper, False)
         self._stepper_bufs = (host, dev, ws)
         self._stepper_key = key
         self._scratch = capi.StepScratch(n)
@@ -343,6 +346,16 @@ class PagedKVCache:
         self._graphs = bool(enable)
         if self._stepper is not None:
             capi.pkv_stepper_use_graphs(self._stepper, self._graphs)
+
+    def use_cascade(self, enable: bool = True) -> None:
+        """Attend shared prefixes once for all sharing sequences (prefix kernel + merge); on by default."""
+        self._cascade = bool(enable)
+        if self._stepper is not None:
+            capi.pkv_stepper_use_cascade(self._stepper, self._cascade)
+
+    def cascade_count(self) -> int:
+        """Steps of the current step executor that used the cascade."""
+        return capi.pkv_stepper_cascade_count(self._stepper) if self._stepper is not None else 0
 
     def graph_stats(self):
         """(graphs captured, graphs replayed) by the current step executor."""

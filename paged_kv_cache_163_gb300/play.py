@@ -51,13 +51,15 @@ def step_inputs(w: Workload, step: int = 0, device="cuda"):
     return k, v, q
 
 
-def run(w: Workload, device="cuda", poison=False, alloc_order=None, out_dtype=None):
+def run(w: Workload, device="cuda", poison=False, alloc_order=None, out_dtype=None, cascade=True):
     """Pre-fill, then one decode step; returns (cache, out [layers, B, Hq, D]).
 
     ``out_dtype``: None for the query's dtype, "f32" for the fp32 result.
+    ``cascade``: let the step attend shared prefixes with the prefix kernel.
     """
     import torch
     cache = new_cache(w, device, poison, alloc_order)
+    cache.use_cascade(cascade)
     prefill(w, cache, device)
     k, v, q = step_inputs(w, 0, device)
     out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out_dtype == "f32" else None

@@ -63,7 +63,9 @@ def check_cache_bytes(cache, o, w, layer=0):
 
 
 def full_oracle_check(play, w, layers=1):
-    cache, out = play.run(w, poison=True, out_dtype="f32")
+    # without the cascade: the 16-bit check below decodes again by the public call, which must
+    # sum in the same order (the cascade has its own tests)
+    cache, out = play.run(w, poison=True, out_dtype="f32", cascade=False)
     assert cache.check() == 0
     o = oracle_play(w, layers=1)
     check_tables(cache, o, w.seq_ids)

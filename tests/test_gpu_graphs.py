@@ -64,6 +64,8 @@ def test_replayed_steps_equal_eager_steps(play, cache_dtype, layers):
     from paged_kv_cache_163_gb300 import capi
     w = _workload(cache_dtype, layers, seed=60 + layers)
     eager, graph = play.new_cache(w, poison=True), play.new_cache(w, poison=True)
+    for c in (eager, graph):                 # graph replays attend without the cascade: compare like with like
+        c.use_cascade(False)
     play.prefill(w, eager)
     play.prefill(w, graph)
     graph.use_graphs(True)
@@ -92,6 +94,8 @@ def test_replayed_steps_equal_eager_steps(play, cache_dtype, layers):
 def test_copy_on_write_step_runs_eagerly_and_replays_resume(play):
     w = _workload("bf16", 2, seed=70, n=6)
     eager, graph = play.new_cache(w, poison=True), play.new_cache(w, poison=True)
+    for c in (eager, graph):                 # graph replays attend without the cascade: compare like with like
+        c.use_cascade(False)
     play.prefill(w, eager)
     play.prefill(w, graph)
     graph.use_graphs(True)
@@ -119,6 +123,8 @@ def test_copy_on_write_step_runs_eagerly_and_replays_resume(play):
 def test_new_buffers_capture_again(play):
     w = _workload("bf16", 1, seed=71)
     eager, graph = play.new_cache(w, poison=True), play.new_cache(w, poison=True)
+    for c in (eager, graph):                 # graph replays attend without the cascade: compare like with like
+        c.use_cascade(False)
     play.prefill(w, eager)
     play.prefill(w, graph)
     graph.use_graphs(True)
@@ -146,6 +152,8 @@ def test_other_calls_on_the_workspace_between_replays(play):
     """A public decode call on the stepper's workspace shifts the counter-bank parity: steps stay right."""
     w = _workload("bf16", 1, seed=72)
     eager, graph = play.new_cache(w, poison=True), play.new_cache(w, poison=True)
+    for c in (eager, graph):                 # graph replays attend without the cascade: compare like with like
+        c.use_cascade(False)
     play.prefill(w, eager)
     play.prefill(w, graph)
     graph.use_graphs(True)

@@ -46,7 +46,7 @@ def test_shared_prefix_equals_private_copies(play, cache_dtype):
     lens = [prefix + s for s in (64, 100, 512, 77, 1, 300, 250, 129)]
     w = wl.custom("share", lens=lens, num_q_heads=32, num_kv_heads=8, head_dim=128, q_dtype="bf16",
                   cache_dtype=cache_dtype, prefix_len=prefix, seed=21)
-    shared, out_shared = play.run(w)
+    shared, out_shared = play.run(w, cascade=False)   # same summation order as the private copies
     assert len(shared.cow_pairs) == len(lens) - 1
     # private copies: every sequence appends the whole prefix itself
     from paged_kv_cache_163_gb300.engine import PagedKVCache
