@@ -17,11 +17,11 @@
 // streams the members' own tiles meanwhile, and waits for this grid only
 // before its first merge that reads these partials.
 //
-// A CTA: 8 compute warps of 16 query rows each (two MMA n-tiles of 8), and
+// A CTA: compute warps of 8 kNT query rows each (kNT MMA n-tiles of 8), and
 // one producer warp that streams the chunk's K / V tiles (the tensor-core
 // decode's layout and TMA maps) through an 8-stage ring with full / empty
 // mbarriers.  Per tile a compute warp does the decode's K Q^T and V^T P^T
-// MMAs for both n-tiles, sharing the K and V fragment conversion between
+// MMAs for its n-tiles, sharing the K and V fragment conversion between
 // them.  Prefix tiles are always full (16 tokens).
 #pragma once
 
@@ -32,12 +32,13 @@ namespace pkv {
 template <int G, int CDT, int QDT>
 struct PrefixCfg {
   using M = MmaCfg<G, CDT, QDT>;
-  static constexpr int kWarps = 8;  // compute warps
+  static constexpr int kNT = 2;                          // MMA n-tiles (8 query rows each) a warp
+  static constexpr int kWarps = kPrefixRows / (8 * kNT);  // compute warps
   static constexpr int kThreads = (kWarps + 1) * 32;
   static constexpr int kStages = 8;
   static constexpr int kStage = round_up_c(M::kKV + 2 * M::kScale, 1024);  // K, V (swizzled, 1024-aligned), scales
   static constexpr int kSmem = 1024 + kStages * kStage + 128;
-  static_assert(kWarps * 16 == kPrefixRows, "rows per CTA");
+  static_assert(kWarps * 8 * kNT == kPrefixRows, "rows per CTA");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -124,13 +125,14 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
     return;
   }
 
-  // ---- compute warps: rows r0 .. r0 + 15 of the group's (member, head) rows ----
-  const int r0 = rb * kPrefixRows + warp * 16;
+  // ---- compute warps: rows r0 .. r0 + 8 NT - 1 of the group's (member, head) rows ----
+  constexpr int NT = PC::kNT;
+  const int r0 = rb * kPrefixRows + warp * 8 * NT;
   const int hq = p.num_kv_heads * G;
-  // Q^T B fragments for n-tiles 0 and 1 (column g = row r0 + 8 nt + g)
-  uint32_t qb[2][8][2];
+  // Q^T B fragments per n-tile (column g = row r0 + 8 nt + g)
+  uint32_t qb[NT][8][2];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  for (int nt = 0; nt < NT; ++nt) {
     const int rn = r0 + 8 * nt + g;
     const int mi = rn / G, gr = rn - (rn / G) * G;
     const uint8_t *qrow = nullptr;
@@ -153,10 +155,10 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
       }
     }
   }
-  float oacc[2][8][4];
-  float m_run[2][2], l_run[2][2];
+  float oacc[NT][8][4];
+  float m_run[NT][2], l_run[NT][2];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
     const uint8_t *vt = kt + C::kTile;
     const uint8_t *ab = kt + C::kKV;
     // ---- S^T = K Q^T for both n-tiles ----
-    float sacc4[2][2][4] = {};  // [n-tile][chain][c]
+    float sacc4[NT][2][4] = {};  // [n-tile][chain][c]
     if constexpr (C::kCode8) {
       uint4 kr[2][2];
 #pragma unroll
@@ -196,8 +198,8 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
         uint32_t a[4];
         code4_to_f16x2<C::KT>(word(kr[0][s >> 2], s & 3), a[0], a[2]);
         code4_to_f16x2<C::KT>(word(kr[1][s >> 2], s & 3), a[1], a[3]);
-        mma_16816(sacc4[0][s & 1], a, qb[0][s][0], qb[0][s][1], false);
-        mma_16816(sacc4[1][s & 1], a, qb[1][s][0], qb[1][s][1], false);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(sacc4[nt][s & 1], a, qb[nt][s][0], qb[nt][s][1], false);
       }
     } else {
       uint4 kr[2][2][2];
@@ -215,8 +217,8 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
         const int h = s >> 2, j = (s & 3) >> 1, t = s & 1;
         const uint32_t a[4] = {word(kr[0][h][j], 2 * t), word(kr[1][h][j], 2 * t), word(kr[0][h][j], 2 * t + 1),
                                word(kr[1][h][j], 2 * t + 1)};
-        mma_16816(sacc4[0][s & 1], a, qb[0][s][0], qb[0][s][1], C::kBf16);
-        mma_16816(sacc4[1][s & 1], a, qb[1][s][0], qb[1][s][1], C::kBf16);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(sacc4[nt][s & 1], a, qb[nt][s][0], qb[nt][s][1], C::kBf16);
       }
     }
     // ---- scale, online softmax (base 2); V scales relative to the tile's largest ----
@@ -239,9 +241,9 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
       ru = vunit * rv;
       vunit = vmax;
     }
-    uint32_t pb[2][2][2];  // [n-tile][hi / lo][b0, b1]
+    uint32_t pb[NT][2][2];  // [n-tile][hi / lo][b0, b1]
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
       float sacc[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) sacc[c] = sacc4[nt][0][c] + sacc4[nt][1][c];
@@ -300,8 +302,8 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
           uint32_t a[4];
           int4_pair_to_f16x2(prmt(x0, y0, vsel[b]), a[0], a[1]);
           int4_pair_to_f16x2(prmt(x1, y1, vsel[b]), a[2], a[3]);
-          mma_16816(oacc[0][4 * w + b], a, pb[0][0][0], pb[0][0][1], false);
-          mma_16816(oacc[1][4 * w + b], a, pb[1][0][0], pb[1][0][1], false);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[nt][4 * w + b], a, pb[nt][0][0], pb[nt][0][1], false);
         }
       }
     } else if constexpr (C::kCode8) {
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
         code4_to_f16x2<C::VT>(prmt(x0, y0, 0x7362), b[0], b[1]);
         code4_to_f16x2<C::VT>(prmt(x1, y1, 0x7362), b[2], b[3]);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
           mma_16816(oacc[nt][2 * w], a, pb[nt][0][0], pb[nt][0][1], false);
           mma_16816(oacc[nt][2 * w + 1], b, pb[nt][0][0], pb[nt][0][1], false);
         }
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
         const uint32_t a[4] = {prmt(x0, y0, 0x5410), prmt(x0, y0, 0x7632), prmt(x1, y1, 0x5410),
                                prmt(x1, y1, 0x7632)};
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
           mma_16816(oacc[nt][m], a, pb[nt][0][0], pb[nt][0][1], C::kBf16);
           if constexpr (C::kBf16) mma_16816(oacc[nt][m], a, pb[nt][1][0], pb[nt][1][1], true);
         }
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
 
   // ---- partials: rows r0 + 8 nt + 2 q4 + j ----
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       float lt = l_run[nt][j];
