@@ -46,19 +46,20 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu capture), keyed by workload and by the hash of the decode kernel source it
 # was taken on; reported only while the source is unchanged.
 NCU_TRAFFIC = {
-    # decode kernel source dfbcb1ed16419f52: tensor-core kernel with the step's append fused in,
-    # 16-warp CTAs for one-byte caches, 4-bit V for the mixed cache, 16-byte output stores; default
-    # "auto" variant.  dram__bytes_read.sum + dram__bytes_write.sum of one launch (the fifth decode
-    # call of a --steps 4 --warmup 3 run)
-    ("llama3-8b", "dfbcb1ed16419f52"): 146_223_360,              # full capture: 142.75 MB read + 3.47 MB written
-    ("llama3-8b:bs32", "dfbcb1ed16419f52"): 145_833_728,
-    ("mha7b-40layer", "dfbcb1ed16419f52"): 271_597_056,
-    ("prefix-share", "dfbcb1ed16419f52"): 47_972_096,
-    ("long-fp8", "dfbcb1ed16419f52"): 813_543_680,               # full capture: 810.21 MB read + 3.33 MB written
-    ("long-fp8:fp8_e5m2", "dfbcb1ed16419f52"): 813_450_496,
-    ("long-fp8:int8", "dfbcb1ed16419f52"): 813_331_968,
-    ("long-fp8:fp8_e4m3_int4", "dfbcb1ed16419f52"): 619_787_776,
-    ("long-fp8:bs32", "dfbcb1ed16419f52"): 797_107_200,
+    # decode kernel source e0c71427bd962c48: tensor-core kernel with the step's append fused in, 16-warp
+    # CTAs for one-byte caches, 4-bit V for the mixed cache, 16-byte output stores, cascade for
+    # shared prefixes; default "auto" variant.  dram__bytes_read.sum + dram__bytes_write.sum of one
+    # call (the fifth decode call of a --steps 4 --warmup 3 run; prefix-share: its prefix kernel
+    # plus its decode, whose DRAM reads include the prefix partials ncu's replay flushed from L2)
+    ("llama3-8b", "e0c71427bd962c48"): 146_108_672,              # full capture: 142.76 MB read + 3.35 MB written
+    ("llama3-8b:bs32", "e0c71427bd962c48"): 145_810_944,
+    ("mha7b-40layer", "e0c71427bd962c48"): 271_581_184,
+    ("prefix-share", "e0c71427bd962c48"): 52_875_520,
+    ("long-fp8", "e0c71427bd962c48"): 813_658_624,               # full capture: 810.28 MB read + 3.37 MB written
+    ("long-fp8:fp8_e5m2", "e0c71427bd962c48"): 813_417_984,
+    ("long-fp8:int8", "e0c71427bd962c48"): 813_433_856,
+    ("long-fp8:fp8_e4m3_int4", "e0c71427bd962c48"): 619_795_712,
+    ("long-fp8:bs32", "e0c71427bd962c48"): 797_102_592,
 }
 
 
