@@ -383,6 +383,8 @@ def run_ours(args, world, rank, local):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(t_total * 1e3 / args.steps, 4),
+        # spread of the timed steps on this rank (CUDA events around each step)
+        "step_ms_percentiles": {f"p{q}": round(float(np.percentile(step_ms, q)), 4) for q in (10, 50, 90)},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
