@@ -29,9 +29,13 @@
  *  - Cache layout, per layer: k_cache, v_cache
  *    [num_blocks][num_kv_heads][block_size][head_dim] (the V cache of
  *    FP8_E4M3_INT4 holds head_dim / 2 bytes a row); coded caches
- *    (FP8_E4M3, FP8_E5M2, INT8, FP8_E4M3_INT4) also have scales k_scale,
- *    v_scale float32 [num_blocks][num_kv_heads][block_size].  block_size is
- *    16 or 32.
+ *    (FP8_E4M3, FP8_E5M2, INT8, FP8_E4M3_INT4) also have one float32 scale
+ *    array [num_blocks][num_kv_heads][2][block_size]: a (block, head)'s K
+ *    scales, then its V scales.  Calls take it as k_scale (its start) and
+ *    v_scale, which must be k_scale + block_size, and fail with
+ *    PKV_ERR_INVALID otherwise.  With 16-token blocks the K and V scales of
+ *    a block's tokens are then one 128-byte unit, read with one copy.
+ *    block_size is 16 or 32.
  *    Token n of a sequence lives at slot
  *    table[n / block_size] * block_size + n % block_size.
  *  - Several layers are several calls with per-layer cache pointers.
@@ -260,7 +264,9 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
  *   FP8_E4M3_INT4: K rows as FP8_E4M3; V rows R = 7, Q = nearest integer,
  *             ties to even, clamped to [-7, 7], stored two a byte as
  *             code + 8 (even element in the low nibble);
- * the scale goes to k_scale / v_scale at the same slot. */
+ * the scale of slot (block, offset), head h goes to
+ * k_scale[((block * num_kv_heads + h) * 2) * block_size + offset] (K) and
+ * to v_scale at the same index (V). */
 pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int32_t num_tokens,
                            int32_t num_kv_heads, int32_t head_dim, const int32_t *slot_mapping,
                            void *k_cache, void *v_cache, pkv_dtype cache_dtype, float *k_scale,
@@ -381,7 +387,8 @@ typedef struct {
   pkv_dtype q_dtype, cache_dtype;
   void *k_cache, *v_cache;          /* layer 0; layer l at + l * cache_layer_stride bytes */
   int64_t cache_layer_stride;
-  float *k_scale, *v_scale;         /* coded caches only (else NULL); layer l at + l * scale_layer_stride bytes */
+  float *k_scale, *v_scale;         /* coded caches only (else NULL): v_scale = k_scale + block_size;
+                                       layer l at + l * scale_layer_stride bytes */
   int64_t scale_layer_stride;
   int32_t block_size;               /* 16 or 32: must match the block manager's */
   int64_t v_cache_layer_stride;     /* V layer stride in bytes; 0: the same as cache_layer_stride */

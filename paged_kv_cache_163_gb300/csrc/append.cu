@@ -55,11 +55,12 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t *__restrict__
   }
   const int64_t blk = slot / bs;
   const int off = slot % bs;
-  const int64_t row = (blk * num_kv_heads + h) * bs + off;  // index of the cache row
+  const int64_t row = (blk * num_kv_heads + h) * bs + off;        // index of the cache row
+  const int64_t srow = (blk * num_kv_heads + h) * 2 * bs + off;  // of its scale (K and V side by side)
   if (kind)
-    append_row<D, IDT, v_part(CDT)>(v + th * D * 2, v_cache, v_scale, row, lane);
+    append_row<D, IDT, v_part(CDT)>(v + th * D * 2, v_cache, v_scale, row, srow, lane);
   else
-    append_row<D, IDT, k_part(CDT)>(k + th * D * 2, k_cache, k_scale, row, lane);
+    append_row<D, IDT, k_part(CDT)>(k + th * D * 2, k_cache, k_scale, row, srow, lane);
 }
 
 // Step metadata: page-locked host staging -> device, 16-byte vectors.  A
@@ -74,9 +75,9 @@ __global__ void __launch_bounds__(256) copy_meta_kernel(const int4 *__restrict__
 }
 
 // One CTA per (pair, K-or-V): copies a whole physical block (all heads, all
-// slots) and, for coded caches, its scales.
-__global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t *k_cache, uint8_t *v_cache,
-                                                          float *k_scale, float *v_scale,
+// slots); for coded caches the K CTA also copies the block's scales, which
+// are one contiguous run (K and V scales side by side per head).
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t *k_cache, uint8_t *v_cache, float *scales,
                                                           const int32_t *__restrict__ src,
                                                           const int32_t *__restrict__ dst,
                                                           int64_t k_block_bytes, int64_t v_block_bytes,
@@ -95,10 +96,9 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t *k_cache, uint
   uint4 *dp = reinterpret_cast<uint4 *>(base + d * block_bytes);
   const int64_t n16 = block_bytes / 16;
   for (int64_t i = threadIdx.x; i < n16; i += blockDim.x) dp[i] = sp[i];
-  float *sc = kind ? v_scale : k_scale;
-  if (sc) {
+  if (scales && kind == 0) {
     for (int i = threadIdx.x; i < scale_elems; i += blockDim.x)
-      sc[static_cast<int64_t>(d) * scale_elems + i] = sc[static_cast<int64_t>(s) * scale_elems + i];
+      scales[static_cast<int64_t>(d) * scale_elems + i] = scales[static_cast<int64_t>(s) * scale_elems + i];
   }
 }
 
@@ -179,12 +179,11 @@ cudaError_t run_copy_blocks(const CopyArgs &a) {
   const int64_t rows = static_cast<int64_t>(a.num_kv_heads) * a.block_size;
   const int64_t k_bytes = rows * row_bytes(k_part(a.cache_dtype), a.head_dim);
   const int64_t v_bytes = rows * row_bytes(v_part(a.cache_dtype), a.head_dim);
-  const int32_t scale_elems = a.num_kv_heads * a.block_size;
+  const int32_t scale_elems = 2 * a.num_kv_heads * a.block_size;  // K and V scales of a block
   dim3 grid(a.num_pairs, 2);
   copy_blocks_kernel<<<grid, 256, 0, a.stream>>>(
-      static_cast<uint8_t *>(a.k_cache), static_cast<uint8_t *>(a.v_cache),
-      scaled ? a.k_scale : nullptr, scaled ? a.v_scale : nullptr, a.src, a.dst, k_bytes, v_bytes, scale_elems,
-      a.num_blocks, a.d_error);
+      static_cast<uint8_t *>(a.k_cache), static_cast<uint8_t *>(a.v_cache), scaled ? a.k_scale : nullptr, a.src,
+      a.dst, k_bytes, v_bytes, scale_elems, a.num_blocks, a.d_error);
   return cudaGetLastError();
 }
 

@@ -270,8 +270,8 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
   if (num_pairs > 65535) return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: at most 65535 pairs per call");
   if (!k_cache || !v_cache || !src || !dst || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: NULL or misaligned pointer");
-  if (has_scales(cache_dtype) && (!k_scale || !v_scale))
-    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: a coded cache needs k_scale and v_scale");
+  if (has_scales(cache_dtype) && (!k_scale || v_scale != k_scale + block_size))
+    return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: a coded cache needs k_scale, and v_scale = k_scale + block_size");
   CopyArgs a{k_cache, v_cache, k_scale, v_scale, src, dst, num_pairs, num_kv_heads,
              head_dim, cache_dtype, num_blocks, d_error, reinterpret_cast<cudaStream_t>(stream), block_size};
   cudaError_t e = run_copy_blocks(a);
@@ -300,8 +300,8 @@ pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int
   if (!k || !v || !slot_mapping || !k_cache || !v_cache || !aligned16(k) || !aligned16(v) ||
       !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PKV_ERR_INVALID, "paged_kv_append: NULL or misaligned pointer");
-  if (has_scales(cache_dtype) && (!k_scale || !v_scale))
-    return fail(PKV_ERR_INVALID, "paged_kv_append: a coded cache needs k_scale and v_scale");
+  if (has_scales(cache_dtype) && (!k_scale || v_scale != k_scale + block_size))
+    return fail(PKV_ERR_INVALID, "paged_kv_append: a coded cache needs k_scale, and v_scale = k_scale + block_size");
   AppendArgs a{k, v, in_dtype, num_tokens, num_kv_heads, head_dim, slot_mapping, k_cache, v_cache,
                cache_dtype, k_scale, v_scale, num_blocks, d_error,
                reinterpret_cast<cudaStream_t>(stream), block_size};
@@ -410,9 +410,9 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
       !aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(workspace))
     return fail(PKV_ERR_INVALID, "paged_attention_decode: NULL or misaligned pointer");
-  if (has_scales(cache_dtype) &&
-      (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
-    return fail(PKV_ERR_INVALID, "paged_attention_decode: a coded cache needs aligned k_scale and v_scale");
+  if (has_scales(cache_dtype) && (!k_scale || !aligned16(k_scale) || v_scale != k_scale + block_size))
+    return fail(PKV_ERR_INVALID,
+                "paged_attention_decode: a coded cache needs an aligned k_scale, and v_scale = k_scale + block_size");
   if ((k_new != nullptr) != (v_new != nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
     return fail(PKV_ERR_INVALID, "paged_attention_decode_append: k_new and v_new must both be given, 16-byte aligned");
   DecodeLayout lay;

@@ -253,17 +253,28 @@ __device__ __forceinline__ void store_slice(uint8_t *dst, uint2 r) {
   }
 }
 
+// Scales of coded caches: one fp32 array [blocks][heads][2][block_size],
+// a (block, head)'s K scales followed by its V scales (v_scale = k_scale +
+// block_size), so with 16-token blocks the K and V scales of a tile are one
+// 128-byte unit.  Index, from k_scale or v_scale, of the first scale of
+// 16-token tile `tile` = (block * heads + head) * tiles per block + tile in
+// the block (tiles per block: 1 or 2).
+__device__ __forceinline__ int64_t scale_index(int64_t tile, int tpb) {
+  return tpb == 1 ? tile * 32 : (tile >> 1) * 64 + (tile & 1) * 16;
+}
+
 // Encode `src_row` and store it as cache row `row` (index into
-// [blocks][heads][block_size]); lane 0 stores the scale of coded storage.
+// [blocks][heads][block_size]); lane 0 stores the scale of coded storage at
+// scales[srow].
 template <int D, int IDT, int CDT>
 __device__ __forceinline__ void append_row(const uint8_t *src_row, uint8_t *cache, float *scales, int64_t row,
-                                           int lane) {
+                                           int64_t srow, int lane) {
   float s;
   const uint2 r = encode_slice<D, IDT, CDT>(src_row, lane, s);
   constexpr int B = slice_bytes<D, CDT>();
   store_slice<D, CDT>(cache + row * (B * 32) + lane * B, r);
   if constexpr (is_coded(CDT)) {
-    if (lane == 0) scales[row] = s;
+    if (lane == 0) scales[srow] = s;
   }
 }
 

@@ -459,9 +459,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
           const size_t tile = static_cast<size_t>(d.x);
           bulk_g2s(sb, p.k_cache + tile * C::kTile, C::kTile, bars + st, pol);
           bulk_g2s(sb + C::kOffV, p.v_cache + tile * C::kVTile, C::kVTile, bars + st, pol);
-          if constexpr (C::kScale > 0) {
-            bulk_g2s(sb + C::kOffKS, p.k_scale + tile * kBS, C::kScale, bars + st, pol);
-            bulk_g2s(sb + C::kOffVS, p.v_scale + tile * kBS, C::kScale, bars + st, pol);
+          if constexpr (C::kScale > 0) {  // one 128-byte unit for 16-token blocks
+            const int64_t si = scale_index(static_cast<int64_t>(tile), p.tiles_per_block);
+            if (p.tiles_per_block == 1) {
+              bulk_g2s(sb + C::kOffKS, p.k_scale + si, 2 * C::kScale, bars + st, pol);
+            } else {
+              bulk_g2s(sb + C::kOffKS, p.k_scale + si, C::kScale, bars + st, pol);
+              bulk_g2s(sb + C::kOffVS, p.v_scale + si, C::kScale, bars + st, pol);
+            }
           }
         }
         if (need_q) bulk_g2s(sb + C::kOffQ, p.q + static_cast<size_t>(item) * C::kQ, C::kQ, bars + st);
@@ -610,8 +615,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, G, CDT, QDT>::kThreads, 1)
         if (lane == 0) {
           reinterpret_cast<float *>(sb + C::kOffKS)[r] = kscl;
           reinterpret_cast<float *>(sb + C::kOffVS)[r] = vscl;
-          const_cast<float *>(p.k_scale)[grow] = kscl;
-          const_cast<float *>(p.v_scale)[grow] = vscl;
+          const int64_t gs = scale_index(d.x, p.tiles_per_block) + r;
+          const_cast<float *>(p.k_scale)[gs] = kscl;
+          const_cast<float *>(p.v_scale)[gs] = vscl;
         }
       }
       __syncwarp();

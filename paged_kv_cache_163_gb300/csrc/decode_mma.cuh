@@ -179,8 +179,13 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
             } else {
               tma_load_2d(tb + C::kTile, &tmv, 0, row, bars + st, pol);
             }
-            bulk_g2s(ab, p.k_scale + tile * kBS, C::kScale, bars + st, pol);
-            bulk_g2s(ab + C::kScale, p.v_scale + tile * kBS, C::kScale, bars + st, pol);
+            const int64_t si = scale_index(tile, p.tiles_per_block);
+            if (p.tiles_per_block == 1) {  // K and V scales: one 128-byte unit
+              bulk_g2s(ab, p.k_scale + si, 2 * C::kScale, bars + st, pol);
+            } else {
+              bulk_g2s(ab, p.k_scale + si, C::kScale, bars + st, pol);
+              bulk_g2s(ab + C::kScale, p.v_scale + si, C::kScale, bars + st, pol);
+            }
           } else {
             tma_load_2d(tb, &tmk, 0, row, bars + st, pol);
             tma_load_2d(tb + 2048, &tmk, 64, row, bars + st, pol);
@@ -377,8 +382,9 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
           float *sab = reinterpret_cast<float *>(aux + st * C::kAux);
           sab[r] = ks;
           sab[kBS + r] = vs;
-          const_cast<float *>(p.k_scale)[grow] = ks;
-          const_cast<float *>(p.v_scale)[grow] = vs;
+          const int64_t gs = scale_index(d.x, p.tiles_per_block) + r;
+          const_cast<float *>(p.k_scale)[gs] = ks;
+          const_cast<float *>(p.v_scale)[gs] = vs;
         }
       }
       __syncwarp();

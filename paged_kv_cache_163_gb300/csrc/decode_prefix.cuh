@@ -110,8 +110,13 @@ __global__ void __launch_bounds__(PrefixCfg<G, CDT, QDT>::kThreads, 1)
           } else {
             tma_load_2d(tb + C::kTile, &tmv, 0, row, full + st, pol);
           }
-          bulk_g2s(tb + C::kKV, p.k_scale + tile * kBS, C::kScale, full + st, pol);
-          bulk_g2s(tb + C::kKV + C::kScale, p.v_scale + tile * kBS, C::kScale, full + st, pol);
+          const int64_t si = scale_index(tile, p.tiles_per_block);
+          if (p.tiles_per_block == 1) {  // K and V scales: one 128-byte unit
+            bulk_g2s(tb + C::kKV, p.k_scale + si, 2 * C::kScale, full + st, pol);
+          } else {
+            bulk_g2s(tb + C::kKV, p.k_scale + si, C::kScale, full + st, pol);
+            bulk_g2s(tb + C::kKV + C::kScale, p.v_scale + si, C::kScale, full + st, pol);
+          }
         } else {
           tma_load_2d(tb, &tmk, 0, row, full + st, pol);
           tma_load_2d(tb + 2048, &tmk, 64, row, full + st, pol);

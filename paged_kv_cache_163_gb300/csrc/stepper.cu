@@ -234,7 +234,8 @@ pkv_status pkv_stepper_create(const pkv_pool_desc *pool, int32_t max_seqs, int32
   if (pool->block_size != PKV_BLOCK_SIZE && pool->block_size != PKV_BLOCK_SIZE_32)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_stepper_create: block_size must be 16 or 32");
   if (pool->num_layers <= 0 || pool->num_blocks <= 0 || pool->num_kv_heads <= 0 || !pool->k_cache ||
-      !pool->v_cache || (pkv::has_scales(pool->cache_dtype) && (!pool->k_scale || !pool->v_scale)))
+      !pool->v_cache ||
+      (pkv::has_scales(pool->cache_dtype) && (!pool->k_scale || pool->v_scale != pool->k_scale + pool->block_size)))
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_create: bad pool descriptor");
   if (!host_staging || host_staging_bytes < pkv_stepper_host_bytes(max_seqs, max_blocks_per_seq) ||
       !dev_meta || dev_meta_bytes < pkv_stepper_device_bytes(max_seqs, max_blocks_per_seq))

@@ -71,12 +71,13 @@ class PagedKVCache:
         self.k = torch.empty(shape, dtype=tdt, device=self.device)
         self.v = torch.empty(shape[:4] + (capi.v_row_elems(cache_dtype, head_dim),), dtype=tdt, device=self.device)
         if cache_dtype in capi.SCALED_CACHES:
-            self.k_scale = torch.empty(shape[:4], dtype=torch.float32, device=self.device)
-            self.v_scale = torch.empty(shape[:4], dtype=torch.float32, device=self.device)
+            # [layers][blocks][heads][2][block_size]: a (block, head)'s K scales, then its V scales
+            self._scales = torch.empty(shape[:3] + (2, block_size), dtype=torch.float32, device=self.device)
+            self.k_scale, self.v_scale = self._scales[:, :, :, 0, :], self._scales[:, :, :, 1, :]
         else:
-            self.k_scale = self.v_scale = None
+            self._scales = self.k_scale = self.v_scale = None
         if poison:  # unwritten slots read as NaN: a kernel that strays onto one shows it
-            for t in (self.k, self.v, self.k_scale, self.v_scale):
+            for t in (self.k, self.v, self._scales):
                 if t is not None:
                     t.view(torch.uint8).fill_(0xFF)
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)

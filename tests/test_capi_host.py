@@ -153,6 +153,28 @@ def test_invalid_arguments_raise():
     capi.pkv_bm_destroy(bm)
 
 
+@pytest.mark.parametrize("bs", [16, 32])
+def test_coded_caches_take_one_scale_array(bs):
+    """Scales are one array [blocks][heads][2][block_size] (K, then V): v_scale must be k_scale + block_size.
+
+    Stand-in addresses (16-byte aligned, never dereferenced): the call
+    rejects the pointers before it touches the device.
+    """
+    lib = capi.load()
+    base = 1 << 24
+    k, v, slots, kc, vc, err = base, base + 4096, base + 8192, base + 12288, base + 16384, base + 20480
+    ks = base + 65536
+    for vs in (ks + 4 * bs * 2, ks + 4 * (bs - 16), ks + 4 * bs * 64, ks):
+        st = lib.paged_kv_append(k, v, capi.PKV_BF16, 1, 2, 128, slots, kc, vc, capi.PKV_FP8_E4M3, ks, vs, 4, bs,
+                                 err, None)
+        assert capi.STATUS[st] == "PKV_ERR_INVALID"
+        st = lib.paged_kv_copy_blocks(kc, vc, ks, vs, slots, slots, 1, 2, 128, capi.PKV_INT8, 4, bs, err, None)
+        assert capi.STATUS[st] == "PKV_ERR_INVALID"
+    st = lib.paged_kv_append(k, v, capi.PKV_BF16, 1, 2, 128, slots, kc, vc, capi.PKV_FP8_E4M3, None, ks + 4 * bs, 4,
+                             bs, err, None)
+    assert capi.STATUS[st] == "PKV_ERR_INVALID"
+
+
 def test_workload_allocations_match_oracle():
     from paged_kv_cache_163_gb300 import workloads as wl
     for wid in (1, 2, 4):

@@ -35,9 +35,9 @@ def run_append(capi, rows_k, rows_v, slots, num_blocks, hkv, d, in_dtype, cache_
     kc.view(torch.uint8).fill_(0xFF)
     vc.view(torch.uint8).fill_(0xFF)
     ks = vs = None
-    if cache_dtype in SCALED_CACHES:
-        ks = torch.full((num_blocks, hkv, 16), float("nan"), device=dev)
-        vs = torch.full_like(ks, float("nan"))
+    if cache_dtype in SCALED_CACHES:  # one array: a (block, head)'s K scales, then its V scales
+        both = torch.full((num_blocks, hkv, 2, 16), float("nan"), device=dev)
+        ks, vs = both[:, :, 0], both[:, :, 1]
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     k = torch.from_numpy(rows_k).to(dev).to(torch_dtype(in_dtype))
     v = torch.from_numpy(rows_v).to(dev).to(torch_dtype(in_dtype))
@@ -261,8 +261,8 @@ def test_copy_blocks(capi, cache_dtype, d):
     kc_t, vc_t = kc.view(torch_dtype(cache_dtype)), vc.view(torch_dtype(cache_dtype))
     ks = vs = None
     if cache_dtype in SCALED_CACHES:
-        ks = torch.rand((nb, hkv, 16), generator=g).to(dev)
-        vs = torch.rand((nb, hkv, 16), generator=g).to(dev)
+        both = torch.rand((nb, hkv, 2, 16), generator=g).to(dev)
+        ks, vs = both[:, :, 0], both[:, :, 1]
     before = [t.clone() if t is not None else None for t in (kc, vc, ks, vs)]
     src = torch.tensor([3, 7, 11], dtype=torch.int32, device=dev)
     dst = torch.tensor([15, 0, 19], dtype=torch.int32, device=dev)
