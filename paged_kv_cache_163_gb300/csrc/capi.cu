@@ -382,7 +382,7 @@ pkv_status copy_blocks_unchecked(const CopyArgs &a) {
   return PKV_OK;
 }
 
-pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_new, void *out, pkv_dtype out_dtype,
+pkv_status attention_decode(int programmatic, const void *k_new, const void *v_new, void *out, pkv_dtype out_dtype,
                             const void *q, pkv_dtype q_dtype,
                             const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
                             const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -447,6 +447,7 @@ pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_
   p.d_error = d_error;
   p.stream = reinterpret_cast<cudaStream_t>(stream);
   p.programmatic = programmatic ? 1 : 0;
+  p.early_kv = programmatic == 2 ? 1 : 0;
   p.k_new = static_cast<const uint8_t *>(k_new);
   p.v_new = static_cast<const uint8_t *>(v_new);
   if (host_lens && num_seqs <= kInlineLens) {

@@ -44,6 +44,9 @@ struct DecodeParams {
   int32_t *d_error;
   cudaStream_t stream;
   int32_t programmatic;  // 1: launch as a programmatic dependent of the stream's previous kernel
+  // 1: that kernel writes no K/V cache or scale memory, so the first tiles'
+  // cache copies may start before the wait for it (queries and new rows after)
+  int32_t early_kv;
   // Optional fused append: row (b, kvh) of k_new / v_new ([num_seqs][num_kv_heads][head_dim] in the
   // query dtype) is written at position context_lens[b] - 1 before that tile is read.  NULL: none.
   const uint8_t *k_new;
@@ -200,7 +203,9 @@ PKV_PREFIX_DECL(e4m3i4_bf16)
 // passed in the launch parameters when the batch is small enough.  `plan`:
 // optional cascade (tensor-core path only): the prefix kernel runs first and
 // the decode folds its partials in.
-pkv_status attention_decode(bool programmatic, const void *k_new, const void *v_new, void *out, pkv_dtype out_dtype,
+// programmatic: 0 ordinary launch; 1 programmatic dependent of the stream's
+// previous kernel; 2 the same, and that kernel writes no K/V cache memory.
+pkv_status attention_decode(int programmatic, const void *k_new, const void *v_new, void *out, pkv_dtype out_dtype,
                             const void *q, pkv_dtype q_dtype,
                             const void *k_cache, const void *v_cache, pkv_dtype cache_dtype, const float *k_scale,
                             const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,

@@ -153,7 +153,10 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
     desc[(w & 1) * 32 + lane] = d;
   };
 
-  auto issue = [&](int m) {
+  // Copies of warp-local tile m into its stage.  part 0: all of them; 1: the
+  // cache copies only (with the stage's arrival for all its bytes; nothing
+  // for a tile without a block); 2: the rest (queries, new rows).
+  auto issue = [&](int m, int part) {
     const int2 d = desc[((m >> 5) & 1) * 32 + (m & 31)];
     if (lane == 0) {
       const int st = m % C::kStages;
@@ -165,11 +168,15 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       const uint32_t bytes =
           (d.x >= 0 ? C::kKV + 2 * C::kScale : 0) + (need_q ? C::kQ : 0) + (need_new ? C::kNew : 0);
       fence_proxy_async_smem();
-      if (bytes == 0) {
-        mbar_arrive(bars + st);
-      } else {
+      if (part == 0 || (part == 1) == (d.x >= 0)) {  // the part that arrives on the stage's barrier
+        if (bytes == 0) {
+          mbar_arrive(bars + st);
+          return;
+        }
         mbar_arrive_expect_tx(bars + st, bytes);
-        if (d.x >= 0) {
+      }
+      {
+        if (d.x >= 0 && part != 2) {
           const int64_t tile = d.x;
           const int row = static_cast<int>(tile * kBS);
           if constexpr (C::kCode8) {
@@ -193,10 +200,12 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
             tma_load_2d(tb + C::kTile + 2048, &tmv, 64, row, bars + st, pol);
           }
         }
-        if (need_q) bulk_g2s(ab + 2 * C::kScale, p.q + static_cast<size_t>(item) * C::kQ, C::kQ, bars + st);
-        if (need_new) {
-          bulk_g2s(ab + C::kOffNew, p.k_new + static_cast<size_t>(item) * D * 2, D * 2, bars + st);
-          bulk_g2s(ab + C::kOffNew + D * 2, p.v_new + static_cast<size_t>(item) * D * 2, D * 2, bars + st);
+        if (part != 1) {
+          if (need_q) bulk_g2s(ab + 2 * C::kScale, p.q + static_cast<size_t>(item) * C::kQ, C::kQ, bars + st);
+          if (need_new) {
+            bulk_g2s(ab + C::kOffNew, p.k_new + static_cast<size_t>(item) * D * 2, D * 2, bars + st);
+            bulk_g2s(ab + C::kOffNew + D * 2, p.v_new + static_cast<size_t>(item) * D * 2, D * 2, bars + st);
+          }
         }
       }
     }
@@ -205,6 +214,15 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
   if (count > 0) {
     fill_window(0);
     fill_window(1);
+  }
+  // Behind a kernel that writes no K/V cache memory the first tiles' cache
+  // copies may start now; their queries and new rows (inputs that kernel
+  // may write) follow the wait.
+  const bool early = p.early_kv && !p.pfx_n && count > 0;
+  if (early) {
+    __syncwarp();
+#pragma unroll 1
+    for (int i = 0; i < C::kStages && i < count; ++i) issue(i, 1);
   }
   // from here the previous kernel's writes are visible.  Behind a prefix
   // kernel (cascade) that kernel's predecessors are done already (it waited
@@ -218,7 +236,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
   }
   __syncwarp();
 #pragma unroll 1
-  for (int i = 0; i < C::kStages && i < count; ++i) issue(i);
+  for (int i = 0; i < C::kStages && i < count; ++i) issue(i, early ? 2 : 0);
 
   uint32_t qb[8][2];   // Q^T B fragments (8 k-steps)
   float oacc[8][4];    // O^T accumulators (8 m-tiles of 16 head_dim rows x 8 heads)
@@ -564,7 +582,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       }
     }
     __syncwarp();  // the stage is free again
-    if (n + C::kStages < count) issue(n + C::kStages);
+    if (n + C::kStages < count) issue(n + C::kStages, 0);
   }
   griddep_launch_dependents();
   flush(cur_item, whole_start && saw_last);

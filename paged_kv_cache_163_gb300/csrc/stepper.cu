@@ -427,8 +427,13 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
       // copy kernel finished before layer 0 got past its wait.
       const int32_t *t_lens = l == 0 ? Hd + 3 * n : d_lens;
       const int32_t *t_tables = l == 0 ? Hd + 4 * n : d_tables;
+      // The kernel before a layer's decode writes no K/V cache memory when it
+      // is the previous layer's decode (other layers' rows) or this step's
+      // metadata copy (launched after the copy-on-write copies), so the decode
+      // may start its first cache copies before waiting for it.
+      const int programmatic = (l > 0 || P.num_layers > 1) ? 2 : 1;
       pkv_status r = pkv::attention_decode(
-          true, layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l),
+          programmatic, layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l),
           layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l), P.q_dtype,
           layer_ptr(P.k_cache, P.cache_layer_stride, l), layer_ptr(P.v_cache, v_stride, l), P.cache_dtype,
           scale_ptr(P.k_scale, l), scale_ptr(P.v_scale, l), t_tables, mb, t_lens, max_len, n, P.num_q_heads,
