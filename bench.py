@@ -46,21 +46,22 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu capture), keyed by workload and by the hash of the decode kernel source it
 # was taken on; reported only while the source is unchanged.
 NCU_TRAFFIC = {
-    # decode kernel source 9f085607ad4b46ef: tensor-core kernel with the step's append fused in, 16-warp
+    # decode kernel source 0496016a5ccc7739: tensor-core kernel with the step's append fused in, 16-warp
     # CTAs for one-byte caches, 4-bit V for the mixed cache, K and V scales of a tile in one 128-byte
-    # unit, 16-byte output stores, cascade for shared prefixes; default "auto" variant.
+    # unit, first cache copies before the programmatic wait behind kernels that write no cache,
+    # 16-byte output stores, cascade for shared prefixes; default "auto" variant.
     # dram__bytes_read.sum + dram__bytes_write.sum of one call (the fifth decode call of a --steps 4
     # --warmup 3 run; prefix-share: its prefix kernel plus its decode, whose DRAM reads include the
     # prefix partials ncu's replay flushed from L2)
-    ("llama3-8b", "9f085607ad4b46ef"): 145_800_448,              # 142.78 MB read + 3.02 MB written
-    ("llama3-8b:bs32", "9f085607ad4b46ef"): 145_834_496,
-    ("mha7b-40layer", "9f085607ad4b46ef"): 271_578_112,
-    ("prefix-share", "9f085607ad4b46ef"): 52_877_568,
-    ("long-fp8", "9f085607ad4b46ef"): 796_797_184,               # 793.59 MB read + 3.21 MB written
-    ("long-fp8:fp8_e5m2", "9f085607ad4b46ef"): 796_726_784,
-    ("long-fp8:int8", "9f085607ad4b46ef"): 796_787_200,
-    ("long-fp8:fp8_e4m3_int4", "9f085607ad4b46ef"): 604_500_736,
-    ("long-fp8:bs32", "9f085607ad4b46ef"): 797_180_160,
+    ("llama3-8b", "0496016a5ccc7739"): 145_694_464,
+    ("llama3-8b:bs32", "0496016a5ccc7739"): 145_843_456,
+    ("mha7b-40layer", "0496016a5ccc7739"): 271_298_304,
+    ("prefix-share", "0496016a5ccc7739"): 52_879_616,
+    ("long-fp8", "0496016a5ccc7739"): 796_831_744,
+    ("long-fp8:fp8_e5m2", "0496016a5ccc7739"): 796_802_304,
+    ("long-fp8:int8", "0496016a5ccc7739"): 796_821_504,
+    ("long-fp8:fp8_e4m3_int4", "0496016a5ccc7739"): 604_133_632,
+    ("long-fp8:bs32", "0496016a5ccc7739"): 797_052_160,
 }
 
 
