@@ -135,11 +135,12 @@ pkv_status pkv_seq_fork(pkv_bm *bm, int64_t parent, int64_t child);
 pkv_status pkv_seq_free(pkv_bm *bm, int64_t seq_id);
 
 /* Append one token to each seq_ids[i], in order (a sequence may repeat).
- * For a sequence of length n: if n % 16 == 0 a block is taken from the free
- * list and added to its table; else if its last block is shared, a new block
- * is taken, the pair (old -> new) is recorded in cow_src/cow_dst and the old
- * block loses one reference (copy-on-write; the last holder writes in place).
- * slot_mapping[i] = table[n / 16] * 16 + n % 16, then n becomes n + 1.
+ * With bs the manager's block size (16 or 32) and n the sequence's length:
+ * if n % bs == 0 a block is taken from the free list and added to its table;
+ * else if its last block is shared, a new block is taken, the pair
+ * (old -> new) is recorded in cow_src/cow_dst and the old block loses one
+ * reference (copy-on-write; the last holder writes in place).
+ * slot_mapping[i] = table[n / bs] * bs + n % bs, then n becomes n + 1.
  * Arrays: seq_ids[n], slot_mapping[n], cow_src[n], cow_dst[n] (host memory);
  * *num_cow receives the number of pairs.  All-or-nothing: returns
  * PKV_ERR_NO_BLOCKS, with nothing changed, when the free list cannot cover
@@ -356,10 +357,12 @@ pkv_status paged_attention_decode_append(void *out, pkv_dtype out_dtype, const v
  * PKV_ERR_WORKSPACE with the size in pkv_last_error().  The call allocates
  * nothing.  Its first call on a device looks up the buffer's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture; it also zero-fills the buffer once.  All calls
- * on a device share the buffer and it keeps the last call's contents, which
- * the next call can start from; calls whose kernels overlap on the GPU race,
- * so serialise them. */
+ * before any stream capture.  The split counters in the buffer are cleared
+ * on the caller's stream by the same per-workspace rule as
+ * paged_attention_decode (first call on the buffer, or a change of
+ * num_seqs / num_kv_heads); nothing else in it needs an initial value.  All
+ * calls on a device share the buffer and it keeps the last call's contents;
+ * calls whose kernels overlap on the GPU race, so serialise them. */
 #define PKV_STATIC_SCRATCH_BYTES (16u << 20)
 pkv_status paged_attention_decode_static(void *out, pkv_dtype out_dtype, const void *q,
                                          pkv_dtype q_dtype, const void *k_cache, const void *v_cache,

@@ -16,11 +16,16 @@
 // any stream capture.
 //
 // Every call on a device shares the one buffer, and the buffer keeps the last
-// call's contents.  The decode's per-item counters must start at zero or at
-// a value an earlier call left, so the set-up also zero-fills the buffer
-// once (cudaMemset, no allocation).  Calls whose kernels overlap on the GPU
-// (for example on two concurrent streams) race on the buffer, so serialise
-// them.
+// call's contents.  Only the decode's split counters must start at zero;
+// the partials are written before they are read.  paged_attention_decode
+// keeps its counters per workspace address: the first call on an address,
+// and any call whose (num_seqs, num_kv_heads) differ from the last call on
+// it, clears the counter banks with cudaMemsetAsync on the caller's stream
+// (prepare_counters in capi.cu), and every kernel clears the bank the next
+// call uses.  So this file clears nothing itself, and the clear is ordered
+// on the same stream as the decode it serves.  Calls whose kernels overlap
+// on the GPU (for example on two concurrent streams) race on the buffer, so
+// serialise them.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -57,11 +62,6 @@ pkv_status scratch_for_current_device(void **out) {
     if (e != cudaSuccess || p == nullptr) {
       std::string msg = std::string("paged_attention_decode_static: cudaGetSymbolAddress: ") +
                         cudaGetErrorString(e);
-      return fail(PKV_ERR_CUDA, msg.c_str());
-    }
-    e = cudaMemset(p, 0, kStaticScratchBytes);
-    if (e != cudaSuccess) {
-      std::string msg = std::string("paged_attention_decode_static: cudaMemset: ") + cudaGetErrorString(e);
       return fail(PKV_ERR_CUDA, msg.c_str());
     }
     g_scratch_ptr[dev] = p;

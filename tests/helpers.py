@@ -82,7 +82,7 @@ def oracle_bits(values, dtype):
 
 
 def check_rounding(cache, w, out32, layers=None):
-    """The query-dtype output equals the fp32 output rounded once to nearest even."""
+    """The query-dtype output equals the fp32 output rounded once to nearest even; returns it."""
     import torch
     from paged_kv_cache_163_gb300.play import to_device
     q = to_device(np.stack([w.q_rows(li) for li in range(w.num_layers)]), w.q_dtype, out32.device)
@@ -90,3 +90,68 @@ def check_rounding(cache, w, out32, layers=None):
     sel = out32 if layers is None else out32[list(layers)]
     got = out16 if layers is None else out16[list(layers)]
     assert torch.equal(got, sel.to(got.dtype)), "16-bit output is not the fp32 result rounded once"
+    return out16
+
+
+def coded_seq_reference(args):
+    """Oracle results of one sequence of a coded-cache workload, for a process pool.
+
+    args = (workload id, cache dtype, sequence).  Returns (sequence, K codes
+    [L, Hkv, row], K scales [L, Hkv], V codes, V scales, fp64 attention
+    output [Hq, D] of the step's query over the dequantised codes).
+    """
+    from oracle.cache import code_values, part_types, quantize_rows
+    from paged_kv_cache_163_gb300 import workloads as wl
+    wid, cache_dtype, seq = args
+    w = wl.make(wid, cache_dtype=cache_dtype)
+    L = int(w.context_lens[seq])
+    kt, vt = part_types(w.cache_dtype)
+    kc, ks = quantize_rows(w.kv_rows(0, seq, 0, L), kt)
+    vc, vs = quantize_rows(w.kv_rows(1, seq, 0, L), vt)
+    K = code_values(kc, kt) * ks.astype(np.float64)[..., None]
+    V = code_values(vc, vt) * vs.astype(np.float64)[..., None]
+    ref = decode_attention(w.q_rows(0)[seq], K, V, w.scale)
+    return seq, kc, ks, vc, vs, ref
+
+
+def parallel_map(fn, items, max_workers=16):
+    """fn over items in spawned processes (BLAS threads 1 each); results in item order."""
+    import multiprocessing as mp
+    import os
+    from concurrent.futures import ProcessPoolExecutor
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    n = max(1, min(max_workers, cores, len(items)))
+    keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in keys}
+    for k in keys:
+        os.environ[k] = "1"
+    try:
+        with ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn")) as ex:
+            return list(ex.map(fn, items))
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def compare_cache_bytes(cache, model, cache_dtype, layer=0):
+    """Every slot the oracle's PagedCacheModel marks filled holds the same bytes (and scales) on the GPU."""
+    filled = model.filled
+    scaled = model.k_scale is not None or model.v_scale is not None
+    for got, want, part in ((cache.k[layer], model.k, model.k_type), (cache.v[layer], model.v, model.v_type)):
+        g = cache_bits(got).transpose(0, 2, 1, 3)[filled]
+        w = want.transpose(0, 2, 1, 3)[filled]
+        if part in ("f16", "bf16"):
+            w = oracle_bits(w, part)
+        assert np.array_equal(g, w), f"{part} cache bytes differ"
+    if scaled:
+        for got, want in ((cache.k_scale[layer], model.k_scale), (cache.v_scale[layer], model.v_scale)):
+            if want is None:
+                continue
+            g = got.cpu().numpy().transpose(0, 2, 1)[filled]
+            assert np.array_equal(g, want.transpose(0, 2, 1)[filled]), f"{cache_dtype} scales differ"

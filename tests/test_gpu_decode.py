@@ -5,20 +5,20 @@ block manager -> append -> decode).  Integer results (block tables, slot
 mappings, copy-on-write pairs, cache bytes) must be bit-exact; attention
 outputs must satisfy max |err| <= 1e-2 and relative L2 <= 2e-3.
 
-Small workloads compare every output and every cache byte; the full-size
-ones compare every output for the oracle-sized ones (workloads 2-4) and
-sampled sequences plus sampled cache blocks for the 16 x 16K-32K FP8 one.
+Every workload compares every output and every filled cache slot: the
+16 x 16K-32K FP8 one too, with the oracle's quantisation and attention of
+its sequences computed once, in a pool of spawned processes.  Workloads
+without outliers also compare the 16-bit output with the oracle directly.
 """
 import numpy as np
 import pytest
 
 from oracle.allocator import AllocatorModel
-from oracle.cache import quantize_rows
 from paged_kv_cache_163_gb300.capi import SCALED_CACHES
 from paged_kv_cache_163_gb300 import workloads as wl
 
-from helpers import (assert_close, cache_bits, check_rounding, oracle_bits, oracle_play, oracle_seq_output,
-                     to_f64)
+from helpers import (assert_close, cache_bits, check_rounding, coded_seq_reference, oracle_bits, oracle_play,
+                     oracle_seq_output, parallel_map, to_f64)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -71,11 +71,16 @@ def full_oracle_check(play, w, layers=1):
     check_tables(cache, o, w.seq_ids)
     assert cache.cow_pairs == o.cow_log
     check_cache_bytes(cache, o, w)
-    res = []
+    res, refs = [], []
     for li in range(layers):
         ref = o.decode(w.seq_ids, w.q_rows(li), w.scale)
+        refs.append(ref)
         res.append(assert_close(to_f64(out[li]), ref, f"{w.name} layer {li}"))
-    check_rounding(cache, w, out)
+    out16 = check_rounding(cache, w, out)
+    if w.outlier_p == 0:
+        # no x20 outliers: the rounded 16-bit output itself stays inside the tolerance
+        for li in range(layers):
+            assert_close(to_f64(out16[li]), refs[li], f"{w.name} layer {li}, {w.q_dtype} output")
     assert cache.check() == 0
     cache.close()
     return res
@@ -109,21 +114,39 @@ def test_mha_40_layers_fp16(play, kernel_kind):
     K = [wl.round_to(w.kv_rows(0, s, 0, 2048), "f16").astype(np.float64) for s in range(8)]
     V = [wl.round_to(w.kv_rows(1, s, 0, 2048), "f16").astype(np.float64) for s in range(8)]
     from oracle.attention import decode_attention
+    refs = {}
     for li in range(0, 40, 3):
         q = w.q_rows(li)
-        ref = np.stack([decode_attention(q[s], K[s], V[s], w.scale) for s in range(8)])
-        assert_close(to_f64(out[li]), ref, f"layer {li}")
+        refs[li] = np.stack([decode_attention(q[s], K[s], V[s], w.scale) for s in range(8)])
+        assert_close(to_f64(out[li]), refs[li], f"layer {li}")
     # cache bytes of sampled layers equal the input rows
     for li in (0, 39):
         got = cache_bits(cache.k[li])[t[3]]                     # [128, 32, 16, 128] of sequence 3
         want = oracle_bits(K[3].reshape(128, 16, 32, 128).transpose(0, 2, 1, 3), "f16")
         assert np.array_equal(got, want)
-    check_rounding(cache, w, out, layers=[0, 17, 39])
+    out16 = check_rounding(cache, w, out, layers=[0, 18, 39])
+    for li in (0, 18, 39):
+        assert_close(to_f64(out16[li]), refs[li], f"layer {li}, fp16 output")
     cache.close()
 
 
+@pytest.fixture(scope="module")
+def long_fp8_reference():
+    """Oracle codes, scales and fp64 outputs of every sequence of the 16 x 16K-32K FP8 workload."""
+    w = wl.make(5)
+    return {r[0]: r[1:] for r in parallel_map(coded_seq_reference, [(5, None, s) for s in range(w.num_seqs)])}
+
+
+def gathered(t, table_row, n_blocks, length):
+    """A sequence's rows of a paged pool [blocks, Hkv, bs, ...] -> [length, Hkv, ...] (host)."""
+    idx = torch.as_tensor(np.asarray(table_row[:n_blocks], dtype=np.int64), device=t.device)
+    g = t.index_select(0, idx).cpu().numpy()                  # [nb, Hkv, bs, ...]
+    g = np.swapaxes(g, 1, 2)                                  # [nb, bs, Hkv, ...]
+    return g.reshape((-1,) + g.shape[2:])[:length]
+
+
 @pytest.mark.parametrize("kernel_kind", ["simt", "mma"], indirect=True)
-def test_long_context_fp8_sampled(play, kernel_kind):
+def test_long_context_fp8_every_sequence(play, kernel_kind, long_fp8_reference):
     w = wl.make(5)
     cache, out = play.run(w, poison=False, out_dtype="f32")
     assert cache.check() == 0
@@ -137,21 +160,17 @@ def test_long_context_fp8_sampled(play, kernel_kind):
     t, lens = cache.tables(w.seq_ids)
     mt, ml = model.block_tables(w.seq_ids, t.shape[1])
     assert t.tolist() == mt and lens.tolist() == ml
-    q = w.q_rows(0)
     got = to_f64(out[0])
-    rng = np.random.default_rng(0)
-    for s in sorted(set([int(np.argmax(w.context_lens)), int(np.argmin(w.context_lens))]
-                        + rng.choice(w.num_seqs, 2, replace=False).tolist())):
-        ref = oracle_seq_output(w, s, q[s])
+    for s in range(w.num_seqs):
+        kc, ks, vc, vs, ref = long_fp8_reference[s]
         assert_close(got[s], ref, f"sequence {s}")
-        # sampled blocks: codes and scales equal the oracle's quantisation of the rows
-        for lb in (0, int(lens[s] - 1) // 16):
-            rows_k = w.kv_rows(0, s, lb * 16, min(lb * 16 + 16, int(lens[s])))
-            codes, scales = quantize_rows(rows_k)
-            n = len(rows_k)
-            gk = cache_bits(cache.k[0][int(t[s, lb])])[:, :n].transpose(1, 0, 2)
-            gs = cache.k_scale[0][int(t[s, lb])][:, :n].cpu().numpy().T
-            assert np.array_equal(gk, codes) and np.array_equal(gs, scales)
+        # every filled slot: codes and scales equal the oracle's quantisation of the rows
+        L = int(lens[s])
+        nb = -(-L // 16)
+        assert np.array_equal(gathered(cache.k[0], t[s], nb, L), kc), f"K codes of sequence {s}"
+        assert np.array_equal(gathered(cache.v[0], t[s], nb, L), vc), f"V codes of sequence {s}"
+        assert np.array_equal(gathered(cache.k_scale[0], t[s], nb, L), ks), f"K scales of sequence {s}"
+        assert np.array_equal(gathered(cache.v_scale[0], t[s], nb, L), vs), f"V scales of sequence {s}"
     check_rounding(cache, w, out)
     cache.close()
 
