@@ -73,7 +73,7 @@ NCU_TRAFFIC = {
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cuh", "decode_mma.cuh", "decode_prefix.cuh", "common.cuh", "dtypes.h"):
+    for f in ("decode.cuh", "decode_mma.cuh", "decode_prefix.cuh", "decode_prefix_umma.cuh", "common.cuh", "dtypes.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_163_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -97,6 +97,10 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--kernel", choices=["auto", "simt", "mma"], default="auto",
                     help="decode kernel variant (auto: tensor-core tiles for head_dim 128)")
+    ap.add_argument("--prefix-kernel", choices=["auto", "mma_sync", "tcgen05"], default="auto",
+                    help="cascade prefix kernel (auto: mma.sync; tcgen05 for 16-bit caches when asked)")
+    ap.add_argument("--prefix-chunk-tiles", type=int, default=0,
+                    help="16-token tiles per tcgen05 prefix CTA (0: the library default)")
     return ap.parse_args(argv)
 
 
@@ -289,6 +293,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     capi.load()
     capi.pkv_set_decode_kernel(args.kernel)
+    capi.pkv_set_prefix_kernel(args.prefix_kernel, args.prefix_chunk_tiles)
     wid = WORKLOADS[args.workload]
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
     attn_steps = max(3, min(args.steps, 30))
@@ -420,6 +425,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded N(0,1); no dataset or weights)",
         "config": workload_config(w, args.workload, {"parallelism": f"replicas x{world} (sequences sharded)",
                                                      "decode_kernel": args.kernel,
+                                                     "prefix_kernel": args.prefix_kernel,
                                                      "step_launch": "cuda graph replay" if args.graph else "eager"}),
         "hbm_frac_step": round(value / world / peak, 4),
         "seq_tokens_per_s_per_layer": round(world * tok_total / (t_total / w.num_layers), 1),

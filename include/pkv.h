@@ -282,6 +282,21 @@ typedef enum { PKV_DECODE_AUTO = 0, PKV_DECODE_SIMT = 1, PKV_DECODE_MMA = 2 } pk
 pkv_status pkv_set_decode_kernel(pkv_decode_kernel kind);
 pkv_decode_kernel pkv_get_decode_kernel(void);
 
+/* Which kernel attends the shared prefixes of the step executor's cascade
+ * ("KV Cache 与 vLLM" §3.3, "KV Cache优化实战" §5.2; see pkv_stepper_use_cascade).
+ * MMA_SYNC: warp-level mma.sync m16n8k16 over 16-token tiles, any cache
+ * type.  TCGEN05: fifth-generation tensor-core MMAs (tcgen05, accumulators
+ * in tensor memory) over 64-token sub-chunks, for f16 / bf16 caches with a
+ * query of the same type (other caches keep MMA_SYNC).  AUTO (default):
+ * MMA_SYNC, the faster of the two on the measured workloads.
+ * chunk_tiles: 16-token tiles a tcgen05 CTA attends (the prefix is cut into
+ * ceil(tiles / chunk_tiles) chunks, at most 16); 0 keeps the default (16).
+ * Process-wide; affects steps issued after it.  PKV_ERR_INVALID for an
+ * unknown kind or a chunk_tiles outside [0, 4096]. */
+typedef enum { PKV_PREFIX_AUTO = 0, PKV_PREFIX_MMA_SYNC = 1, PKV_PREFIX_TCGEN05 = 2 } pkv_prefix_kernel;
+pkv_status pkv_set_prefix_kernel(pkv_prefix_kernel kind, int32_t chunk_tiles);
+pkv_prefix_kernel pkv_get_prefix_kernel(void);
+
 /* Device workspace (bytes) paged_attention_decode needs for these shapes on
  * the current device (split-KV partials and per-(sequence, KV head)
  * counters).  Depends on the device's SM count.  Fill a new workspace with

@@ -132,6 +132,8 @@ _PROTOS = {
     "pkv_launch_count": (C.c_int64, []),
     "pkv_copy_segments": (C.c_int, [C.c_void_p, C.c_int32, _vp]),
     "pkv_set_decode_kernel": (C.c_int, [C.c_int]),
+    "pkv_set_prefix_kernel": (C.c_int, [C.c_int, C.c_int32]),
+    "pkv_get_prefix_kernel": (C.c_int, []),
     "pkv_get_decode_kernel": (C.c_int, []),
     "pkv_status_string": (C.c_char_p, [C.c_int]),
     "pkv_last_error": (C.c_char_p, []),
@@ -583,6 +585,19 @@ def pkv_set_decode_kernel(kind) -> None:
 def pkv_get_decode_kernel() -> str:
     v = int(load().pkv_get_decode_kernel())
     return {k: n for n, k in DECODE_KERNELS.items()}[v]
+
+
+PREFIX_KERNELS = {"auto": 0, "mma_sync": 1, "tcgen05": 2}
+
+
+def pkv_set_prefix_kernel(kind, chunk_tiles: int = 0) -> None:
+    """Select the cascade's prefix kernel process-wide: 'auto', 'mma_sync' or 'tcgen05'."""
+    _check(load().pkv_set_prefix_kernel(PREFIX_KERNELS.get(kind, kind), int(chunk_tiles)), "pkv_set_prefix_kernel")
+
+
+def pkv_get_prefix_kernel() -> str:
+    v = int(load().pkv_get_prefix_kernel())
+    return {k: n for n, k in PREFIX_KERNELS.items()}[v]
 
 
 def pkv_launch_count() -> int:

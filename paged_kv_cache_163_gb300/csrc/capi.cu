@@ -43,6 +43,8 @@ int sm_count() {
 }
 
 std::atomic<int> g_decode_kind{PKV_DECODE_AUTO};
+std::atomic<int> g_prefix_kind{PKV_PREFIX_AUTO};
+std::atomic<int> g_prefix_chunk_tiles{16};
 
 // Per-workspace state of the split counters.  A decode call with epoch e
 // counts in bank e & 1 and clears the other bank for the next call, so the
@@ -113,6 +115,17 @@ PrefixFn pick_prefix(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
   if (cache_dtype == PKV_FP8_E4M3_INT4 && q_dtype == PKV_F16) return prefix_call_e4m3i4_f16;
   return prefix_call_e4m3i4_bf16;  // dtypes validated before
 }
+
+}  // namespace
+
+bool prefix_uses_umma(pkv_dtype q_dtype, pkv_dtype cache_dtype) {
+  return g_prefix_kind.load() == PKV_PREFIX_TCGEN05 && q_dtype == cache_dtype &&
+         (cache_dtype == PKV_F16 || cache_dtype == PKV_BF16);
+}
+
+int32_t prefix_umma_chunk_tiles() { return g_prefix_chunk_tiles.load(); }
+
+namespace {
 
 bool use_mma(int32_t head_dim) {
   const int k = g_decode_kind.load();
@@ -254,6 +267,18 @@ pkv_status pkv_set_decode_kernel(pkv_decode_kernel kind) {
 }
 
 pkv_decode_kernel pkv_get_decode_kernel(void) { return static_cast<pkv_decode_kernel>(g_decode_kind.load()); }
+
+pkv_status pkv_set_prefix_kernel(pkv_prefix_kernel kind, int32_t chunk_tiles) {
+  if (kind != PKV_PREFIX_AUTO && kind != PKV_PREFIX_MMA_SYNC && kind != PKV_PREFIX_TCGEN05)
+    return fail(PKV_ERR_INVALID, "pkv_set_prefix_kernel: unknown kind");
+  if (chunk_tiles < 0 || chunk_tiles > 4096)
+    return fail(PKV_ERR_INVALID, "pkv_set_prefix_kernel: chunk_tiles outside [0, 4096]");
+  g_prefix_kind.store(kind);
+  g_prefix_chunk_tiles.store(chunk_tiles == 0 ? 16 : chunk_tiles);
+  return PKV_OK;
+}
+
+pkv_prefix_kernel pkv_get_prefix_kernel(void) { return static_cast<pkv_prefix_kernel>(g_prefix_kind.load()); }
 
 pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                                 const int32_t *src, const int32_t *dst, int32_t num_pairs,
@@ -498,7 +523,12 @@ pkv_status attention_decode(int programmatic, const void *k_new, const void *v_n
       std::memcpy(p.pfx_base, plan->pp.base, sizeof(int32_t) * static_cast<size_t>(num_seqs));
       p.pfx_ml = pp.ml;
       p.pfx_o = pp.o;
-      e = pick_prefix(q_dtype, cache_dtype)(num_q_heads / num_kv_heads, &p, &pp, &tmk, &tmv, plan->units);
+      if (plan->umma) {
+        e = (cache_dtype == PKV_BF16 ? prefix_umma_call_bf16 : prefix_umma_call_f16)(num_q_heads / num_kv_heads, &p,
+                                                                                    &pp, &tmk, &tmv, plan->units);
+      } else {
+        e = pick_prefix(q_dtype, cache_dtype)(num_q_heads / num_kv_heads, &p, &pp, &tmk, &tmv, plan->units);
+      }
       if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode: prefix kernel");
       ++t_launches;
     }

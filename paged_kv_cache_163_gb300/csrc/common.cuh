@@ -77,6 +77,16 @@ __device__ __forceinline__ void code4_to_f16x2(uint32_t w, uint32_t &lo, uint32_
   }
 }
 
+// Biased form of code4_to_f16x2 for INT8, for MMA operands whose bias the
+// caller removes itself: the binary16 words 0x6400 | (x ^ 0x80), whose values
+// are 1152 + x exactly (no subtraction).
+__device__ __forceinline__ void int8x4_to_f16x2_biased(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+}
+constexpr float kInt8Bias = 1152.f;
+
 // Four codes (byte 0 first) to four floats.
 template <int DT>
 __device__ __forceinline__ void unpack_code4(uint32_t w, float *out) {
@@ -107,6 +117,16 @@ __device__ __forceinline__ void int4_pair_to_f16x2(uint32_t w, uint32_t &lo, uin
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64086408u));
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(b), "r"(0x2C002C00u), "r"(0xD480D480u));
 }
+
+// Biased form of int4_pair_to_f16x2, for MMA operands whose bias the caller
+// removes itself: low nibbles n become 0x6400 | n = 1024 + n = 1032 + code,
+// high nibbles 0x6400 | 16 n = 1024 + 16 n = 1152 + 16 code (exact).
+__device__ __forceinline__ void int4_pair_to_f16x2_biased(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(lo) : "r"(w));  // (w & m) | c
+  asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(hi) : "r"(w));
+}
+constexpr float kInt4LoBias = 1032.f;
+constexpr float kInt4HiBias = 1152.f;  // on values scaled by 16
 
 // n bytes (n = 1 or 2) of a 4-bit row -> 2 n floats, element order.
 template <int NBYTES>

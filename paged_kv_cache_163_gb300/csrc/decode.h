@@ -103,6 +103,7 @@ constexpr int kMinPrefixTiles = 16;
 struct CascadePlan {
   PrefixParams pp;
   int32_t units;  // prefix kernel CTAs
+  int32_t umma;   // 1: the tcgen05 prefix kernel runs (its chunking), 0: the mma.sync one
   int32_t start[kInlineLens];
   int32_t chunks[kInlineLens];
 };
@@ -192,6 +193,19 @@ PKV_PREFIX_DECL(int8_bf16)
 PKV_PREFIX_DECL(e4m3i4_f16)
 PKV_PREFIX_DECL(e4m3i4_bf16)
 #undef PKV_PREFIX_DECL
+
+// Prefix kernel on tcgen05 tensor cores (decode_prefix_umma.cuh): 16-bit caches
+// with a query of the same type, head_dim 128.
+cudaError_t prefix_umma_call_f16(int group, const DecodeParams *p, const PrefixParams *pp, const CUtensorMap *tmk,
+                                 const CUtensorMap *tmv, int grid);
+cudaError_t prefix_umma_call_bf16(int group, const DecodeParams *p, const PrefixParams *pp, const CUtensorMap *tmk,
+                                  const CUtensorMap *tmv, int grid);
+
+// The process-wide prefix-kernel choice (pkv_set_prefix_kernel): whether a
+// cascade over a cache of this type runs the tcgen05 kernel, and the tiles
+// one of its CTAs attends.
+bool prefix_uses_umma(pkv_dtype q_dtype, pkv_dtype cache_dtype);
+int32_t prefix_umma_chunk_tiles();
 
 // paged_attention_decode (k_new == v_new == NULL) or
 // paged_attention_decode_append, with a choice of launch: programmatic ==

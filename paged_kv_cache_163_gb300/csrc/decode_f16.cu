@@ -2,6 +2,7 @@
 #include "decode.cuh"
 #include "decode_mma.cuh"
 #include "decode_prefix.cuh"
+#include "decode_prefix_umma.cuh"
 
 namespace pkv {
 
@@ -18,6 +19,11 @@ cudaError_t decode_mma_call_f16(int group, int op, const DecodeParams *p, const 
 cudaError_t prefix_call_f16(int group, const DecodeParams *p, const PrefixParams *pp, const CUtensorMap *tmk,
                             const CUtensorMap *tmv, int grid) {
   return prefix_family<PKV_F16, PKV_F16>(group, p, pp, tmk, tmv, grid);
+}
+
+cudaError_t prefix_umma_call_f16(int group, const DecodeParams *p, const PrefixParams *pp, const CUtensorMap *tmk,
+                                 const CUtensorMap *tmv, int grid) {
+  return prefix_umma_family<PKV_F16, PKV_F16>(group, p, pp, tmk, tmv, grid);
 }
 
 }  // namespace pkv

@@ -71,6 +71,16 @@ struct MmaCfg {
   static constexpr int KT = k_part(CDT), VT = v_part(CDT);  // storage types of K and of V
   static constexpr bool kCode8 = is_code8(KT);  // one-byte K codes (FP8 E4M3 / E5M2, INT8) with scales
   static constexpr bool kVInt4 = VT == kInt4;   // 4-bit V codes: plain 64-byte rows, no swizzle
+  // INT8 K codes enter the score MMA biased (1152 + k); the bias comes off
+  // the score as 1152 x the query head's sum, once per item.
+  static constexpr bool kKBias = KT == PKV_INT8;
+  // INT8 / 4-bit V codes enter the output MMA biased; the bias comes off the
+  // accumulator in the per-tile rescale (an FFMA instead of an FMUL), with the
+  // tile's column sums of P from one more MMA against all-ones A.
+  static constexpr bool kVBias = VT == PKV_INT8 || VT == kInt4;
+  static constexpr float kBiasLo = VT == kInt4 ? kInt4LoBias : kInt8Bias;  // accumulator rows g
+  static constexpr float kBiasHi = VT == kInt4 ? kInt4HiBias : kInt8Bias;  // rows g + 8
+  static constexpr float kHiScale = VT == kInt4 ? 0.0625f : 1.f;          // 4-bit high nibbles carry x16
   // One-byte tiles are half the bytes, so an SM holds twice the warps (with
   // at most 128 registers a thread).  They form one 16-warp CTA: two 8-warp
   // CTAs on an SM were measured to run unevenly (the CTA launched first
@@ -245,6 +255,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
   // of the latest tile (P carries the tile's scales relative to it, so the
   // fp16 B operand stays in [0, 1] whatever the scales' magnitude).
   float vunit = 1.f;
+  float kbias0 = 0.f, kbias1 = 0.f;  // INT8 K: 1152 x sum of the f16 query of heads 2 q4, 2 q4 + 1
   int cur_item = -1;
   bool whole_start = false, saw_last = false;
 
@@ -278,7 +289,7 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             r[2 * c] = oacc[ib + c][j] * inv;
-            r[2 * c + 1] = oacc[ib + c][2 + j] * inv;
+            r[2 * c + 1] = oacc[ib + c][2 + j] * (inv * C::kHiScale);
           }
           if (p.out_f32) {
             float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + row + d0);
@@ -296,10 +307,11 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
 #pragma unroll
         for (int ib = 0; ib < 8; ib += 4) {
           float4 *dst = reinterpret_cast<float4 *>(op + out_d<C::kCode8>(g, ib, 0));
-          dst[0] = make_float4(oacc[ib][j] * vunit, oacc[ib][2 + j] * vunit, oacc[ib + 1][j] * vunit,
-                               oacc[ib + 1][2 + j] * vunit);
-          dst[1] = make_float4(oacc[ib + 2][j] * vunit, oacc[ib + 2][2 + j] * vunit, oacc[ib + 3][j] * vunit,
-                               oacc[ib + 3][2 + j] * vunit);
+          const float vh = vunit * C::kHiScale;
+          dst[0] = make_float4(oacc[ib][j] * vunit, oacc[ib][2 + j] * vh, oacc[ib + 1][j] * vunit,
+                               oacc[ib + 1][2 + j] * vh);
+          dst[1] = make_float4(oacc[ib + 2][j] * vunit, oacc[ib + 2][2 + j] * vh, oacc[ib + 3][j] * vunit,
+                               oacc[ib + 3][2 + j] * vh);
         }
         if (g == 0) {
           p.ws_ml[(slot * G + n) * 2] = m_run[j];
@@ -366,6 +378,19 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
           qb[s][1] = raw.y;
         }
       }
+      if constexpr (C::kKBias) {
+        // head g's query sum: this lane's 32 head_dim values, then the other three lanes of the group
+        float qs = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const float2 a = unpack2<PKV_F16>(qb[s][0]), b = unpack2<PKV_F16>(qb[s][1]);
+          qs += (a.x + a.y) + (b.x + b.y);
+        }
+        qs += __shfl_xor_sync(kFull, qs, 1);
+        qs += __shfl_xor_sync(kFull, qs, 2);
+        kbias0 = kInt8Bias * __shfl_sync(kFull, qs, 8 * q4);      // head 2 q4 (lane group 2 q4)
+        kbias1 = kInt8Bias * __shfl_sync(kFull, qs, 8 * q4 + 4);  // head 2 q4 + 1
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -423,8 +448,13 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           uint32_t a[4];
-          code4_to_f16x2<C::KT>(word(kr[0][s >> 2], s & 3), a[0], a[2]);
-          code4_to_f16x2<C::KT>(word(kr[1][s >> 2], s & 3), a[1], a[3]);
+          if constexpr (C::kKBias) {
+            int8x4_to_f16x2_biased(word(kr[0][s >> 2], s & 3), a[0], a[2]);
+            int8x4_to_f16x2_biased(word(kr[1][s >> 2], s & 3), a[1], a[3]);
+          } else {
+            code4_to_f16x2<C::KT>(word(kr[0][s >> 2], s & 3), a[0], a[2]);
+            code4_to_f16x2<C::KT>(word(kr[1][s >> 2], s & 3), a[1], a[3]);
+          }
           mma_16816(sacc4[s & 3], a, qb[s][0], qb[s][1], false);
         }
       } else {
@@ -449,6 +479,12 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       float sacc[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) sacc[c] = (sacc4[0][c] + sacc4[1][c]) + (sacc4[2][c] + sacc4[3][c]);
+      if constexpr (C::kKBias) {
+        sacc[0] -= kbias0;
+        sacc[1] -= kbias1;
+        sacc[2] -= kbias0;
+        sacc[3] -= kbias1;
+      }
       // ---- scale, mask, online softmax (base 2) ----
       float sc0 = p.scale_log2, sc1 = p.scale_log2;
       if constexpr (C::kCode8) {
@@ -493,13 +529,6 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
         al1 *= ru;
         vunit = vmax;
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        oacc[i][0] *= al0;
-        oacc[i][1] *= al1;
-        oacc[i][2] *= al0;
-        oacc[i][3] *= al1;
-      }
       // ---- P^T B fragments (k rows = tokens, n columns = heads) ----
       uint32_t pb[2][2];  // [hi / lo][b0, b1]
       if constexpr (C::kBf16) {
@@ -513,6 +542,30 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
       } else {
         pb[0][0] = movmatrix_t(pack2<PKV_F16>(p00, p01));
         pb[0][1] = movmatrix_t(pack2<PKV_F16>(p10, p11));
+      }
+      // ---- rescale O to the new maximum (and V scale unit); biased V codes:
+      //      also take off the bias the tile's MMAs are about to add ----
+      if constexpr (C::kVBias) {
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};  // column sums of P^T: heads 2 q4, 2 q4 + 1 (rows g, g + 8 alike)
+        const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
+        mma_16816(ps, ones, pb[0][0], pb[0][1], false);
+        const float b0 = -C::kBiasLo * ps[0], b1 = -C::kBiasLo * ps[1];
+        const float b2 = -C::kBiasHi * ps[0], b3 = -C::kBiasHi * ps[1];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          oacc[i][0] = fmaf(oacc[i][0], al0, b0);
+          oacc[i][1] = fmaf(oacc[i][1], al1, b1);
+          oacc[i][2] = fmaf(oacc[i][2], al0, b2);
+          oacc[i][3] = fmaf(oacc[i][3], al1, b3);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          oacc[i][0] *= al0;
+          oacc[i][1] *= al1;
+          oacc[i][2] *= al0;
+          oacc[i][3] *= al1;
+        }
       }
       // ---- O^T += V^T P^T ----
       const bool tail = ntok < kBS;
@@ -537,8 +590,8 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
             uint32_t a[4];
-            int4_pair_to_f16x2(prmt(x0, y0, vsel[b]), a[0], a[1]);
-            int4_pair_to_f16x2(prmt(x1, y1, vsel[b]), a[2], a[3]);
+            int4_pair_to_f16x2_biased(prmt(x0, y0, vsel[b]), a[0], a[1]);
+            int4_pair_to_f16x2_biased(prmt(x1, y1, vsel[b]), a[2], a[3]);
             mma_16816(oacc[4 * w + b], a, pb[0][0], pb[0][1], false);
           }
         }
@@ -553,10 +606,17 @@ __global__ void __launch_bounds__(MmaCfg<G, CDT, QDT>::kThreads, MmaCfg<G, CDT, 
         for (int w = 0; w < 4; ++w) {
           const uint32_t x0 = word(vr[0], w), y0 = word(vr[1], w), x1 = word(vr[2], w), y1 = word(vr[3], w);
           uint32_t a[4], b[4];
-          code4_to_f16x2<C::VT>(prmt(x0, y0, 0x5140), a[0], a[1]);
-          code4_to_f16x2<C::VT>(prmt(x1, y1, 0x5140), a[2], a[3]);
-          code4_to_f16x2<C::VT>(prmt(x0, y0, 0x7362), b[0], b[1]);
-          code4_to_f16x2<C::VT>(prmt(x1, y1, 0x7362), b[2], b[3]);
+          if constexpr (C::kVBias) {  // INT8
+            int8x4_to_f16x2_biased(prmt(x0, y0, 0x5140), a[0], a[1]);
+            int8x4_to_f16x2_biased(prmt(x1, y1, 0x5140), a[2], a[3]);
+            int8x4_to_f16x2_biased(prmt(x0, y0, 0x7362), b[0], b[1]);
+            int8x4_to_f16x2_biased(prmt(x1, y1, 0x7362), b[2], b[3]);
+          } else {
+            code4_to_f16x2<C::VT>(prmt(x0, y0, 0x5140), a[0], a[1]);
+            code4_to_f16x2<C::VT>(prmt(x1, y1, 0x5140), a[2], a[3]);
+            code4_to_f16x2<C::VT>(prmt(x0, y0, 0x7362), b[0], b[1]);
+            code4_to_f16x2<C::VT>(prmt(x1, y1, 0x7362), b[2], b[3]);
+          }
           mma_16816(oacc[2 * w], a, pb[0][0], pb[0][1], false);
           mma_16816(oacc[2 * w + 1], b, pb[0][0], pb[0][1], false);
         }

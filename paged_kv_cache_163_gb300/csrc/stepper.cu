@@ -180,15 +180,21 @@ bool plan_cascade(pkv_stepper *st, const int32_t *tables, int32_t mb, const int3
     a = e;
   }
   if (pp.num_groups == 0) return false;
+  // mma.sync kernel: chunks so that it takes about 45% of the SMs (measured
+  // best for it).  tcgen05 kernel: chunks of about chunk_tiles tiles each,
+  // so it takes few SMs and the decode keeps the rest.
+  pl.umma = pkv::prefix_uses_umma(P.q_dtype, P.cache_dtype) ? 1 : 0;
   const int32_t target = std::max(8, st->sms * 5 / 11);
   const int32_t want = std::max(1, (target + rows_blocks * P.num_kv_heads - 1) / (rows_blocks * P.num_kv_heads));
+  const int32_t per_chunk = std::max(1, pkv::prefix_umma_chunk_tiles());
   std::fill(pl.start, pl.start + n, 0);
   std::fill(pl.chunks, pl.chunks + n, 0);
   std::fill(pp.base, pp.base + n, 0);
   int32_t units = 0, slot = 0;
   for (int32_t gi = 0; gi < pp.num_groups; ++gi) {
     pkv::PrefixGroup &g = pp.group[gi];
-    g.chunks = std::min({want, pkv::kMaxPrefixChunks, std::max(1, g.tiles / 4)});
+    g.chunks = pl.umma ? std::min(pkv::kMaxPrefixChunks, std::max(1, (g.tiles + per_chunk - 1) / per_chunk))
+                       : std::min({want, pkv::kMaxPrefixChunks, std::max(1, g.tiles / 4)});
     g.unit0 = units;
     units += g.row_blocks * g.chunks * P.num_kv_heads;
     for (int32_t k = 0; k < g.members; ++k) {

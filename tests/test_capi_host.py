@@ -215,3 +215,21 @@ def test_sizing_calls_match_oracle():
         for dt in ("bf16", "fp8_e4m3", "int8", "fp8_e4m3_int4"):
             assert capi.pkv_pool_blocks(budget, layers, hkv, d, dt) == sizing.pool_blocks(budget, layers, hkv, d, dt)
     assert capi.pkv_kv_bytes(-1, 1, 64, 1, "f16") == -1
+
+
+def test_kernel_selectors_validate_and_round_trip():
+    """The decode- and prefix-kernel selectors refuse unknown values and keep the last valid one."""
+    capi.pkv_set_prefix_kernel("tcgen05", 24)
+    assert capi.pkv_get_prefix_kernel() == "tcgen05"
+    with pytest.raises(capi.PkvError):
+        capi.pkv_set_prefix_kernel(7, 0)
+    with pytest.raises(capi.PkvError):
+        capi.pkv_set_prefix_kernel("mma_sync", -1)
+    with pytest.raises(capi.PkvError):
+        capi.pkv_set_prefix_kernel("mma_sync", 4097)
+    assert capi.pkv_get_prefix_kernel() == "tcgen05"
+    capi.pkv_set_prefix_kernel("auto", 0)
+    assert capi.pkv_get_prefix_kernel() == "auto"
+    with pytest.raises(capi.PkvError):
+        capi.pkv_set_decode_kernel(9)
+    assert capi.pkv_get_decode_kernel() == "auto"

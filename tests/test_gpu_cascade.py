@@ -7,6 +7,11 @@ The attention is unchanged: results must match the oracle (fp64 over each
 member's whole context) within the tolerance, match the step without the
 cascade within it too (the fp32 additions come in another order), and
 leave the cache byte for byte as the plain step does.
+
+16-bit caches run both prefix kernels: the tcgen05 one (tensor-memory
+accumulators, 64-token sub-chunks; also with chunks that are not a
+multiple of a sub-chunk, and with one chunk of many sub-chunks) and the
+warp-level mma.sync one.
 """
 import numpy as np
 import pytest
@@ -26,6 +31,16 @@ def play():
     from paged_kv_cache_163_gb300 import capi, play as p
     capi.load()
     return p
+
+
+@pytest.fixture
+def prefix_kernel(request):
+    """Run a test under one prefix kernel (and chunk size), then restore the default."""
+    from paged_kv_cache_163_gb300 import capi
+    kind, chunk = request.param
+    capi.pkv_set_prefix_kernel(kind, chunk)
+    yield kind
+    capi.pkv_set_prefix_kernel("auto", 0)
 
 
 def _rows(rng, n, hkv, d, dtype):
@@ -93,6 +108,16 @@ CASES = [("bf16", "bf16", 32, 8, 16), ("f16", "f16", 32, 4, 16), ("bf16", "fp8_e
          ("bf16", "fp8_e5m2", 16, 8, 16)]
 
 
+SIXTEEN_BIT = [c for c in CASES if c[1] in ("bf16", "f16")]
+PREFIX_KERNELS = [("tcgen05", 0), ("tcgen05", 5), ("tcgen05", 200), ("mma_sync", 0)]
+
+
+@pytest.mark.parametrize("prefix_kernel", PREFIX_KERNELS, indirect=True, ids=lambda k: f"{k[0]}-{k[1]}")
+@pytest.mark.parametrize("q_dtype,cache_dtype,hq,hkv,bs", SIXTEEN_BIT)
+def test_cascade_16bit_both_prefix_kernels(play, prefix_kernel, q_dtype, cache_dtype, hq, hkv, bs):
+    test_cascade_matches_oracle_and_plain_step(play, q_dtype, cache_dtype, hq, hkv, bs)
+
+
 @pytest.mark.parametrize("q_dtype,cache_dtype,hq,hkv,bs", CASES)
 def test_cascade_matches_oracle_and_plain_step(play, q_dtype, cache_dtype, hq, hkv, bs):
     groups = [(1500, [1564, 1600, 1501, 1800, 1517]), (700, [705, 1600]), (300, [340, 341, 342])]
@@ -115,7 +140,8 @@ def test_cascade_matches_oracle_and_plain_step(play, q_dtype, cache_dtype, hq, h
     off.close()
 
 
-def test_cascade_with_more_rows_than_one_cta(play):
+@pytest.mark.parametrize("prefix_kernel", [("tcgen05", 0), ("mma_sync", 0)], indirect=True, ids=lambda k: k[0])
+def test_cascade_with_more_rows_than_one_cta(play, prefix_kernel):
     """40 members x 4 query heads = 160 rows: two row blocks of the prefix kernel."""
     groups = [(1024, [1024 + 1 + 7 * i for i in range(40)])]
     kw = dict(hq=32, hkv=8, d=128, q_dtype="bf16", cache_dtype="bf16", bs=16, seed=3)
@@ -138,7 +164,8 @@ def test_short_shared_prefix_stays_plain(play):
     on.close()
 
 
-def test_prefix_share_workload_through_the_step(play):
+@pytest.mark.parametrize("prefix_kernel", [("tcgen05", 0), ("mma_sync", 0)], indirect=True, ids=lambda k: k[0])
+def test_prefix_share_workload_through_the_step(play, prefix_kernel):
     """The prefix-share workload (32 forks of a 1500-token prefix) steps with the cascade, several steps."""
     w = wl.make(4, extra_steps=4)
     cache, out = play.run(w, out_dtype="f32")
