@@ -52,22 +52,22 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu capture), keyed by workload and by the hash of the decode kernel source it
 # was taken on; reported only while the source is unchanged.
 NCU_TRAFFIC = {
-    # decode kernel source 0496016a5ccc7739: tensor-core kernel with the step's append fused in, 16-warp
-    # CTAs for one-byte caches, 4-bit V for the mixed cache, K and V scales of a tile in one 128-byte
-    # unit, first cache copies before the programmatic wait behind kernels that write no cache,
-    # 16-byte output stores, cascade for shared prefixes; default "auto" variant.
+    # decode kernel source 169e922fdc625868: tensor-core kernel with the step's append fused in, 16-warp
+    # CTAs for one-byte caches, biased INT8 / 4-bit MMA operands, K and V scales of a tile in one
+    # 128-byte unit, first cache copies before the programmatic wait behind kernels that write no cache,
+    # cascade with the mma.sync prefix kernel; default "auto" variants.
     # dram__bytes_read.sum + dram__bytes_write.sum of one call (the fifth decode call of a --steps 4
     # --warmup 3 run; prefix-share: its prefix kernel plus its decode, whose DRAM reads include the
     # prefix partials ncu's replay flushed from L2)
-    ("llama3-8b", "0496016a5ccc7739"): 145_694_464,
-    ("llama3-8b:bs32", "0496016a5ccc7739"): 145_843_456,
-    ("mha7b-40layer", "0496016a5ccc7739"): 271_298_304,
-    ("prefix-share", "0496016a5ccc7739"): 52_879_616,
-    ("long-fp8", "0496016a5ccc7739"): 796_831_744,
-    ("long-fp8:fp8_e5m2", "0496016a5ccc7739"): 796_802_304,
-    ("long-fp8:int8", "0496016a5ccc7739"): 796_821_504,
-    ("long-fp8:fp8_e4m3_int4", "0496016a5ccc7739"): 604_133_632,
-    ("long-fp8:bs32", "0496016a5ccc7739"): 797_052_160,
+    ("llama3-8b", "169e922fdc625868"): 145_499_136,
+    ("llama3-8b:bs32", "169e922fdc625868"): 145_780_992,
+    ("mha7b-40layer", "169e922fdc625868"): 271_572_736,
+    ("prefix-share", "169e922fdc625868"): 52_878_592,
+    ("long-fp8", "169e922fdc625868"): 796_690_688,
+    ("long-fp8:fp8_e5m2", "169e922fdc625868"): 796_850_688,
+    ("long-fp8:int8", "169e922fdc625868"): 796_819_712,
+    ("long-fp8:fp8_e4m3_int4", "169e922fdc625868"): 605_418_752,
+    ("long-fp8:bs32", "169e922fdc625868"): 797_131_008,
 }
 
 
@@ -405,7 +405,8 @@ def run_ours(args, world, rank, local):
     traffic_key = args.workload if args.cache_dtype is None else f"{args.workload}:{args.cache_dtype}"
     if args.block_size != 16:
         traffic_key += f":bs{args.block_size}"
-    traffic = NCU_TRAFFIC.get((traffic_key, kernel_hash())) if args.kernel == "auto" else None
+    traffic = (NCU_TRAFFIC.get((traffic_key, kernel_hash()))
+               if args.kernel == "auto" and args.prefix_kernel == "auto" else None)
     value = whole_job_rate(world, kv_total, t_total) / 1e9
     result = {
         "metric": METRIC,
