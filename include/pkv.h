@@ -514,6 +514,19 @@ typedef struct {
 } pkv_copy_segment;
 pkv_status pkv_copy_segments(const pkv_copy_segment *segs, int32_t num_segs, pkv_stream_t stream);
 
+/* Register the next pkv_stepper_step's host-to-device input copies (its
+ * k_new, v_new and q rows living in page-locked host memory; the step is
+ * given the device copies).  The step launches them as one
+ * pkv_copy_segments kernel after its host work (block manager, tables) and
+ * right before its first attention launch, so the GPU does not wait for
+ * the host between the copy and the attention; the first layer's decode may
+ * start its first cache copies while the copy runs (the copy writes no
+ * cache).  Same rules as pkv_copy_segments (at most PKV_MAX_COPY_SEGMENTS,
+ * 16-byte aligned, sizes multiples of 16; PKV_ERR_INVALID otherwise, nothing
+ * registered).  The registration applies to the next step call only, which
+ * drops it if it fails before launching; a new call replaces it. */
+pkv_status pkv_stepper_copy_inputs(pkv_stepper *st, const pkv_copy_segment *segs, int32_t num_segs);
+
 /* Number of kernel launches the calling thread has made through this
  * library (for launch accounting). */
 int64_t pkv_launch_count(void);

@@ -131,6 +131,7 @@ _PROTOS = {
     "pkv_read_device_error": (C.c_int, [_vp, _i32p, C.c_int32, _vp]),
     "pkv_launch_count": (C.c_int64, []),
     "pkv_copy_segments": (C.c_int, [C.c_void_p, C.c_int32, _vp]),
+    "pkv_stepper_copy_inputs": (C.c_int, [_vp, C.c_void_p, C.c_int32]),
     "pkv_set_decode_kernel": (C.c_int, [C.c_int]),
     "pkv_set_prefix_kernel": (C.c_int, [C.c_int, C.c_int32]),
     "pkv_get_prefix_kernel": (C.c_int, []),
@@ -495,15 +496,25 @@ class StepScratch:
         self.addr = (self.src.ctypes.data, self.dst.ctypes.data, self.ncow.ctypes.data)
 
 
-def pkv_copy_segments(pairs, stream) -> None:
-    """One-launch copy of [(dst tensor, src tensor), ...] (same byte sizes; device or pinned host memory)."""
+def _segments(pairs, where):
     segs = (CopySegment * max(1, len(pairs)))()
     for i, (dst, src) in enumerate(pairs):
         nb = src.numel() * src.element_size()
         if dst.numel() * dst.element_size() != nb:
-            raise ValueError("pkv_copy_segments: sizes differ")
+            raise ValueError(f"{where}: sizes differ")
         segs[i].dst, segs[i].src, segs[i].bytes = dst.data_ptr(), src.data_ptr(), nb
-    _check(load().pkv_copy_segments(segs, len(pairs), stream), "pkv_copy_segments")
+    return segs
+
+
+def pkv_copy_segments(pairs, stream) -> None:
+    """One-launch copy of [(dst tensor, src tensor), ...] (same byte sizes; device or pinned host memory)."""
+    _check(load().pkv_copy_segments(_segments(pairs, "pkv_copy_segments"), len(pairs), stream), "pkv_copy_segments")
+
+
+def pkv_stepper_copy_inputs(st, pairs) -> None:
+    """Register [(device tensor, pinned host tensor), ...] copies for the stepper's next step."""
+    _check(load().pkv_stepper_copy_inputs(st, _segments(pairs, "pkv_stepper_copy_inputs"), len(pairs)),
+           "pkv_stepper_copy_inputs")
 
 
 def current_stream_handle(device_index: int) -> int:

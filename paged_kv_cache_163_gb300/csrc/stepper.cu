@@ -78,6 +78,7 @@ struct pkv_stepper {
   pkv::CascadePlan plan;
   std::vector<int32_t> order;    // scratch for the cascade plan
   int64_t cascades = 0;
+  std::vector<pkv_copy_segment> in_copies;  // the next step's host-input copies (pkv_stepper_copy_inputs)
 };
 
 namespace {
@@ -301,6 +302,21 @@ void pkv_stepper_destroy(pkv_stepper *st) {
   delete st;
 }
 
+pkv_status pkv_stepper_copy_inputs(pkv_stepper *st, const pkv_copy_segment *segs, int32_t num_segs) {
+  if (!st) return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_copy_inputs: NULL stepper");
+  if (num_segs < 0 || num_segs > PKV_MAX_COPY_SEGMENTS || (num_segs > 0 && !segs))
+    return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_copy_inputs: bad segment count");
+  for (int32_t i = 0; i < num_segs; ++i) {
+    const pkv_copy_segment &g = segs[i];
+    const uintptr_t a = reinterpret_cast<uintptr_t>(g.dst) | reinterpret_cast<uintptr_t>(g.src);
+    if (g.bytes < 0 || (g.bytes & 15) || (g.bytes && (!g.dst || !g.src || (a & 15u))))
+      return pkv::fail(PKV_ERR_INVALID,
+                       "pkv_stepper_copy_inputs: NULL or misaligned pointer, or a size not a multiple of 16");
+  }
+  st->in_copies.assign(segs, segs + num_segs);
+  return PKV_OK;
+}
+
 pkv_status pkv_stepper_use_cascade(pkv_stepper *st, int32_t enable) {
   if (!st) return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_use_cascade: NULL stepper");
   st->cascade = enable != 0;
@@ -333,7 +349,11 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
                             int64_t out_layer_stride, float scale, int32_t *cow_src, int32_t *cow_dst,
                             int32_t *num_cow, int32_t *d_error, void *attn_begin, void *attn_end,
                             pkv_stream_t stream) {
-  if (!st || !bm || n < 0 || n > st->max_seqs || (n > 0 && (!seq_ids || !k_new || !v_new || !q || !out)))
+  if (!st) return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: bad argument");
+  // registered input copies belong to this step only, whatever becomes of it
+  std::vector<pkv_copy_segment> in_copies;
+  in_copies.swap(st->in_copies);
+  if (!bm || n < 0 || n > st->max_seqs || (n > 0 && (!seq_ids || !k_new || !v_new || !q || !out)))
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: bad argument");
   if (pkv_bm_block_size(bm) != st->pool.block_size)
     return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: the block manager's block size differs from the pool's");
@@ -411,6 +431,17 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
       if (s != PKV_OK) return s;
     }
   }
+  // Host inputs registered for this step: one copy kernel, launched only now
+  // that the host work is done, so the GPU goes from it straight to the
+  // attention launches.  It is an ordinary launch (it starts after every
+  // kernel before it, the copy-on-write copies included) and writes no K/V
+  // cache, so a one-layer step's decode may start its first cache copies
+  // while it runs.
+  const bool input_copy = !in_copies.empty();
+  if (input_copy) {
+    s = pkv_copy_segments(in_copies.data(), static_cast<int32_t>(in_copies.size()), stream);
+    if (s != PKV_OK) return s;
+  }
   // The step's attention launches: with more layers one small kernel first
   // copies the staging to Dh; layer 0 reads the staging in place.
   // Eager launches carry the lengths in their parameters; a captured graph
@@ -434,10 +465,12 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
       const int32_t *t_lens = l == 0 ? Hd + 3 * n : d_lens;
       const int32_t *t_tables = l == 0 ? Hd + 4 * n : d_tables;
       // The kernel before a layer's decode writes no K/V cache memory when it
-      // is the previous layer's decode (other layers' rows) or this step's
-      // metadata copy (launched after the copy-on-write copies), so the decode
-      // may start its first cache copies before waiting for it.
-      const int programmatic = (l > 0 || P.num_layers > 1) ? 2 : 1;
+      // is the previous layer's decode (other layers' rows), this step's
+      // metadata copy or its host-input copy (both launched after the
+      // copy-on-write copies), so the decode may start its first cache copies
+      // before waiting for it.  (A graph replay carries the launches as
+      // captured; its first kernel follows the input copy in stream order.)
+      const int programmatic = (l > 0 || P.num_layers > 1 || (eager && input_copy)) ? 2 : 1;
       pkv_status r = pkv::attention_decode(
           programmatic, layer_ptr(k_new, kv_layer_stride, l), layer_ptr(v_new, kv_layer_stride, l),
           layer_ptr(out, out_layer_stride, l), out_dtype, layer_ptr(q, q_layer_stride, l), P.q_dtype,

@@ -315,8 +315,9 @@ class PagedKVCache:
         """A step whose inputs and output are page-locked host tensors.
 
         One copy kernel moves the step's K/V rows and queries from host to
-        device buffers (read in place over the host link; the step's first
-        decode starts its prologue meanwhile), and the decode kernels store
+        device buffers (read in place over the host link), launched by the
+        step executor after its host work and right before the attention (the
+        step's first decode starts meanwhile), and the decode kernels store
         the output straight into the host tensor.  Synchronise the stream
         before reading ``out`` on the host.
         """
@@ -331,10 +332,11 @@ class PagedKVCache:
             self._io = [torch.empty(t.shape, dtype=t.dtype, device=self.device) for t in (k_rows, v_rows, q)]
             self._io_key = key
         kd, vd, qd = self._io
-        sh = capi.current_stream_handle(self._device_index) if stream is None else stream
         ins = [(d, h) for d, h in ((kd, k_rows), (vd, v_rows), (qd, q)) if not h.is_cuda]
         if ins:
-            capi.pkv_copy_segments(ins, sh)
+            key = (len(seq_ids), q.shape[-2], q.dtype)
+            st = self._stepper if key == self._stepper_key else self._stepper_for(*key)
+            capi.pkv_stepper_copy_inputs(st, ins)
         return self._step_native(seq_ids, k_rows if k_rows.is_cuda else kd, v_rows if v_rows.is_cuda else vd,
                                  q if q.is_cuda else qd, scale, out, stream, marks)
 
