@@ -11,7 +11,8 @@ leave the cache byte for byte as the plain step does.
 16-bit caches run both prefix kernels: the tcgen05 one (tensor-memory
 accumulators, 64-token sub-chunks; also with chunks that are not a
 multiple of a sub-chunk, and with one chunk of many sub-chunks) and the
-warp-level mma.sync one.
+warp-level mma.sync one, for GQA groups of 1, 2, 4 and 8; asking for the
+tcgen05 kernel with a one-byte cache keeps the mma.sync one.
 """
 import numpy as np
 import pytest
@@ -105,7 +106,7 @@ def _build(play, groups, loners, *, hq, hkv, d, q_dtype, cache_dtype, bs, seed, 
 
 CASES = [("bf16", "bf16", 32, 8, 16), ("f16", "f16", 32, 4, 16), ("bf16", "fp8_e4m3", 32, 8, 16),
          ("bf16", "fp8_e4m3_int4", 32, 8, 16), ("f16", "int8", 8, 8, 16), ("bf16", "bf16", 32, 8, 32),
-         ("bf16", "fp8_e5m2", 16, 8, 16)]
+         ("bf16", "fp8_e5m2", 16, 8, 16), ("bf16", "bf16", 8, 8, 16), ("f16", "f16", 16, 8, 16)]
 
 
 SIXTEEN_BIT = [c for c in CASES if c[1] in ("bf16", "f16")]
@@ -115,6 +116,13 @@ PREFIX_KERNELS = [("tcgen05", 0), ("tcgen05", 5), ("tcgen05", 200), ("mma_sync",
 @pytest.mark.parametrize("prefix_kernel", PREFIX_KERNELS, indirect=True, ids=lambda k: f"{k[0]}-{k[1]}")
 @pytest.mark.parametrize("q_dtype,cache_dtype,hq,hkv,bs", SIXTEEN_BIT)
 def test_cascade_16bit_both_prefix_kernels(play, prefix_kernel, q_dtype, cache_dtype, hq, hkv, bs):
+    test_cascade_matches_oracle_and_plain_step(play, q_dtype, cache_dtype, hq, hkv, bs)
+
+
+@pytest.mark.parametrize("prefix_kernel", [("tcgen05", 0)], indirect=True, ids=lambda k: k[0])
+@pytest.mark.parametrize("q_dtype,cache_dtype,hq,hkv,bs", [("bf16", "fp8_e4m3", 32, 8, 16), ("f16", "int8", 8, 8, 16)])
+def test_tcgen05_request_on_one_byte_cache_falls_back(play, prefix_kernel, q_dtype, cache_dtype, hq, hkv, bs):
+    """The tcgen05 prefix kernel takes 16-bit caches; a one-byte cache keeps the mma.sync one, correctly."""
     test_cascade_matches_oracle_and_plain_step(play, q_dtype, cache_dtype, hq, hkv, bs)
 
 
