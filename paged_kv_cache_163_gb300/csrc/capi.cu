@@ -18,6 +18,7 @@
 #include "dtypes.h"
 #include "pkv.h"
 #include "status.h"
+#include "trace.h"
 
 namespace pkv {
 namespace {
@@ -284,6 +285,7 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
                                 const int32_t *src, const int32_t *dst, int32_t num_pairs,
                                 int32_t num_kv_heads, int32_t head_dim, pkv_dtype cache_dtype,
                                 int32_t num_blocks, int32_t block_size, int32_t *d_error, pkv_stream_t stream) {
+  pkv::TraceRange trace("pkv.copy_blocks");
   if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0)
     return fail(PKV_ERR_INVALID, "paged_kv_copy_blocks: bad sizes");
   if (block_size != PKV_BLOCK_SIZE && block_size != PKV_BLOCK_SIZE_32)
@@ -310,6 +312,7 @@ pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int
                            void *k_cache, void *v_cache, pkv_dtype cache_dtype, float *k_scale,
                            float *v_scale, int32_t num_blocks, int32_t block_size, int32_t *d_error,
                            pkv_stream_t stream) {
+  pkv::TraceRange trace("pkv.append");
   if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0)
     return fail(PKV_ERR_INVALID, "paged_kv_append: bad sizes");
   if (block_size != PKV_BLOCK_SIZE && block_size != PKV_BLOCK_SIZE_32)
@@ -337,6 +340,7 @@ pkv_status paged_kv_append(const void *k, const void *v, pkv_dtype in_dtype, int
 }
 
 pkv_status pkv_copy_segments(const pkv_copy_segment *segs, int32_t num_segs, pkv_stream_t stream) {
+  pkv::TraceRange trace("pkv.copy_segments");
   if (num_segs < 0 || num_segs > PKV_MAX_COPY_SEGMENTS || (num_segs > 0 && !segs))
     return fail(PKV_ERR_INVALID, "pkv_copy_segments: bad segment count");
   CopySegs c{};
@@ -555,6 +559,7 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
                                   int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                                   int32_t block_size, float scale, void *workspace, size_t workspace_bytes,
                                   int32_t *d_error, pkv_stream_t stream) {
+  pkv::TraceRange trace("pkv.decode");
   return pkv::attention_decode(false, nullptr, nullptr, out, out_dtype, q, q_dtype, k_cache, v_cache, cache_dtype,
                                k_scale, v_scale, block_tables, max_blocks_per_seq, context_lens, max_context_len,
                                num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
@@ -569,6 +574,7 @@ pkv_status paged_attention_decode_append(void *out, pkv_dtype out_dtype, const v
                                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                          int32_t num_blocks, int32_t block_size, float scale, void *workspace,
                                          size_t workspace_bytes, int32_t *d_error, pkv_stream_t stream) {
+  pkv::TraceRange trace("pkv.decode_append");
   if (num_seqs > 0 && (!k_new || !v_new))
     return fail(PKV_ERR_INVALID, "paged_attention_decode_append: NULL k_new or v_new");
   return pkv::attention_decode(false, k_new, v_new, out, out_dtype, q, q_dtype, k_cache, v_cache, cache_dtype,

@@ -35,6 +35,7 @@
 #include "dtypes.h"
 #include "pkv.h"
 #include "status.h"
+#include "trace.h"
 
 // What a captured step graph baked in besides the stepper's own buffers.
 struct GraphKey {
@@ -349,6 +350,7 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
                             int64_t out_layer_stride, float scale, int32_t *cow_src, int32_t *cow_dst,
                             int32_t *num_cow, int32_t *d_error, void *attn_begin, void *attn_end,
                             pkv_stream_t stream) {
+  pkv::TraceRange trace("pkv.step");
   if (!st) return pkv::fail(PKV_ERR_INVALID, "pkv_stepper_step: bad argument");
   // registered input copies belong to this step only, whatever becomes of it
   std::vector<pkv_copy_segment> in_copies;
@@ -402,10 +404,14 @@ pkv_status pkv_stepper_step(pkv_stepper *st, pkv_bm *bm, const int64_t *seq_ids,
   int32_t *H = st->host + h * st->half_ints;
   int32_t *slots = H, *src = H + n, *dst = H + 2 * n, *lens = H + 3 * n, *tables = H + 4 * n;
   int32_t ncow = 0;
-  pkv_status s = pkv_seq_append_slots(bm, seq_ids, n, slots, src, dst, &ncow);
-  if (s != PKV_OK) return s;
-  s = pkv_build_block_tables(bm, seq_ids, n, mb, tables, lens);
-  if (s != PKV_OK) return s;
+  pkv_status s;
+  {
+    pkv::TraceRange host_trace("pkv.step.block_manager");
+    s = pkv_seq_append_slots(bm, seq_ids, n, slots, src, dst, &ncow);
+    if (s != PKV_OK) return s;
+    s = pkv_build_block_tables(bm, seq_ids, n, mb, tables, lens);
+    if (s != PKV_OK) return s;
+  }
   if (num_cow) *num_cow = ncow;
   if (cow_src && ncow) std::memcpy(cow_src, src, sizeof(int32_t) * ncow);
   if (cow_dst && ncow) std::memcpy(cow_dst, dst, sizeof(int32_t) * ncow);
