@@ -116,3 +116,34 @@ def test_registered_input_copies_rules(play):
     torch.cuda.synchronize()
     assert cache.check() == 0
     cache.close()
+
+
+def test_host_tensors_with_graph_replay(play):
+    """Host-buffer steps replayed from CUDA graphs (the input copy launched before the graph) equal device steps.
+
+    Graph steps widen the tables to a power of two, which sets the grid from a
+    larger context bound; the lengths here are large enough that both kinds
+    of step run a full wave, so the work split (and the sum order) is the same.
+    """
+    rng = np.random.default_rng(12)
+    lens = rng.integers(2500, 3000, 8).tolist()
+    w = wl.custom("hostio-graph", lens=lens, num_q_heads=32, num_kv_heads=8, head_dim=128, q_dtype="bf16",
+                  cache_dtype="fp8_e4m3", num_layers=2, seed=35, slack=0.5)
+    a, b = play.new_cache(w), play.new_cache(w)
+    play.prefill(w, a)
+    play.prefill(w, b)
+    b.use_graphs(True)
+    out_h = None
+    for step in range(4):
+        k, v, q = play.step_inputs(w, step)
+        out_d = a.step(w.seq_ids, k, v, q, scale=w.scale)
+        if out_h is None:
+            out_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        b.step(w.seq_ids, k.cpu().pin_memory(), v.cpu().pin_memory(), q.cpu().pin_memory(), scale=w.scale,
+               out=out_h)
+        torch.cuda.synchronize()
+        assert torch.equal(out_d.cpu(), out_h), f"step {step}"
+    assert b.graph_stats()[1] > 0, "the host-buffer steps should replay graphs"
+    assert a.check() == 0 and b.check() == 0
+    a.close()
+    b.close()
