@@ -38,6 +38,19 @@ __device__ __forceinline__ float2 unpack2<PKV_F16>(uint32_t w) {
   return __half22float2(h);
 }
 
+// Hardware approximations (PTX ex2.approx / rcp.approx): 2^x with relative
+// error ~2^-22 (2^-inf = 0), and 1/x within 1 ulp; subnormals flush to zero.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---- one-byte cache codes ----------------------------------------------------
 // FP8 E4M3, FP8 E5M2 and INT8 caches store one byte per element and one
 // fp32 scale per (token, KV head); the value is code value x scale.
