@@ -251,7 +251,7 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
 /* Reshape-and-cache ("KV Cache 与 vLLM" §1.3 append; "企业官网建设流程全解析"
  * §3.2): token t's rows k[t], v[t] ([num_kv_heads][head_dim], in_dtype
  * F16 or BF16) are written to slot slot_mapping[t] (device int32
- * [num_tokens]; -1 skips the token; >= num_blocks * 16 sets
+ * [num_tokens]; -1 skips the token; >= num_blocks * block_size sets
  * PKV_DEVERR_BAD_SLOT and skips it).
  * 16-bit caches: cache_dtype must equal in_dtype; the copy is exact.
  * One-byte caches ("KV Cache优化实战" §3.2-§3.3, per-token per-head scale):
@@ -394,11 +394,11 @@ pkv_status paged_attention_decode_static(void *out, pkv_dtype out_dtype, const v
 /* ("KV Cache 与 vLLM" §3.1-§3.4, "企业官网建设流程全解析" §3.2): the block    */
 /* manager gives every sequence a slot (taking or copying blocks), the slot   */
 /* mapping, copy pairs, lengths and block tables are written to page-locked   */
-/* host staging that the first layer's kernels read in place (its append      */
-/* also copies them to device memory for the later layers), and for every     */
-/* layer the shared blocks are copied, the new K/V rows are written and the   */
-/* new queries attend.  Host work is O(batch + table size); all device work   */
-/* is enqueued on `stream`.                                                   */
+/* host staging that the first layer's kernels read in place (with more than  */
+/* one layer, one small kernel also copies them to device memory for the     */
+/* later layers), and for every layer the shared blocks are copied, the new   */
+/* K/V rows are written and the new queries attend.  Host work is             */
+/* O(batch + table size); all device work is enqueued on `stream`.            */
 /* ------------------------------------------------------------------------ */
 typedef struct {
   int32_t num_layers, num_blocks, num_kv_heads, num_q_heads, head_dim;
