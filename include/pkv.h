@@ -261,7 +261,7 @@ pkv_status paged_kv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, fl
  *   FP8_E4M3: R = 448,   Q = nearest E4M3 code, ties to even, saturating;
  *   FP8_E5M2: R = 57344, Q = nearest E5M2 code, ties to even, saturating;
  *   INT8:     R = 127,   Q = nearest integer, ties to even, clamped to
- *             [-127, 127] (two's complement byte);
+ *             [-127, 127], stored as the byte Q + 128 (zero point 128);
  *   FP8_E4M3_INT4: K rows as FP8_E4M3; V rows R = 7, Q = nearest integer,
  *             ties to even, clamped to [-7, 7], stored two a byte as
  *             code + 8 (even element in the low nibble);

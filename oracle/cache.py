@@ -21,7 +21,8 @@ Storage types:
 
   - ``fp8_e4m3``: R = 448, Q = nearest E4M3 code (``fp8.encode``);
   - ``fp8_e5m2``: R = 57344, Q = nearest E5M2 code (``fp8.e5m2_encode``);
-  - ``int8``: R = 127, Q = nearest integer in [-127, 127] (``int8.encode``).
+  - ``int8``: R = 127, Q = nearest integer in [-127, 127] (``int8.encode``),
+    stored as the byte Q + 128 (``int8.to_bytes``).
 
   The dequantised value is ``value(code) * s`` in fp64.
 * ``fp8_e4m3_int4``: the mixed scheme of "KV Cache优化实战" §3.2 (8-bit
@@ -45,7 +46,7 @@ DTYPES = ("f16", "bf16", "fp8_e4m3", "fp8_e5m2", "int8", "fp8_e4m3_int4")
 CODE_TYPES = {
     "fp8_e4m3": (fp8.MAX_FINITE, fp8.encode, fp8.decode),
     "fp8_e5m2": (fp8.E5M2_MAX_FINITE, fp8.e5m2_encode, fp8.e5m2_decode),
-    "int8": (int8.MAX_CODE, lambda y: int8.encode(y).view(np.uint8), int8.decode),
+    "int8": (int8.MAX_CODE, lambda y: int8.to_bytes(int8.encode(y)), lambda b: int8.decode(int8.from_bytes(b))),
     "int4": (int4.MAX_CODE, lambda y: int4.pack(int4.encode(y)), int4.decode),
 }
 # cache types whose K and V halves are stored differently: (K type, V type)
@@ -65,7 +66,7 @@ def row_bytes(part: str, head_dim: int) -> int:
 def quantize_rows(x: np.ndarray, dtype: str = "fp8_e4m3"):
     """Per-row quantisation of float32 rows ``[..., head_dim]`` to codes.
 
-    Returns (stored bytes uint8 [..., head_dim] -- an int8 code as its byte;
+    Returns (stored bytes uint8 [..., head_dim] -- an int8 code as the byte code + 128;
     [..., head_dim / 2] for int4 --, scale float32 [...]).
     """
     r, enc, _ = CODE_TYPES[dtype]

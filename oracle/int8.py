@@ -11,6 +11,11 @@ to the nearest integer, ties to even, clamped to [-127, 127]; the value is
 ``code * scale``.  (llama.cpp's q8_0 uses 32-element groups and an fp16
 scale; the per-(token, head) granularity matches the other one-byte
 caches here.)
+
+The pages fix no byte encoding either.  A code is stored as the byte
+``code + 128`` (an unsigned byte with zero point 128, as asymmetric uint8
+schemes store theirs), so bytes 1..255 hold codes -127..127; byte 0 is
+never written.
 """
 from __future__ import annotations
 
@@ -29,8 +34,18 @@ def encode(y: np.ndarray) -> np.ndarray:
 
 
 def decode(codes: np.ndarray) -> np.ndarray:
-    """fp64 values of int8 codes (given as int8, or as their uint8 bytes)."""
+    """fp64 values of signed int8 codes."""
     c = np.asarray(codes)
     if c.dtype == np.uint8:
-        c = c.view(np.int8)
+        raise TypeError("decode takes signed codes; stored bytes go through from_bytes first")
     return c.astype(np.float64)
+
+
+def to_bytes(codes: np.ndarray) -> np.ndarray:
+    """Signed codes in [-127, 127] -> stored bytes (code + 128)."""
+    return (np.asarray(codes).astype(np.int16) + 128).astype(np.uint8)
+
+
+def from_bytes(data: np.ndarray) -> np.ndarray:
+    """Stored bytes -> signed codes (byte - 128)."""
+    return (np.asarray(data, dtype=np.uint8).astype(np.int16) - 128).astype(np.int8)

@@ -336,8 +336,8 @@ def _dt(x) -> int:
     if isinstance(x, str):
         return DTYPE_NAMES[x]
     import torch
-    m = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.uint8: PKV_FP8_E4M3, torch.float32: PKV_F32,
-         torch.int8: PKV_INT8}
+    # INT8 caches hold uint8 bytes (code + 128): name them ("int8"), a uint8 tensor reads as FP8 E4M3
+    m = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.uint8: PKV_FP8_E4M3, torch.float32: PKV_F32}
     if hasattr(torch, "float8_e4m3fn"):
         m[torch.float8_e4m3fn] = PKV_FP8_E4M3
     if hasattr(torch, "float8_e5m2"):

@@ -64,9 +64,10 @@ __device__ __forceinline__ float code_range() {
 
 // Four codes (byte 0 first) -> two f16x2 words (codes 0, 1 and codes 2, 3).
 // Exact for all three types: every E4M3 / E5M2 value and every integer in
-// [-128, 127] is a binary16 number.  INT8 goes through the biased-exponent
-// identity: the binary16 word 0x6400 | (x ^ 0x80) is 1152 + x, so one
-// f16x2 subtraction of 1152 recovers x exactly.
+// [-128, 127] is a binary16 number.  INT8 codes x are stored as the byte
+// x + 128 and go through the biased-exponent identity: the binary16 word
+// 0x6400 | (x + 128) is 1152 + x, so one f16x2 subtraction of 1152 recovers
+// x exactly.
 template <int DT>
 __device__ __forceinline__ void code4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
   static_assert(is_code8(DT), "one-byte cache type");
@@ -81,22 +82,20 @@ __device__ __forceinline__ void code4_to_f16x2(uint32_t w, uint32_t &lo, uint32_
         : "=r"(lo), "=r"(hi)
         : "r"(w));
   } else {
-    const uint32_t u = w ^ 0x80808080u;
     uint32_t a, b;
-    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
-    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(w), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(w), "r"(0x64646464u));
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
   }
 }
 
 // Biased form of code4_to_f16x2 for INT8, for MMA operands whose bias the
-// caller removes itself: the binary16 words 0x6400 | (x ^ 0x80), whose values
-// are 1152 + x exactly (no subtraction).
+// caller removes itself: the binary16 words 0x6400 | (x + 128), whose values
+// are 1152 + x exactly (two byte permutes, no subtraction).
 __device__ __forceinline__ void int8x4_to_f16x2_biased(uint32_t w, uint32_t &lo, uint32_t &hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(w), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(w), "r"(0x64646464u));
 }
 constexpr float kInt8Bias = 1152.f;
 
@@ -174,10 +173,10 @@ __device__ __forceinline__ uint32_t encode2(float a, float b) {
     return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   } else if constexpr (DT == PKV_FP8_E5M2) {
     return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E5M2);
-  } else {
+  } else {  // INT8: code in [-127, 127], stored as the byte code + 128
     const int ia = min(max(__float2int_rn(a), -127), 127);
     const int ib = min(max(__float2int_rn(b), -127), 127);
-    return (static_cast<uint32_t>(ia) & 0xffu) | ((static_cast<uint32_t>(ib) & 0xffu) << 8);
+    return static_cast<uint32_t>(ia + 128) | (static_cast<uint32_t>(ib + 128) << 8);
   }
 }
 

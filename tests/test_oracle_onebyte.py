@@ -78,7 +78,19 @@ def test_int8_rounding_and_clamp():
     y = np.array([0.0, 0.49, 0.5, 1.5, 2.5, -2.5, -3.5, 126.5, 127.4, 128.0, -200.0, 7.0], dtype=np.float32)
     assert int8.encode(y).tolist() == [0, 0, 0, 2, 2, -2, -4, 126, 127, 127, -127, 7]
     assert int8.decode(np.array([-127, 0, 127], dtype=np.int8)).tolist() == [-127.0, 0.0, 127.0]
-    assert int8.decode(np.array([0x81, 0x7F], dtype=np.uint8)).tolist() == [-127.0, 127.0]
+
+
+def test_int8_storage_bytes():
+    # stored byte = code + 128: codes -127..127 take bytes 1..255, zero is 0x80
+    codes = np.arange(-127, 128, dtype=np.int8)
+    b = int8.to_bytes(codes)
+    assert b.dtype == np.uint8 and b.tolist() == list(range(1, 256))
+    assert int8.to_bytes(np.array([-127, -1, 0, 1, 127], dtype=np.int8)).tolist() == [0x01, 0x7F, 0x80, 0x81, 0xFF]
+    assert np.array_equal(int8.from_bytes(b), codes)
+    # the cache's decoder reads stored bytes
+    assert CODE_TYPES["int8"][2](np.array([0x01, 0x80, 0xFF], dtype=np.uint8)).tolist() == [-127.0, 0.0, 127.0]
+    with pytest.raises(TypeError):
+        int8.decode(np.array([0x81], dtype=np.uint8))
 
 
 @pytest.mark.parametrize("dtype", ["int8", "fp8_e5m2", "fp8_e4m3"])
@@ -100,7 +112,7 @@ def test_int8_error_bound_and_zero_rows():
     x = rng.standard_normal((300, 64)).astype(np.float32)
     x[7] = 0.0
     codes, s = quantize_rows(x, "int8")
-    assert s[7] == 1.0 and not codes[7].any()
+    assert s[7] == 1.0 and not int8.from_bytes(codes[7]).any()
     err = np.abs(dequantize_rows(x, "int8") - x.astype(np.float64))
     # half a step of the scale, plus the fp32 rounding of the quotient
     assert np.all(err <= s.astype(np.float64)[:, None] * (0.5 + 1e-5))
