@@ -52,22 +52,22 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu capture), keyed by workload and by the hash of the decode kernel source it
 # was taken on; reported only while the source is unchanged.
 NCU_TRAFFIC = {
-    # decode kernel source ceb09f92f4acb56f: tensor-core kernel with the step's append fused in, 16-warp
-    # CTAs for one-byte caches, biased INT8 / 4-bit MMA operands, K and V scales of a tile in one
+    # decode kernel source 35280b6bc0d3afb8: tensor-core kernel with the step's append fused in, 16-warp
+    # CTAs for one-byte caches, biased INT8 (stored code + 128) / 4-bit MMA operands, K and V scales of a tile in one
     # 128-byte unit, first cache copies before the programmatic wait behind kernels that write no cache,
     # cascade with the mma.sync prefix kernel, approximate softmax exponentials for 4-bit V; default "auto" variants.
     # dram__bytes_read.sum + dram__bytes_write.sum of one call (the fifth decode call of a --steps 4
     # --warmup 3 run; prefix-share: its prefix kernel plus its decode, whose DRAM reads include the
     # prefix partials ncu's replay flushed from L2)
-    ("llama3-8b", "ceb09f92f4acb56f"): 145_822_464,
-    ("llama3-8b:bs32", "ceb09f92f4acb56f"): 145_796_608,
-    ("mha7b-40layer", "ceb09f92f4acb56f"): 271_591_168,
-    ("prefix-share", "ceb09f92f4acb56f"): 52_896_512,
-    ("long-fp8", "ceb09f92f4acb56f"): 796_569_856,
-    ("long-fp8:fp8_e5m2", "ceb09f92f4acb56f"): 796_798_720,
-    ("long-fp8:int8", "ceb09f92f4acb56f"): 796_795_136,
-    ("long-fp8:fp8_e4m3_int4", "ceb09f92f4acb56f"): 604_398_080,
-    ("long-fp8:bs32", "ceb09f92f4acb56f"): 797_221_888,
+    ("llama3-8b", "35280b6bc0d3afb8"): 145_818_368,
+    ("llama3-8b:bs32", "35280b6bc0d3afb8"): 145_939_968,
+    ("mha7b-40layer", "35280b6bc0d3afb8"): 271_543_808,
+    ("prefix-share", "35280b6bc0d3afb8"): 52_880_128,
+    ("long-fp8", "35280b6bc0d3afb8"): 796_624_384,
+    ("long-fp8:fp8_e5m2", "35280b6bc0d3afb8"): 796_783_104,
+    ("long-fp8:int8", "35280b6bc0d3afb8"): 796_804_864,
+    ("long-fp8:fp8_e4m3_int4", "35280b6bc0d3afb8"): 604_555_008,
+    ("long-fp8:bs32", "35280b6bc0d3afb8"): 797_113_344,
 }
 
 
