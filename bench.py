@@ -22,6 +22,8 @@ same workload instead (bounded samples per step).
 from __future__ import annotations
 
 import argparse
+import contextlib
+import gc
 import hashlib
 import json
 import os
@@ -69,6 +71,20 @@ NCU_TRAFFIC = {
     ("long-fp8:fp8_e4m3_int4", "35280b6bc0d3afb8"): 604_555_008,
     ("long-fp8:bs32", "35280b6bc0d3afb8"): 797_113_344,
 }
+
+
+@contextlib.contextmanager
+def no_gc():
+    """Python's cyclic garbage collector off inside a timed region (as timeit does), so a
+    collection pass of the host interpreter does not land in a step's time."""
+    gc.collect()
+    was = gc.isenabled()
+    gc.disable()
+    try:
+        yield
+    finally:
+        if was:
+            gc.enable()
 
 
 def kernel_hash() -> str:
@@ -339,13 +355,14 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     launches0 = capi.pkv_launch_count()
     clocks.mark("t0")
-    for i in range(args.steps):
-        k, v, q = feed(args.warmup + i)
-        scrub(i + 7)
-        ev[i][0].record(stream)
-        cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    with no_gc():
+        for i in range(args.steps):
+            k, v, q = feed(args.warmup + i)
+            scrub(i + 7)
+            ev[i][0].record(stream)
+            cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
     clocks.mark("t1")
     if world > 1:
         torch.distributed.barrier()
@@ -364,11 +381,12 @@ def run_ours(args, world, rank, local):
     # two extra events per step stay out of the step timing above)
     marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(attn_steps)]
     first_attn = args.warmup + args.steps
-    for i in range(attn_steps):
-        k, v, q = feed(first_attn + i)
-        scrub(i + 3)
-        cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out, marks=marks[i])
-    torch.cuda.synchronize()
+    with no_gc():
+        for i in range(attn_steps):
+            k, v, q = feed(first_attn + i)
+            scrub(i + 3)
+            cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out, marks=marks[i])
+        torch.cuda.synchronize()
     attn_ms = [a.elapsed_time(b) for a, b in marks]
     assert cache.check() == 0
 
@@ -499,14 +517,8 @@ def run_e2e(w, cache, steps, first_step, dev, scrub, warmup=3):
     first_step += warmup
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize()
-    meta_bytes = 0
-    for i, (k, v, q) in enumerate(hosts):
-        scrub(i)
-        ev[i][0].record(stream)
-        # host tensors in, host tensor out: the step copies the inputs in with one kernel, and the
-        # decode stores the output straight into the page-locked host tensor
-        cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out_h)
-        ev[i][1].record(stream)
+    with no_gc():
+        _e2e_steps(w, cache, hosts, ev, stream, scrub, out_h)
     torch.cuda.synchronize()
     assert cache.check() == 0
     t = sum(a.elapsed_time(b) for a, b in ev) / 1e3
@@ -518,6 +530,17 @@ def run_e2e(w, cache, steps, first_step, dev, scrub, warmup=3):
     return {"value": round(kv / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()), "steps": steps,
             "ms_per_step": round(t * 1e3 / steps, 4)}
+
+
+def _e2e_steps(w, cache, hosts, ev, stream, scrub, out_h):
+    """The timed host-buffer steps of run_e2e (CUDA events around each step)."""
+    for i, (k, v, q) in enumerate(hosts):
+        scrub(i)
+        ev[i][0].record(stream)
+        # host tensors in, host tensor out: the step copies the inputs in with one kernel, and the
+        # decode stores the output straight into the page-locked host tensor
+        cache.step(w.seq_ids, k, v, q, scale=w.scale, out=out_h)
+        ev[i][1].record(stream)
 
 
 # ---------------------------------------------------------------------------
