@@ -527,9 +527,12 @@ def run_e2e(w, cache, steps, first_step, dev, scrub, warmup=3):
     max_blocks = int(max(-(-int(L) // w.block_size) for L in lens))
     meta_bytes = 4 * (w.num_seqs + w.num_seqs * max_blocks + w.num_seqs)
     h2d = sum(x.numel() * x.element_size() for x in hosts[0]) + meta_bytes
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     return {"value": round(kv / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()), "steps": steps,
-            "ms_per_step": round(t * 1e3 / steps, 4)}
+            "ms_per_step": round(t * 1e3 / steps, 4),
+            "step_ms_percentiles": {f"p{q}": round(float(np.percentile(step_ms, q)), 4) for q in (10, 50, 90)},
+            "step_ms_max": round(max(step_ms), 4)}
 
 
 def _e2e_steps(w, cache, hosts, ev, stream, scrub, out_h):
