@@ -76,8 +76,8 @@ NCU_TRAFFIC = {
 @contextlib.contextmanager
 def no_gc():
     """Python's cyclic garbage collector off inside a timed region (as timeit does), so a
-    collection pass of the host interpreter does not land in a step's time."""
-    gc.collect()
+    collection pass of the host interpreter does not land in a step's time.  (No collection
+    on entry: a full pass right before the first timed step left that step's host work slow.)"""
     was = gc.isenabled()
     gc.disable()
     try:
@@ -340,6 +340,11 @@ def run_ours(args, world, rank, local):
             dst.copy_(src)
         return static
 
+    # the clock sampler starts before the warm-up steps: its start-up (a subprocess and a pause
+    # for its first samples) left the host slow for the first timed step when it came just before
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for s in range(args.warmup):
         k, v, q = feed(s)
         scrub(s)
@@ -347,9 +352,6 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     assert cache.check() == 0
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
